@@ -1,0 +1,448 @@
+"""Benchmark of one DDTree verification round (build + tree attention + tree GDN + walk +
+commit) on the batched workload: 32 requests, drafter depth 15, vocabulary 151936,
+budget 64, prefixes ~ U[1024, 32768], 16 full-attention layers (Hq 24, Hkv 4, d 256) and
+48 GDN layers (Hk 16, Hv 48, dk = dv = 128), bf16 data, fp32 state.
+
+Prints ONE JSON line (rank 0).  `value` = drafted tree nodes verified per second over
+the whole job (all ranks), with every input resident in HBM; `e2e` is the same metric
+with each round's inputs copied from pinned host memory and its emitted tokens copied
+back inside the timed region.  `--impl reference` times the plain CPU oracle instead.
+
+Multi-GPU: requests are independent, so N ranks run N independent replicas of the
+workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "verified tree nodes/sec per round at 1 GB300; achieved HBM GB/s vs peak"
+UNIT = "nodes/s"
+WORKLOAD = 5
+KERNELS = ("build", "attn", "gdn", "walk", "commit")
+
+
+# ---------------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_max(x, world, dev):
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def all_sum(x, world, dev):
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken during the timed region."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader",
+                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, uuid):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10 or (uuid and f[1] != uuid):
+                continue
+            try:
+                sm.append(float(f[2].split()[0]))
+                mx.append(float(f[3].split()[0]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_uuid():
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------- accounting
+def attn_flops_bytes(r):
+    """Algorithmic work of one ddt_tree_attn launch: 4*d flops per (query row, visible
+    key); bytes = prefix K/V once per (layer, request, kv head) + tree K/V + q + o."""
+    c = r.cfg
+    depth = r.tree["depth"].cpu().numpy()
+    nn = r.tree["n_nodes"].cpu().numpy()
+    P = r.prefix0.cpu().numpy().astype(np.float64)
+    keys = 0.0
+    for b in range(len(nn)):
+        keys += float(nn[b]) * P[b] + float((depth[b, :nn[b]] + 1).sum())
+    flops = 4.0 * c["d"] * c["Hq"] * r.Lf * keys
+    esz = 2 if c["dtype"] == torch.bfloat16 else 4
+    bytes_ = r.Lf * c["Hkv"] * c["d"] * esz * 2 * float(P.sum())
+    bytes_ += r.Lf * float(nn.sum()) * c["d"] * esz * (2 * c["Hkv"] + c["Hq"] + c["Hq"])
+    return flops, bytes_
+
+
+def round_bytes(r):
+    """Algorithmic HBM bytes of the whole round (read + write once)."""
+    c = r.cfg
+    esz = 2 if c["dtype"] == torch.bfloat16 else 4
+    B, D, V, N = c["B"], c["D"], c["V"], r.N
+    total = B * D * V * esz + B * N * V * esz                     # drafter + target logits
+    if r.Lf:
+        total += attn_flops_bytes(r)[1]
+        total += 2 * r.Lf * B * (D + 1) * c["Hkv"] * c["d"] * esz  # commit: copied KV rows (upper bound)
+    if r.Lg:
+        C = 2 * c["Hk"] * c["dk"] + c["Hv"] * c["dv"]
+        S = r.Lg * B * c["Hv"] * c["dk"] * c["dv"] * 4
+        total += S + r.Lg * B * N * C * esz + r.Lg * B * N * c["Hv"] * c["dv"] * esz  # tree GDN
+        total += 2 * S                                                             # commit of the state
+    return float(total)
+
+
+# --------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    from tree_speculative_decoding_02_gb300 import ddt, synth
+    from tree_speculative_decoding_02_gb300.round import Round
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ddt.load()
+    cfg = dict(synth.WORKLOADS[args.workload])
+    r = Round(cfg, device=dev, workload=args.workload)
+    st = torch.cuda.current_stream()
+    ev = {k: [] for k in KERNELS}
+
+    # split the five calls so each can be bracketed by events on the launching stream
+    def step(timed):
+        r.restore_prefix()
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if timed else None
+        if timed:
+            marks[0].record(st)
+        c = r.cfg
+        ddt.ddt_build_tree(r.draft_logits, r.root_token, r.prefix_len, c["top_k"], c["budget"], out=r.tree,
+                           workspace=r.build_ws)
+        if timed:
+            marks[1].record(st)
+        a = r.attn
+        ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, r.prefix_len, r.tree["n_nodes"],
+                          r.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out=r.attn_o, status=r.attn_status,
+                          workspace=r.attn_ws)
+        if timed:
+            marks[2].record(st)
+        g = r.gdn
+        ddt.ddt_tree_gdn(g.x, g.conv_w, g.conv_state, g.beta, g.decay, g.S, r.tree["parent"], r.tree["n_nodes"],
+                         Hk=c["Hk"], out=r.gdn_o, status=r.gdn_status)
+        if timed:
+            marks[3].record(st)
+        ddt.ddt_walk_accept(r.tree["token"], r.tree["parent"], r.tree["n_nodes"], r.A - 1,
+                            target_logits=r.target_logits, out=r.walk, workspace=r.walk_ws)
+        if timed:
+            marks[4].record(st)
+        ddt.ddt_commit(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, out=r.commit, k_tree=a.k_tree,
+                       v_tree=a.v_tree, k_cache=a.k_cache, v_cache=a.v_cache, x=g.x, conv_w=g.conv_w, beta=g.beta,
+                       decay=g.decay, S=g.S, conv_state=g.conv_state, Hk=c["Hk"])
+        if timed:
+            marks[5].record(st)
+            for i, k in enumerate(KERNELS):
+                ev[k].append((marks[i], marks[i + 1]))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    nodes_per_step = r.drafted_nodes()
+    for k in ("status",):
+        bad = int((r.tree[k] != 0).sum())
+        if bad:
+            raise RuntimeError(f"build reported {bad} request errors")
+
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv")) if rank == 0 else None
+    if clocks and os.path.isdir(os.path.join(ROOT, "gpurun_out")):
+        clocks.start()
+    elif clocks:
+        clocks = None
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(st)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = t0.elapsed_time(t1)
+    clk = clocks.stop(gpu_uuid()) if clocks else None
+    ms_max = all_max(ms, world, dev)
+    nodes_total = all_sum(nodes_per_step * args.steps, world, dev)
+    value = nodes_total / (ms_max / 1e3)
+    per_kernel = {k: statistics.mean(a.elapsed_time(b) for a, b in ev[k]) for k in KERNELS}
+
+    # end to end through the public API: per-round inputs from pinned host memory,
+    # emitted tokens back to the host, inside the timed region
+    ins = r.round_inputs()
+    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in ins.items()}
+    for k, v in ins.items():
+        host[k].copy_(v)
+    outs = r.round_outputs()
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k, v in ins.items():
+            v.copy_(host[k], non_blocking=True)
+        r.restore_prefix()
+        r.step()
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n_e2e = max(2, min(args.steps, 5))
+    e0.record(st)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    e_ms = all_max(e0.elapsed_time(e1), world, dev)
+    e2e_value = all_sum(nodes_per_step * n_e2e, world, dev) / (e_ms / 1e3)
+
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    tc_peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    fl, by = attn_flops_bytes(r)
+    attn_ms = per_kernel["attn"]
+    tflops = fl / (attn_ms / 1e3) / 1e12
+    rb = round_bytes(r)
+    step_ms = ms / args.steps
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "batched-round-bf16: B=32, D=15, V=151936, budget 64, top-k 8, "
+                               "P~U[1024,32768], 16 attn layers Hq24/Hkv4/d256, 48 GDN layers Hk16/Hv48/dk=dv=128",
+                   "B": cfg["B"], "budget": cfg["budget"], "nodes_per_round": nodes_per_step,
+                   "prefix_total": int(r.prefix0.sum()),
+                   "l2": "inputs larger than L2 (tens of GB per round)", "parallelism": f"replicas x{world}"},
+        "hbm_gbs_round": rb / (step_ms / 1e3) / 1e9,
+        "hbm_frac_round": rb / (step_ms / 1e3) / 1e9 / hbm_peak,
+        "per_kernel_ms": per_kernel,
+        "roofline": {"bound": "tensor", "kernel": "ddt_tree_attn", "achieved": tflops, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": tflops / tc_peak, "traffic": None,
+                     "algorithmic_flops": fl, "algorithmic_bytes": by, "peak_note": "of measured (sustained)"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 10 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(r, seconds=args.cpu_seconds)
+    return out
+
+
+# ------------------------------------------------------------- oracle (CPU) timing
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def request_from_round(r, b):
+    """One request's inputs of a GPU Round, as fp64 host arrays for the oracle."""
+    P = int(r.prefix0[b])
+    a, g = r.attn, r.gdn
+    return {"P": P, "draft_logits": _f64(r.draft_logits[b:b + 1]), "root": r.root_token[b:b + 1].cpu().numpy(),
+            "target_logits": _f64(r.target_logits[b:b + 1]), "q": _f64(a.q[:, b:b + 1]),
+            "k_tree": _f64(a.k_tree[:, b:b + 1]), "v_tree": _f64(a.v_tree[:, b:b + 1]),
+            "k_cache": _f64(a.k_cache[:, b:b + 1, :, :P]), "v_cache": _f64(a.v_cache[:, b:b + 1, :, :P]),
+            "x": _f64(g.x[:, b:b + 1]), "conv_w": _f64(g.conv_w), "conv_state": _f64(g.conv_state[:, b:b + 1]),
+            "beta": _f64(g.beta[:, b:b + 1]), "decay": _f64(g.decay[:, b:b + 1]),
+            "S": np.swapaxes(_f64(g.S[:, b:b + 1]), -1, -2)}
+
+
+def request_synth(cfg, b, workload):
+    """One request of the workload drawn directly with the synth module (B = 1), for the
+    reference arm, which must not touch the CUDA library."""
+    from tree_speculative_decoding_02_gb300 import synth
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = 100 * workload + b
+    P = int(synth.prefix_lengths(cfg["B"], cfg["P_lo"], cfg["P_hi"], g=synth.gen(workload, 2))[b])
+    N = cfg["budget"] + 1
+    dt = cfg["dtype"]
+    a = synth.attn_inputs(cfg["Lf"], 1, N, cfg["Hq"], cfg["Hkv"], cfg["d"], P, [P], workload=wl, dtype=dt,
+                          device=dev, poison=False)
+    g = synth.gdn_inputs(cfg["Lg"], 1, N, cfg["Hk"], cfg["Hv"], cfg["dk"], cfg["dv"], cfg["conv_k"], workload=wl,
+                         dtype=dt, device=dev)
+    return {"P": P, "draft_logits": _f64(synth.draft_logits(1, cfg["D"], cfg["V"], std=cfg["logit_std"],
+                                                           boost=cfg["boost"], g=synth.gen(wl, 1), dtype=dt)),
+            "root": np.array([b], np.int32),
+            "target_logits": _f64(synth.target_logits(1, N, cfg["V"], g=synth.gen(wl, 30), dtype=dt)),
+            "q": _f64(a.q), "k_tree": _f64(a.k_tree), "v_tree": _f64(a.v_tree), "k_cache": _f64(a.k_cache),
+            "v_cache": _f64(a.v_cache), "x": _f64(g.x), "conv_w": _f64(g.conv_w), "conv_state": _f64(g.conv_state),
+            "beta": _f64(g.beta), "decay": _f64(g.decay), "S": _f64(g.S)}
+
+
+def oracle_round(cfg, q):
+    """One request's full round (build, attention, GDN, walk, commit) through the plain
+    oracle; returns (drafted nodes, seconds spent in the oracle)."""
+    import oracle
+
+    t = time.perf_counter()
+    P = q["P"]
+    tree = oracle.build_tree(q["draft_logits"], q["root"], [P], cfg["top_k"], cfg["budget"])
+    oracle.tree_attn(q["q"], q["k_tree"], q["v_tree"], q["k_cache"], q["v_cache"], [P], tree["n_nodes"],
+                     tree["anc"], 1.0 / math.sqrt(cfg["d"]))
+    oracle.tree_gdn(q["x"], q["conv_w"], q["conv_state"], q["beta"], q["decay"], q["S"], tree["parent"],
+                    tree["n_nodes"], cfg["Hk"])
+    wk = oracle.walk(tree["token"], tree["parent"], tree["n_nodes"], cfg["D"], target_logits=q["target_logits"])
+    pad = ((0, 0), (0, 0), (0, 0), (0, cfg["D"] + 1), (0, 0))
+    oracle.commit(wk["acc_nodes"], wk["acc_len"], [P], k_tree=q["k_tree"], v_tree=q["v_tree"],
+                  k_cache=np.pad(q["k_cache"], pad), v_cache=np.pad(q["v_cache"], pad), x=q["x"],
+                  conv_w=q["conv_w"], beta=q["beta"], decay=q["decay"], S=q["S"], conv_state=q["conv_state"],
+                  Hk=cfg["Hk"])
+    return int(tree["n_nodes"][0]) - 1, time.perf_counter() - t
+
+
+def cpu_baseline(r, seconds=15.0, max_requests=8):
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    oracle.build()
+    nodes, t_oracle, done = 0, 0.0, []
+    for b in range(min(max_requests, r.cfg["B"])):
+        n, t = oracle_round(r.cfg, request_from_round(r, b))
+        nodes += n
+        t_oracle += t
+        done.append(b)
+        if t_oracle >= seconds:
+            break
+    return {"value": nodes / t_oracle, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"full round (build, 16-layer tree attention, 48-layer tree GDN, walk, commit) of "
+                      f"requests {done} of the batched workload, fp64, {t_oracle:.1f} s of oracle time"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the plain CPU oracle, one request's full round per step."""
+    if rank != 0:
+        return None
+    import oracle
+    from tree_speculative_decoding_02_gb300 import synth
+
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    oracle.build()
+    cfg = dict(synth.WORKLOADS[args.workload])
+    for i in range(args.warmup):
+        oracle_round(cfg, request_synth(cfg, i % cfg["B"], args.workload))
+    nodes, el = 0, 0.0
+    for i in range(args.steps):
+        n, t = oracle_round(cfg, request_synth(cfg, (args.warmup + i) % cfg["B"], args.workload))
+        nodes += n
+        el += t
+    v = nodes / el
+    return {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "batched-round-bf16, one request's full round per step", "B": 1,
+                       "budget": cfg["budget"]},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one request's full round per step (oracle time only)"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

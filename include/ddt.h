@@ -1,0 +1,217 @@
+/*
+ * ddt.h -- C ABI of the GB300 (sm_103a) DDTree verification-round library.
+ *
+ * One verification round of DDTree tree-speculative decoding for a hybrid target
+ * made of full-attention and Gated DeltaNet (GDN) layers, as five stream-ordered
+ * calls:
+ *
+ *   ddt_build_tree   best-first draft tree from the drafter's per-depth logits
+ *   ddt_tree_attn    tree attention: prefix KV + own ancestors, never siblings
+ *   ddt_tree_gdn     branch-local gated delta rule + short conv, scratch-only state
+ *   ddt_walk_accept  greedy tree walk against the target's argmax
+ *   ddt_commit       copy only the accepted path's KV / recurrent state
+ *
+ * Sources (web pages; no code is printed on them):
+ *   [NOTES] "DDTree on vLLM: candid research notes on tree speculation for Qwen3.6"
+ *           -- "Why a tree instead of a chain", "Why hybrid attention makes it hard",
+ *           "What broke along the way", "Where the next step is".
+ *   [ARCH]  "From Tree-Based Speculative Decoding to Drafter Training: A Research Pivot
+ *           in the DDTree Investigation" -- "The Architecture of DDTree: Tree
+ *           Construction and Verification".
+ *   [CHALL] "The Architecture of Speculation: Bridging DFlash and DDTree for Production
+ *           Inference" -- "The DDTree Integration Challenge".
+ *   [GDN]   Yang, Kautz, Hatamizadeh, "Gated Delta Networks" (ICLR 2025): the gated
+ *           delta rule, which the pages name but do not print.
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers, contiguous, C row-major with the
+ *     shapes given below (outermost first).  The caller owns and allocates every
+ *     buffer, including workspaces; the library allocates no device memory and keeps
+ *     no global state.  Calls are thread-safe.
+ *   - Work is enqueued on `stream`; nothing synchronises the host.  Results and the
+ *     per-request `status` words are valid once the stream has reached the call.
+ *   - Argument errors found on the host (null pointers, unsupported sizes, short
+ *     workspace) return an error before anything is launched.  Data errors found on
+ *     the device (non-finite logits, malformed trees, cache overflow) are written to
+ *     `status[b]` as a ddt_status code, per request; kernels never trap.
+ *   - N = budget + 1 tree rows per request.  Row 0 is the root (the last emitted
+ *     token, not yet in the cache); rows 1..n_nodes[b]-1 are drafted nodes numbered
+ *     breadth first (depth, then parent row, then rank), so every parent row is
+ *     smaller than its children's.  Rows >= n_nodes[b] are padding.
+ *   - W = ceil(N / 32) mask words per row.
+ */
+#ifndef DDT_H
+#define DDT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ddt_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    DDT_OK = 0,
+    DDT_ERR_INVALID_ARG = 1, /* null pointer, bad size, short workspace */
+    DDT_ERR_UNSUPPORTED = 2, /* size/dtype combination not compiled in */
+    DDT_ERR_CAPACITY = 3,    /* prefix_len + committed rows would exceed the cache */
+    DDT_ERR_CUDA = 4,        /* a launch failed; see cudaGetLastError semantics */
+    DDT_ERR_TIMEOUT = 5,     /* reserved: a bounded device wait gave up */
+    DDT_ERR_NONFINITE = 6,   /* NaN or +-Inf logits */
+    DDT_ERR_TREE = 7         /* malformed tree arrays (parent >= child, bad token) */
+} ddt_status;
+
+typedef enum { DDT_F32 = 0, DDT_BF16 = 1 } ddt_dtype;
+
+/* Text of a status code (static storage). */
+const char* ddt_status_string(ddt_status s);
+
+/* Library version, e.g. "ddt 0.1 sm_103a". */
+const char* ddt_version(void);
+
+/* ---------------------------------------------------------------------------------
+ * ddt_build_tree -- [ARCH] best-first tree construction and flattening; [CHALL] 2.
+ *
+ * For each depth d = 1..D of each request: LSE_d = log sum_v exp(logit_d[v]); the
+ * depth's top_k tokens by (logit desc, token id asc).  A node is a path (t_1..t_n)
+ * with t_i among depth i's top_k; its score is log prod_i p_i(t_i) =
+ * sum_i logit_i(t_i) - sum_i LSE_i, each sum formed in fp64 depth 1 first.  The
+ * `budget` nodes taken are those a best-first max-heap pops, seeded with the best
+ * depth-1 token and pushing, per pop, the next-ranked sibling and the best child;
+ * exact score ties go to the lexicographically smaller token path.  If the lattice
+ * holds fewer than `budget` nodes, all of it is taken.
+ *
+ *   draft_logits [B][D][V] (dtype)       root_token [B], prefix_len [B] int32
+ * Outputs (int32 unless noted), padding rows = -1:
+ *   token [B][N], parent [B][N] (root -1), depth [B][N] (root 0),
+ *   position [B][N] = prefix_len[b] + depth, n_nodes [B] (root included),
+ *   anc [B][N][W] uint32: bit j of row i set iff row j is row i or an ancestor of it,
+ *   score [B][N] double (root 0, padding -inf) -- may be NULL,
+ *   status [B]: DDT_OK or DDT_ERR_NONFINITE (then the tree is the root alone).
+ * Limits: 1 <= D <= 64, 1 <= top_k <= min(32, V), 0 <= budget <= 1023.
+ * workspace: ddt_build_tree_workspace(B, D, V, top_k) bytes, 16-byte aligned.
+ * ------------------------------------------------------------------------------- */
+size_t ddt_build_tree_workspace(int B, int D, int V, int top_k);
+ddt_status ddt_build_tree(int B, int D, int V, int top_k, int budget, ddt_dtype dtype,
+                          const void* draft_logits, const int32_t* root_token,
+                          const int32_t* prefix_len, int32_t* token, int32_t* parent,
+                          int32_t* depth, int32_t* position, int32_t* n_nodes, uint32_t* anc,
+                          double* score, int32_t* status, void* workspace, size_t ws_bytes,
+                          ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * ddt_tree_attn -- [NOTES] "Why hybrid attention makes it hard": each tree row attends
+ * to the committed prefix plus its own ancestors (and itself), never its siblings;
+ * [ARCH] the ancestor-only attention mask of the flattened tree.
+ *
+ * For layer l, request b, row i < n_nodes[b], query head h (kv head g = h / (Hq/Hkv)):
+ *   o = softmax(scale * q . K^T) V over keys {k_cache rows 0..prefix_len[b]-1} and
+ *       {k_tree rows j : bit j of anc[b][i]}.
+ * Inputs are taken after any rotary embedding.
+ *   q [L][B][N][Hq][d], k_tree, v_tree [L][B][N][Hkv][d]  (in_dtype)
+ *   k_cache, v_cache [L][B][Hkv][Pcap][d] (in_dtype): only rows < prefix_len[b] are
+ *     read; the rest may hold anything.  Tree rows >= n_nodes[b] are never read.
+ *   prefix_len, n_nodes [B]; anc [B][N][W] as written by ddt_build_tree.
+ *   o [L][B][N][Hq][d] (out_dtype); padding rows are written as zeros.
+ *   status [B]: DDT_ERR_CAPACITY if prefix_len[b] is outside [0, Pcap], DDT_ERR_TREE
+ *     if n_nodes[b] is outside [1, N] (the request's output rows are then zero).
+ * d in {64, 128, 256}; Hq % Hkv == 0; N <= 1024.
+ * workspace: ddt_tree_attn_workspace(...) bytes (split-KV partials), 16-byte aligned.
+ * ------------------------------------------------------------------------------- */
+size_t ddt_tree_attn_workspace(int n_layers, int B, int N, int Hq, int Hkv, int d, int Pcap);
+ddt_status ddt_tree_attn(int n_layers, int B, int N, int Hq, int Hkv, int d, int Pcap,
+                         ddt_dtype in_dtype, ddt_dtype out_dtype, const void* q,
+                         const void* k_tree, const void* v_tree, const void* k_cache,
+                         const void* v_cache, const int32_t* prefix_len, const int32_t* n_nodes,
+                         const uint32_t* anc, float scale, void* o, int32_t* status,
+                         void* workspace, size_t ws_bytes, ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * ddt_tree_gdn -- [NOTES] "Why hybrid attention makes it hard" / "Where the next step
+ * is": each node reads the GDN and conv state of its parent and writes scratch, never
+ * the committed state; [GDN] the gated delta rule.
+ *
+ * Per layer l, request b, value head h (key head g = h / (Hv/Hk)), node n (parent p):
+ *   conv: y[c] = SiLU(sum_j conv_w[c][j] * in_j[c]), j = 0..K-1, in_{K-1} = x_n,
+ *         in_{K-2} = x_p, ... along the node's ancestor path; taps past the root read
+ *         conv_state (row K-2 = newest).
+ *   q^ = y_q / sqrt(|y_q|^2 + 1e-6) / sqrt(dk),  k^ = y_k / sqrt(|y_k|^2 + 1e-6),  v = y_v
+ *   S_n = decay_n * S_p + (beta_n * (v - decay_n * S_p k^)) k^T     (S_root's parent = S)
+ *   o_n = S_n q^
+ * State matrices are stored value-major: S[j][i], j < dv value channel, i < dk key
+ * channel, so o = S q and the update is a rank-one term u k^T.
+ *   x [L][B][N][C] (in_dtype), C = 2*Hk*dk + Hv*dv, channel order q | k | v
+ *   conv_w [L][C][K] (in_dtype), conv_state [L][B][K-1][C] (in_dtype, oldest first)
+ *   beta, decay [L][B][N][Hv] fp32;  S [L][B][Hv][dv][dk] fp32 (read only)
+ *   parent [B][N], n_nodes [B] as written by ddt_build_tree
+ *   o [L][B][N][Hv][dv] (out_dtype); padding rows are zeros.
+ *   status [B]: DDT_ERR_TREE for a malformed parent array (outputs then zero).
+ * Limits: dk, dv in {32, 64, 128}; 1 <= K <= 8; N <= 128; tree depth <= 32.
+ * ------------------------------------------------------------------------------- */
+size_t ddt_tree_gdn_workspace(int n_layers, int B, int N, int Hk, int Hv, int dk, int dv);
+ddt_status ddt_tree_gdn(int n_layers, int B, int N, int Hk, int Hv, int dk, int dv, int conv_k,
+                        ddt_dtype in_dtype, ddt_dtype out_dtype, const void* x,
+                        const void* conv_w, const void* conv_state, const float* beta,
+                        const float* decay, const float* S, const int32_t* parent,
+                        const int32_t* n_nodes, void* o, int32_t* status, void* workspace,
+                        size_t ws_bytes, ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * ddt_walk_accept -- [ARCH] follow_verified_tree; [NOTES] "What broke along the way"
+ * (accepted and emitted tokens are kept apart).
+ *
+ * t_i = argmax_v target_logits[b][i][v] (ties to the lower id).  Starting at the root,
+ * move to the child whose token equals t_cur while one exists.  a = depth reached.
+ *   target_logits [B][N][V] (dtype) or NULL; target_argmax [B][N]: written when
+ *     target_logits is given, read otherwise.
+ *   token, parent, n_nodes as written by ddt_build_tree.
+ * Outputs: acc_nodes [B][A] (rows root, ..., last accepted; -1 pad), acc_len [B] = a,
+ *   bonus [B] = t at the last accepted row (emitted, not an accepted draft),
+ *   emitted [B][A] = tokens of accepted rows 1..a then bonus (-1 pad),
+ *   n_emitted [B] = a + 1, status [B] (DDT_ERR_NONFINITE, DDT_ERR_TREE).
+ * A = max_accept + 1 columns; max_accept >= the tree depth (D).
+ * workspace: ddt_walk_accept_workspace(B, N, V) bytes.
+ * ------------------------------------------------------------------------------- */
+size_t ddt_walk_accept_workspace(int B, int N, int V);
+ddt_status ddt_walk_accept(int B, int N, int V, int max_accept, ddt_dtype dtype,
+                           const void* target_logits, int32_t* target_argmax,
+                           const int32_t* token, const int32_t* parent, const int32_t* n_nodes,
+                           int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
+                           int32_t* emitted, int32_t* n_emitted, int32_t* status,
+                           void* workspace, size_t ws_bytes, ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * ddt_commit -- [NOTES] "Why hybrid attention makes it hard": once a path is accepted,
+ * only that path is copied into the contiguous KV and recurrent buffers; [ARCH] KV
+ * compaction.  In place, per request b with a = acc_len[b], P = prefix_len[b]:
+ *   KV: for every attention layer and kv head, cache row P + j <- tree row
+ *       acc_nodes[b][j], j = 0..a (root first).  The bonus token is not committed.
+ *   GDN: S[l][b][h] <- the state after the last accepted row, i.e. the rule of
+ *       ddt_tree_gdn run along acc_nodes[b][0..a] from the committed state.
+ *   conv_state[l][b] <- the last K-1 rows of [conv_state ; x rows of the path].
+ *   prefix_len[b] <- P + a + 1;  src_row[b][j] = acc_nodes[b][j], dst_pos[b][j] = P + j
+ *   (-1 pad).
+ * If P + a + 1 > Pcap (with attention layers) the request is left untouched and
+ * status[b] = DDT_ERR_CAPACITY.
+ * Attention part: n_attn_layers (may be 0), Hkv, d, Pcap, kv_dtype, k_tree, v_tree
+ *   [La][B][N][Hkv][d], k_cache, v_cache [La][B][Hkv][Pcap][d].
+ * GDN part: n_gdn_layers (may be 0), Hk, Hv, dk, dv, conv_k, x_dtype, x [Lg][B][N][C],
+ *   conv_w [Lg][C][K], beta, decay [Lg][B][N][Hv] fp32, S [Lg][B][Hv][dv][dk] fp32,
+ *   conv_state [Lg][B][K-1][C].
+ * acc_nodes [B][A], acc_len [B] as written by ddt_walk_accept.
+ * ------------------------------------------------------------------------------- */
+ddt_status ddt_commit(int B, int N, int A,
+                      int n_attn_layers, int Hkv, int d, int Pcap, ddt_dtype kv_dtype,
+                      const void* k_tree, const void* v_tree, void* k_cache, void* v_cache,
+                      int n_gdn_layers, int Hk, int Hv, int dk, int dv, int conv_k,
+                      ddt_dtype x_dtype, const void* x, const void* conv_w, const float* beta,
+                      const float* decay, float* S, void* conv_state,
+                      const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len,
+                      int32_t* src_row, int32_t* dst_pos, int32_t* status, ddt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DDT_H */

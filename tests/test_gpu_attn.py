@@ -1,0 +1,100 @@
+"""GPU parity of ddt_tree_attn against the oracle (normwise <= 2e-3 per output row)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import _cases as C
+from tests._parity import TOL, normwise
+from tree_speculative_decoding_02_gb300 import ddt, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(workload, L, B, Hq, Hkv, d, prefix, budget, dtype, Pcap=None, D=6, V=300, k=4):
+    tree, _ = C.tree_from_logits(workload, B, D, V, k, budget, std=2.0, boost=0.0, prefix=prefix)
+    N = budget + 1
+    Pcap = Pcap or (max(prefix) + N + 5)
+    inp = synth.attn_inputs(L, B, N, Hq, Hkv, d, Pcap, np.asarray(prefix), workload=workload, dtype=dtype)
+    return tree, inp, N
+
+
+def _gpu(tree, inp, out_dtype=torch.float32):
+    t = C.tree_to_dev(tree)
+    r = ddt.ddt_tree_attn(inp.q.cuda(), inp.k_tree.cuda(), inp.v_tree.cuda(), inp.k_cache.cuda(),
+                          inp.v_cache.cuda(), inp.prefix_len.cuda(), t["n_nodes"], t["anc"], out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return r
+
+
+def _oracle(tree, inp, d):
+    return oracle.tree_attn(C.f64(inp.q), C.f64(inp.k_tree), C.f64(inp.v_tree),
+                            np.nan_to_num(C.f64(inp.k_cache)), np.nan_to_num(C.f64(inp.v_cache)),
+                            inp.prefix_len.numpy(), tree["n_nodes"], tree["anc"], 1 / math.sqrt(d))["o"]
+
+
+def _check(got, want, tree):
+    got = got.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    for b in range(got.shape[1]):
+        n = int(tree["n_nodes"][b])
+        err = normwise(got[:, b, :n], want[:, b, :n], axes=-1)
+        assert err.max() <= TOL, f"request {b}: max normwise error {err.max():.3g}"
+        assert (got[:, b, n:] == 0).all()
+
+
+def test_attn_tiny_round_fp32():
+    """One layer, Hq=4, Hkv=1, d=64, prefix 256, budget 16, fp32."""
+    tree, inp, N = _case(1, 1, 1, 4, 1, 64, [256], 16, torch.float32, D=8, V=1024, k=8)
+    r = _gpu(tree, inp)
+    _check(r["o"], _oracle(tree, inp, 64), tree)
+    assert int(r["status"][0]) == 0
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_attn_bf16_ragged(d):
+    """bf16, GQA group 6, ragged prefixes (0, 1, 300 rows), NaN-poisoned cache tails."""
+    tree, inp, N = _case(3, 2, 3, 24, 4, d, [0, 1, 300], 64, torch.bfloat16)
+    r = _gpu(tree, inp)
+    _check(r["o"], _oracle(tree, inp, d), tree)
+    rb = _gpu(tree, inp, out_dtype=torch.bfloat16)
+    # bf16 output = fp32 output rounded (within one bf16 ulp)
+    a = r["o"].float()
+    bq = rb["o"].float()
+    ulp = torch.clamp(a.abs(), min=1e-30) * 2.0 ** -7
+    assert ((a - bq).abs() <= ulp).all()
+
+
+def test_attn_no_gqa_and_single_row():
+    tree, inp, N = _case(3, 1, 2, 2, 2, 128, [129, 7], 0, torch.bfloat16)
+    r = _gpu(tree, inp)
+    _check(r["o"], _oracle(tree, inp, 128), tree)
+
+
+def test_attn_bad_prefix_flagged():
+    tree, inp, N = _case(3, 1, 2, 4, 1, 64, [10, 10], 8, torch.float32)
+    inp.prefix_len[1] = inp.k_cache.shape[3] + 1
+    r = _gpu(tree, inp)
+    assert r["status"].cpu().tolist() == [0, 3]
+    assert (r["o"][:, 1] == 0).all()
+
+
+def test_attn_tree_verify_workload_sampled():
+    """Prefix 4096, 16 layers, Hq=24, Hkv=4, d=256, tree of budget 64 from a drafter-vocab
+    build; sampled output rows against the oracle row by row."""
+    tree, _ = C.tree_from_logits(3, 1, 15, 151936, 8, 64, prefix=[4096])
+    N = 65
+    inp = synth.attn_inputs(16, 1, N, 24, 4, 256, 4096 + 16, [4096], workload=3, dtype=torch.bfloat16)
+    r = _gpu(tree, inp)
+    got = r["o"].cpu().double().numpy()
+    rng = np.random.default_rng(0)
+    for _ in range(24):
+        l, i, h = int(rng.integers(16)), int(rng.integers(N)), int(rng.integers(24))
+        g = h // 6
+        want = oracle.attn_row(C.f64(inp.q[l, 0, i, h]), C.f64(inp.k_cache[l, 0, g, :4096]),
+                               C.f64(inp.v_cache[l, 0, g, :4096]), C.f64(inp.k_tree[l, 0, :, g]),
+                               C.f64(inp.v_tree[l, 0, :, g]), tree["anc"][0, i], tree["n_nodes"][0], 1 / 16.0)
+        err = np.abs(got[l, 0, i, h] - want).max() / np.abs(want).max()
+        assert err <= TOL, (l, i, h, err)

@@ -1,0 +1,88 @@
+"""GPU parity of ddt_tree_gdn against the oracle (normwise <= 2e-3 per output row)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import _cases as C
+from tests._parity import TOL, normwise
+from tree_speculative_decoding_02_gb300 import ddt, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(tree, gi, Hk, out_dtype=torch.float32):
+    t = C.tree_to_dev(tree)
+    S_dev = gi.S.transpose(-1, -2).contiguous().cuda()   # [dk][dv] draw -> [dv][dk] layout
+    r = ddt.ddt_tree_gdn(gi.x.cuda(), gi.conv_w.cuda(), gi.conv_state.cuda(), gi.beta.cuda(), gi.decay.cuda(),
+                         S_dev, t["parent"], t["n_nodes"], Hk=Hk, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return r
+
+
+def _check(got, want, tree):
+    got = got.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    for b in range(got.shape[1]):
+        n = int(tree["n_nodes"][b])
+        err = normwise(got[:, b, :n], want[:, b, :n], axes=-1)
+        assert err.max() <= TOL, f"request {b}: max normwise error {err.max():.3g}"
+        assert (got[:, b, n:] == 0).all()
+
+
+def _oracle(tree, gi, Hk):
+    return oracle.tree_gdn(C.f64(gi.x), C.f64(gi.conv_w), C.f64(gi.conv_state), C.f64(gi.beta), C.f64(gi.decay),
+                           C.f64(gi.S), tree["parent"], tree["n_nodes"], Hk)["o"]
+
+
+def test_gdn_tiny_round_fp32():
+    """One GDN layer, Hk=Hv=2, dk=dv=32, conv 4, fp32; budget 16 tree of the tiny round."""
+    tree, _ = C.tree_from_logits(1, 1, 8, 1024, 8, 16, std=2.0, boost=0.0)
+    gi = synth.gdn_inputs(1, 1, 17, 2, 2, 32, 32, 4, workload=1, dtype=torch.float32)
+    r = _gpu(tree, gi, 2)
+    _check(r["o"], _oracle(tree, gi, 2), tree)
+
+
+@pytest.mark.parametrize("dims", [(128, 128), (64, 64), (64, 128)])
+def test_gdn_bf16_multi(dims):
+    dk, dv = dims
+    tree, _ = C.tree_from_logits(4, 2, 15, 3000, 8, 64)
+    gi = synth.gdn_inputs(2, 2, 65, 2, 6, dk, dv, 4, workload=4, dtype=torch.bfloat16)
+    r = _gpu(tree, gi, 2)
+    _check(r["o"], _oracle(tree, gi, 2), tree)
+
+
+def test_gdn_small_trees_and_root_only():
+    tree, _ = C.tree_from_logits(4, 3, 3, 50, 2, 5, std=2.0, boost=0.0)
+    tree0, _ = C.tree_from_logits(4, 3, 3, 50, 2, 0, std=2.0, boost=0.0)
+    for tr in (tree, tree0):
+        N = tr["token"].shape[1]
+        gi = synth.gdn_inputs(1, 3, N, 1, 2, 32, 32, 4, workload=4, dtype=torch.float32)
+        r = _gpu(tr, gi, 1)
+        _check(r["o"], _oracle(tr, gi, 1), tr)
+
+
+def test_gdn_malformed_tree_flagged():
+    tree, _ = C.tree_from_logits(4, 2, 3, 50, 2, 5, std=2.0, boost=0.0)
+    tree["parent"][1][3] = 5   # parent after child
+    gi = synth.gdn_inputs(1, 2, 6, 1, 1, 32, 32, 4, workload=4, dtype=torch.float32)
+    r = _gpu(tree, gi, 1)
+    assert r["status"].cpu().tolist() == [0, 7]
+    assert (r["o"][:, 1] == 0).all()
+
+
+def test_gdn_tree_workload_sampled():
+    """48 layers, Hk=16, Hv=48, dk=dv=128, budget-64 tree from a drafter-vocab build; sampled
+    (layer, value head) units against the oracle."""
+    tree, _ = C.tree_from_logits(4, 1, 15, 151936, 8, 64)
+    gi = synth.gdn_inputs(48, 1, 65, 16, 48, 128, 128, 4, workload=4, dtype=torch.bfloat16)
+    r = _gpu(tree, gi, 16)
+    got = r["o"].cpu().double().numpy()
+    rng = np.random.default_rng(1)
+    for _ in range(8):
+        l, h = int(rng.integers(48)), int(rng.integers(48))
+        u = oracle.gdn_unit(C.f64(gi.x[l, 0]), C.f64(gi.conv_w[l]), C.f64(gi.conv_state[l, 0]),
+                            C.f64(gi.beta[l, 0]), C.f64(gi.decay[l, 0]), C.f64(gi.S[l, 0, h]), tree["parent"][0],
+                            tree["n_nodes"][0], 16, 48, h)
+        err = normwise(got[l, 0, :, h], u["o"], axes=-1)
+        assert err.max() <= TOL, (l, h, err.max())

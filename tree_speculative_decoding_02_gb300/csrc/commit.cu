@@ -1,0 +1,276 @@
+// commit.cu -- ddt_commit: copy only the accepted path into the committed buffers.
+//
+// "DDTree on vLLM: candid research notes", sections "Why hybrid attention makes it hard"
+// and "Where the next step is": once a path is accepted, only that path may be copied
+// back into the contiguous KV and recurrent buffers (an explicit accepted-branch commit
+// with first-class node and parent ids).  "From Tree-Based Speculative Decoding to
+// Drafter Training", section "The Architecture of DDTree": the KV cache is compacted to
+// the accepted path's entries.
+//
+//   k_commit_kv     grid (A, La*Hkv, B): 16-byte vector copy of one tree row into the
+//                   cache at prefix_len + j.
+//   k_commit_gdn    grid (Hv, B, Lg): the committed state (dv x dk fp32) is staged in
+//                   shared memory once, advanced along the accepted path (<= A rank-one
+//                   delta steps) and written back in place: one HBM read and one write.
+//   k_commit_conv   grid (Lg, B): last K-1 raw inputs of [conv state ; path inputs].
+//   k_commit_final  prefix_len, commit indices and status (runs last: the kernels above
+//                   read the old prefix_len).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ddt {
+
+// A request's commit is valid when its accepted path is well formed and fits.
+__device__ __forceinline__ int commit_check(int b, int N, int A, int cap_check, int Pcap,
+                                            const int32_t* acc_nodes, const int32_t* acc_len,
+                                            const int32_t* prefix_len) {
+    const int a = acc_len[b];
+    if (a < 0 || a + 1 > A) return DDT_ERR_INVALID_ARG;
+    for (int j = 0; j <= a; ++j) {
+        const int r = acc_nodes[(long)b * A + j];
+        if (r < 0 || r >= N) return DDT_ERR_TREE;
+    }
+    if (cap_check && (prefix_len[b] < 0 || prefix_len[b] + a + 1 > Pcap)) return DDT_ERR_CAPACITY;
+    return DDT_OK;
+}
+
+template <typename T>
+__global__ void k_commit_kv(int B, int N, int A, int Hkv, int d, int Pcap, int vec, const T* __restrict__ k_tree,
+                            const T* __restrict__ v_tree, T* __restrict__ k_cache, T* __restrict__ v_cache,
+                            const int32_t* __restrict__ acc_nodes, const int32_t* __restrict__ acc_len,
+                            const int32_t* __restrict__ prefix_len) {
+    const int j = blockIdx.x, lg = blockIdx.y, b = blockIdx.z;
+    const int l = lg / Hkv, g = lg % Hkv;
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) s_ok = commit_check(b, N, A, 1, Pcap, acc_nodes, acc_len, prefix_len) == DDT_OK;
+    __syncthreads();
+    if (!s_ok || j > acc_len[b]) return;
+    const int src = acc_nodes[(long)b * A + j];
+    const long lb = (long)l * B + b;
+    const long so = ((lb * N + src) * Hkv + g) * (long)d;
+    const long dof = ((lb * Hkv + g) * (long)Pcap + prefix_len[b] + j) * d;
+    if (vec) {
+        const int nv = d * (int)sizeof(T) / 16;
+        for (int e = threadIdx.x; e < nv; e += blockDim.x) {
+            reinterpret_cast<uint4*>(k_cache + dof)[e] = reinterpret_cast<const uint4*>(k_tree + so)[e];
+            reinterpret_cast<uint4*>(v_cache + dof)[e] = reinterpret_cast<const uint4*>(v_tree + so)[e];
+        }
+    } else {
+        for (int e = threadIdx.x; e < d; e += blockDim.x) {
+            k_cache[dof + e] = k_tree[so + e];
+            v_cache[dof + e] = v_tree[so + e];
+        }
+    }
+}
+
+__device__ __forceinline__ float silu_c(float z) { return z / (1.f + __expf(-z)); }
+
+template <typename Tx, int DK, int DV>
+__global__ void __launch_bounds__(256) k_commit_gdn(int B, int N, int A, int Hk, int Hv, int K, int cap_check,
+                                                     int Pcap, const Tx* __restrict__ x, const Tx* __restrict__ conv_w,
+                                                     const Tx* __restrict__ conv_state,
+                                                     const float* __restrict__ beta, const float* __restrict__ decay,
+                                                     float* __restrict__ S, const int32_t* __restrict__ acc_nodes,
+                                                     const int32_t* __restrict__ acc_len,
+                                                     const int32_t* __restrict__ prefix_len) {
+    extern __shared__ __align__(16) float sS[];  // [DV][DK + 4]
+    __shared__ float s_k[DK], s_v[DV], s_u[DV];
+    __shared__ float s_red[8];
+    __shared__ int s_ok;
+    const int h = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_ok = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len) == DDT_OK;
+    __syncthreads();
+    if (!s_ok) return;
+    const int a = acc_len[b];
+    const int C = 2 * Hk * DK + Hv * DV;
+    const int g = h / (Hv / Hk);
+    const long lb = (long)l * B + b;
+    float* Sg = S + (lb * Hv + h) * (long)DV * DK;
+    for (int e = tid; e < DV * DK / 4; e += 256) {
+        const int r = e / (DK / 4), c4 = e % (DK / 4);
+        *reinterpret_cast<float4*>(sS + r * (DK + 4) + c4 * 4) = reinterpret_cast<const float4*>(Sg)[e];
+    }
+    const int32_t* path = acc_nodes + (long)b * A;
+    const Tx* xb = x + lb * N * C;
+    const Tx* cs = conv_state + lb * (K - 1) * C;
+    const Tx* wl = conv_w + (long)l * C * K;
+    for (int t = 0; t <= a; ++t) {
+        // conv + SiLU of the k and v channels, window along the accepted path
+        for (int e = tid; e < DK + DV; e += 256) {
+            const int c = (e < DK) ? (Hk * DK + g * DK + e) : (2 * Hk * DK + h * DV + e - DK);
+            float acc = 0.f;
+            for (int j = 0; j < K; ++j) {
+                const int back = K - 1 - j;
+                const float in = (back <= t) ? to_f32(xb[(long)path[t - back] * C + c])
+                                             : to_f32(cs[(long)(K - 1 - (back - t)) * C + c]);
+                acc = fmaf(to_f32(wl[(long)c * K + j]), in, acc);
+            }
+            const float y = silu_c(acc);
+            if (e < DK) s_k[e] = y;
+            else s_v[e - DK] = y;
+        }
+        __syncthreads();
+        float part = 0.f;
+        for (int i = tid; i < DK; i += 256) part = fmaf(s_k[i], s_k[i], part);
+        part = warp_sum(part);
+        if (lane == 0) s_red[warp] = part;
+        __syncthreads();
+        float nk = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) nk += s_red[w];
+        const float rk = rsqrtf(nk + 1e-6f);
+        const float at = decay[(lb * N + path[t]) * Hv + h];
+        const float bt = beta[(lb * N + path[t]) * Hv + h];
+        // u = b (v - a S k^)
+        for (int j = tid; j < DV; j += 256) {
+            float pred = 0.f;
+            const float* row = sS + j * (DK + 4);
+            for (int i = 0; i < DK; i += 4) {
+                const float4 s4 = *reinterpret_cast<const float4*>(row + i);
+                pred = fmaf(s4.x, s_k[i], fmaf(s4.y, s_k[i + 1], fmaf(s4.z, s_k[i + 2], fmaf(s4.w, s_k[i + 3], pred))));
+            }
+            s_u[j] = bt * (s_v[j] - at * pred * rk);
+        }
+        __syncthreads();
+        // S <- a S + u k^T
+        for (int e = tid; e < DV * DK; e += 256) {
+            const int j = e / DK, i = e % DK;
+            sS[j * (DK + 4) + i] = fmaf(at, sS[j * (DK + 4) + i], s_u[j] * s_k[i] * rk);
+        }
+        __syncthreads();
+    }
+    for (int e = tid; e < DV * DK / 4; e += 256) {
+        const int r = e / (DK / 4), c4 = e % (DK / 4);
+        reinterpret_cast<float4*>(Sg)[e] = *reinterpret_cast<const float4*>(sS + r * (DK + 4) + c4 * 4);
+    }
+}
+
+template <typename Tx>
+__global__ void k_commit_conv(int B, int N, int A, int C, int K, int cap_check, int Pcap, const Tx* __restrict__ x,
+                              Tx* __restrict__ conv_state, const int32_t* __restrict__ acc_nodes,
+                              const int32_t* __restrict__ acc_len, const int32_t* __restrict__ prefix_len) {
+    const int l = blockIdx.x, b = blockIdx.y;
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) s_ok = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len) == DDT_OK;
+    __syncthreads();
+    if (!s_ok) return;
+    const int n = acc_len[b] + 1;
+    const long lb = (long)l * B + b;
+    Tx* cs = conv_state + lb * (K - 1) * C;
+    const Tx* xb = x + lb * N * C;
+    const int32_t* path = acc_nodes + (long)b * A;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        // new row r = entry r + n of [cs ; path rows]; rows read before they are rewritten
+        for (int r = 0; r < K - 1; ++r) {
+            const int src = r + n;
+            cs[(long)r * C + c] = (src < K - 1) ? cs[(long)src * C + c] : xb[(long)path[src - (K - 1)] * C + c];
+        }
+    }
+}
+
+__global__ void k_commit_final(int B, int N, int A, int cap_check, int Pcap, const int32_t* __restrict__ acc_nodes,
+                               const int32_t* __restrict__ acc_len, int32_t* __restrict__ prefix_len,
+                               int32_t* __restrict__ src_row, int32_t* __restrict__ dst_pos,
+                               int32_t* __restrict__ status) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int st = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len);
+    const int P = prefix_len[b];
+    const int a = acc_len[b];
+    for (int j = 0; j < A; ++j) {
+        const bool on = st == DDT_OK && j <= a;
+        src_row[(long)b * A + j] = on ? acc_nodes[(long)b * A + j] : -1;
+        dst_pos[(long)b * A + j] = on ? P + j : -1;
+    }
+    if (st == DDT_OK) prefix_len[b] = P + a + 1;
+    status[b] = st;
+}
+
+template <typename Tx, int DK, int DV>
+static cudaError_t commit_gdn_go(int B, int N, int A, int Lg, int Hk, int Hv, int K, int cap, int Pcap,
+                                 const void* x, const void* w, const void* cs, const float* beta,
+                                 const float* decay, float* S, const int32_t* an, const int32_t* al,
+                                 const int32_t* pl, cudaStream_t st) {
+    const size_t smem = sizeof(float) * DV * (DK + 4);
+    cudaError_t e = cudaFuncSetAttribute(k_commit_gdn<Tx, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    k_commit_gdn<Tx, DK, DV><<<dim3(Hv, B, Lg), 256, smem, st>>>(
+        B, N, A, Hk, Hv, K, cap, Pcap, static_cast<const Tx*>(x), static_cast<const Tx*>(w),
+        static_cast<const Tx*>(cs), beta, decay, S, an, al, pl);
+    return cudaGetLastError();
+}
+
+template <typename Tx>
+static cudaError_t commit_gdn_dims(int dk, int dv, int B, int N, int A, int Lg, int Hk, int Hv, int K, int cap,
+                                   int Pcap, const void* x, const void* w, const void* cs, const float* beta,
+                                   const float* decay, float* S, const int32_t* an, const int32_t* al,
+                                   const int32_t* pl, cudaStream_t st) {
+#define DDT_CG_CASE(P, Q)                                                                                        \
+    if (dk == P && dv == Q)                                                                                      \
+        return commit_gdn_go<Tx, P, Q>(B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, w, cs, beta, decay, S, an, al, pl, st);
+    DDT_CG_CASE(32, 32)
+    DDT_CG_CASE(64, 64)
+    DDT_CG_CASE(128, 128)
+    DDT_CG_CASE(64, 128)
+    DDT_CG_CASE(128, 64)
+#undef DDT_CG_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap, ddt_dtype kv_dtype,
+                          const void* k_tree, const void* v_tree, void* k_cache, void* v_cache, int Lg, int Hk,
+                          int Hv, int dk, int dv, int K, ddt_dtype x_dtype, const void* x, const void* conv_w,
+                          const float* beta, const float* decay, float* S, void* conv_state,
+                          const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len, int32_t* src_row,
+                          int32_t* dst_pos, int32_t* status, cudaStream_t st) {
+    cudaError_t e;
+    const int cap = La > 0;
+    if (La > 0) {
+        const size_t es = kv_dtype == DDT_BF16 ? 2 : 4;
+        const int vec = ((d * es) % 16 == 0) && (reinterpret_cast<uintptr_t>(k_tree) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(v_tree) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(v_cache) % 16 == 0);
+        dim3 grid(A, La * Hkv, B);
+        if (kv_dtype == DDT_BF16)
+            k_commit_kv<__nv_bfloat16><<<grid, 64, 0, st>>>(
+                B, N, A, Hkv, d, Pcap, vec, static_cast<const __nv_bfloat16*>(k_tree),
+                static_cast<const __nv_bfloat16*>(v_tree), static_cast<__nv_bfloat16*>(k_cache),
+                static_cast<__nv_bfloat16*>(v_cache), acc_nodes, acc_len, prefix_len);
+        else
+            k_commit_kv<float><<<grid, 64, 0, st>>>(B, N, A, Hkv, d, Pcap, vec, static_cast<const float*>(k_tree),
+                                                    static_cast<const float*>(v_tree), static_cast<float*>(k_cache),
+                                                    static_cast<float*>(v_cache), acc_nodes, acc_len, prefix_len);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (Lg > 0) {
+        const int C = 2 * Hk * dk + Hv * dv;
+        if (x_dtype == DDT_BF16) {
+            e = commit_gdn_dims<__nv_bfloat16>(dk, dv, B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, conv_w, conv_state, beta,
+                                               decay, S, acc_nodes, acc_len, prefix_len, st);
+            if (e != cudaSuccess) return e;
+            if (K > 1)
+                k_commit_conv<__nv_bfloat16><<<dim3(Lg, B), 256, 0, st>>>(
+                    B, N, A, C, K, cap, Pcap, static_cast<const __nv_bfloat16*>(x),
+                    static_cast<__nv_bfloat16*>(conv_state), acc_nodes, acc_len, prefix_len);
+        } else {
+            e = commit_gdn_dims<float>(dk, dv, B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, conv_w, conv_state, beta, decay,
+                                       S, acc_nodes, acc_len, prefix_len, st);
+            if (e != cudaSuccess) return e;
+            if (K > 1)
+                k_commit_conv<float><<<dim3(Lg, B), 256, 0, st>>>(B, N, A, C, K, cap, Pcap, static_cast<const float*>(x),
+                                                                  static_cast<float*>(conv_state), acc_nodes, acc_len,
+                                                                  prefix_len);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    k_commit_final<<<(B + 127) / 128, 128, 0, st>>>(B, N, A, cap, Pcap, acc_nodes, acc_len, prefix_len, src_row,
+                                                    dst_pos, status);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt

@@ -1,0 +1,51 @@
+// kernels.h -- internal launchers of the DDTree round library (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ddt.h"
+
+namespace ddt {
+
+constexpr int kBuildChunk = 8192;  // tokens per CTA in the logit passes
+constexpr int kMaxDepth = 64;      // deepest tree the build supports
+constexpr int kMaxTopK = 32;
+constexpr int kMaxBudget = 1023;
+constexpr int kMaxRows = 1024;     // N = budget + 1
+constexpr int kGdnMaxNodes = 128;
+constexpr int kGdnMaxDepth = 32;
+
+size_t build_ws_bytes(int B, int D, int V, int k);
+size_t build_tree_smem(int D, int k, int budget);
+cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype dtype, const void* logits,
+                              const int32_t* root_token, const int32_t* prefix_len, int32_t* token,
+                              int32_t* parent, int32_t* depth, int32_t* position, int32_t* n_nodes,
+                              uint32_t* anc, double* score, int32_t* status, void* ws, cudaStream_t st);
+
+size_t walk_ws_bytes(int B, int N, int V);
+cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void* logits, int32_t* targ,
+                        const int32_t* token, const int32_t* parent, const int32_t* n_nodes, int32_t* acc_nodes,
+                        int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted, int32_t* status,
+                        void* ws, cudaStream_t st);
+
+cudaError_t launch_attn_simt(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype in, ddt_dtype out,
+                             const void* q, const void* k_tree, const void* v_tree, const void* k_cache,
+                             const void* v_cache, const int32_t* prefix_len, const int32_t* n_nodes,
+                             const uint32_t* anc, float scale, void* o, int32_t* status, cudaStream_t st);
+
+size_t gdn_smem_bytes(int N, int dk, int dv);
+cudaError_t launch_gdn_tree(int L, int B, int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in,
+                            ddt_dtype out, const void* x, const void* conv_w, const void* conv_state,
+                            const float* beta, const float* decay, const float* S, const int32_t* parent,
+                            const int32_t* n_nodes, void* o, int32_t* status, cudaStream_t st);
+
+cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap, ddt_dtype kv_dtype,
+                          const void* k_tree, const void* v_tree, void* k_cache, void* v_cache, int Lg, int Hk,
+                          int Hv, int dk, int dv, int K, ddt_dtype x_dtype, const void* x, const void* conv_w,
+                          const float* beta, const float* decay, float* S, void* conv_state,
+                          const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len, int32_t* src_row,
+                          int32_t* dst_pos, int32_t* status, cudaStream_t st);
+
+}  // namespace ddt

@@ -1,0 +1,298 @@
+"""Thin ctypes binding of the libddt.so C ABI (include/ddt.h).
+
+Every function here only checks shapes/dtypes of torch CUDA tensors and passes their
+device pointers, sizes and the current CUDA stream to the C entry point of the same
+name; all of the round's arithmetic runs in the library's CUDA kernels.  There is no
+CPU fallback: without the built library (or without a GPU) every call raises.
+
+Outputs are allocated with torch (PyTorch is the device-memory and stream provider);
+callers that manage memory themselves can pass `out=` dicts of preallocated tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build_ext
+
+F32, BF16 = 0, 1
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "capacity", 4: "cuda", 5: "timeout",
+          6: "non-finite", 7: "malformed tree"}
+
+_lib = None
+_lock = threading.Lock()
+
+_c_int, _c_size, _c_p, _c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+
+_SIGS = {
+    "ddt_status_string": ([_c_int], ctypes.c_char_p),
+    "ddt_version": ([], ctypes.c_char_p),
+    "ddt_build_tree_workspace": ([_c_int] * 4, _c_size),
+    "ddt_build_tree": ([_c_int] * 6 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_tree_attn_workspace": ([_c_int] * 7, _c_size),
+    "ddt_tree_attn": ([_c_int] * 9 + [_c_p] * 8 + [_c_float, _c_p, _c_p, _c_p, _c_size, _c_p], _c_int),
+    "ddt_tree_gdn_workspace": ([_c_int] * 7, _c_size),
+    "ddt_tree_gdn": ([_c_int] * 10 + [_c_p] * 10 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_walk_accept_workspace": ([_c_int] * 3, _c_size),
+    "ddt_walk_accept": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_commit": ([_c_int] * 7 + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13, _c_int),
+}
+EXPORTS = tuple(_SIGS)
+
+
+class DDTError(RuntimeError):
+    pass
+
+
+def lib_path() -> str:
+    return build_ext.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libddt.so (building it first if it is missing or stale and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = build_ext.LIB
+        if build_if_missing and build_ext.is_stale():
+            build_ext.build()
+        if not os.path.exists(path):
+            raise DDTError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _gpu():
+    if not torch.cuda.is_available():
+        raise DDTError("no CUDA device: the DDTree round library runs only on the GPU")
+    return load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise DDTError(f"{what}: {STATUS.get(rc, rc)}")
+
+
+def _need(t, shape, dtype, name):
+    if t is None:
+        raise DDTError(f"{name} is required")
+    if not t.is_cuda or not t.is_contiguous():
+        raise DDTError(f"{name} must be a contiguous CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise DDTError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise DDTError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return t
+
+
+def _ws(nbytes, dev):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=dev)
+
+
+# --------------------------------------------------------------------------- build
+def ddt_build_tree(draft_logits, root_token, prefix_len, top_k: int, budget: int, *, want_score=True,
+                   out=None, workspace=None):
+    """Best-first draft tree.  draft_logits [B][D][V] (fp32/bf16)."""
+    lib = _gpu()
+    B, D, V = draft_logits.shape
+    dev = draft_logits.device
+    _need(draft_logits, (B, D, V), None, "draft_logits")
+    _need(root_token, (B,), torch.int32, "root_token")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    N = budget + 1
+    W = (N + 31) // 32
+    o = out or {}
+    i32 = dict(dtype=torch.int32, device=dev)
+    res = {
+        "token": o.get("token", torch.empty((B, N), **i32)),
+        "parent": o.get("parent", torch.empty((B, N), **i32)),
+        "depth": o.get("depth", torch.empty((B, N), **i32)),
+        "position": o.get("position", torch.empty((B, N), **i32)),
+        "n_nodes": o.get("n_nodes", torch.empty((B,), **i32)),
+        "anc": o.get("anc", torch.empty((B, N, W), dtype=torch.int32, device=dev)),
+        "score": o.get("score", torch.empty((B, N), dtype=torch.float64, device=dev)) if want_score else None,
+        "status": o.get("status", torch.empty((B,), **i32)),
+    }
+    need = lib.ddt_build_tree_workspace(B, D, V, top_k)
+    ws = workspace if workspace is not None else _ws(need, dev)
+    rc = lib.ddt_build_tree(B, D, V, int(top_k), int(budget), _DT[draft_logits.dtype], _ptr(draft_logits),
+                            _ptr(root_token), _ptr(prefix_len), _ptr(res["token"]), _ptr(res["parent"]),
+                            _ptr(res["depth"]), _ptr(res["position"]), _ptr(res["n_nodes"]), _ptr(res["anc"]),
+                            _ptr(res["score"]), _ptr(res["status"]), _ptr(ws), ws.numel(), _stream())
+    _check(rc, "ddt_build_tree")
+    return res
+
+
+# ----------------------------------------------------------------------- attention
+def ddt_tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc, *, scale=None,
+                  out_dtype=None, out=None, status=None, workspace=None):
+    """q [L][B][N][Hq][d]; k/v_tree [L][B][N][Hkv][d]; k/v_cache [L][B][Hkv][Pcap][d]."""
+    lib = _gpu()
+    L, B, N, Hq, d = q.shape
+    Hkv = k_tree.shape[3]
+    Pcap = k_cache.shape[3]
+    dt = q.dtype
+    _need(q, (L, B, N, Hq, d), dt, "q")
+    _need(k_tree, (L, B, N, Hkv, d), dt, "k_tree")
+    _need(v_tree, (L, B, N, Hkv, d), dt, "v_tree")
+    _need(k_cache, (L, B, Hkv, Pcap, d), dt, "k_cache")
+    _need(v_cache, (L, B, Hkv, Pcap, d), dt, "v_cache")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    _need(anc, (B, N, (N + 31) // 32), None, "anc")
+    out_dtype = out_dtype or dt
+    o = out if out is not None else torch.empty((L, B, N, Hq, d), dtype=out_dtype, device=q.device)
+    _need(o, (L, B, N, Hq, d), out_dtype, "o")
+    st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=q.device)
+    scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    need = lib.ddt_tree_attn_workspace(L, B, N, Hq, Hkv, d, Pcap)
+    ws = workspace if workspace is not None else _ws(need, q.device)
+    rc = lib.ddt_tree_attn(L, B, N, Hq, Hkv, d, Pcap, _DT[dt], _DT[out_dtype], _ptr(q), _ptr(k_tree), _ptr(v_tree),
+                           _ptr(k_cache), _ptr(v_cache), _ptr(prefix_len), _ptr(n_nodes), _ptr(anc), scale, _ptr(o),
+                           _ptr(st), _ptr(ws), ws.numel(), _stream())
+    _check(rc, "ddt_tree_attn")
+    return {"o": o, "status": st}
+
+
+# ----------------------------------------------------------------------------- GDN
+def ddt_tree_gdn(x, conv_w, conv_state, beta, decay, S, parent, n_nodes, *, Hk: int, out_dtype=None, out=None,
+                 status=None, workspace=None):
+    """x [L][B][N][C]; conv_w [L][C][K]; conv_state [L][B][K-1][C]; beta/decay [L][B][N][Hv] fp32;
+    S [L][B][Hv][dv][dk] fp32; parent [B][N]; n_nodes [B]."""
+    lib = _gpu()
+    L, B, N, C = x.shape
+    Hv, dv, dk = S.shape[2], S.shape[3], S.shape[4]
+    K = conv_w.shape[2]
+    dt = x.dtype
+    _need(x, (L, B, N, C), dt, "x")
+    if C != 2 * Hk * dk + Hv * dv:
+        raise DDTError("x channels must be 2*Hk*dk + Hv*dv")
+    _need(conv_w, (L, C, K), dt, "conv_w")
+    _need(conv_state, (L, B, K - 1, C), dt, "conv_state")
+    _need(beta, (L, B, N, Hv), torch.float32, "beta")
+    _need(decay, (L, B, N, Hv), torch.float32, "decay")
+    _need(S, (L, B, Hv, dv, dk), torch.float32, "S")
+    _need(parent, (B, N), torch.int32, "parent")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    out_dtype = out_dtype or dt
+    o = out if out is not None else torch.empty((L, B, N, Hv, dv), dtype=out_dtype, device=x.device)
+    _need(o, (L, B, N, Hv, dv), out_dtype, "o")
+    st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=x.device)
+    need = lib.ddt_tree_gdn_workspace(L, B, N, Hk, Hv, dk, dv)
+    ws = workspace if workspace is not None else _ws(need, x.device)
+    rc = lib.ddt_tree_gdn(L, B, N, Hk, Hv, dk, dv, K, _DT[dt], _DT[out_dtype], _ptr(x), _ptr(conv_w),
+                          _ptr(conv_state), _ptr(beta), _ptr(decay), _ptr(S), _ptr(parent), _ptr(n_nodes), _ptr(o),
+                          _ptr(st), _ptr(ws), ws.numel(), _stream())
+    _check(rc, "ddt_tree_gdn")
+    return {"o": o, "status": st}
+
+
+# ---------------------------------------------------------------------------- walk
+def ddt_walk_accept(token, parent, n_nodes, max_accept: int, *, target_logits=None, target_argmax=None, out=None,
+                    workspace=None):
+    """Greedy walk.  target_logits [B][N][V] (or target_argmax [B][N] int32)."""
+    lib = _gpu()
+    B, N = token.shape
+    dev = token.device
+    _need(token, (B, N), torch.int32, "token")
+    _need(parent, (B, N), torch.int32, "parent")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    A = max_accept + 1
+    o = out or {}
+    i32 = dict(dtype=torch.int32, device=dev)
+    if target_logits is not None:
+        V = target_logits.shape[2]
+        _need(target_logits, (B, N, V), None, "target_logits")
+        targ = o.get("target_argmax", torch.empty((B, N), **i32))
+        dt = _DT[target_logits.dtype]
+    else:
+        V = 1
+        targ = _need(target_argmax, (B, N), torch.int32, "target_argmax")
+        dt = F32
+    res = {"target_argmax": targ,
+           "acc_nodes": o.get("acc_nodes", torch.empty((B, A), **i32)),
+           "acc_len": o.get("acc_len", torch.empty((B,), **i32)),
+           "bonus": o.get("bonus", torch.empty((B,), **i32)),
+           "emitted": o.get("emitted", torch.empty((B, A), **i32)),
+           "n_emitted": o.get("n_emitted", torch.empty((B,), **i32)),
+           "status": o.get("status", torch.empty((B,), **i32))}
+    need = lib.ddt_walk_accept_workspace(B, N, V)
+    ws = workspace if workspace is not None else _ws(need, dev)
+    rc = lib.ddt_walk_accept(B, N, V, int(max_accept), dt, _ptr(target_logits), _ptr(targ), _ptr(token),
+                             _ptr(parent), _ptr(n_nodes), _ptr(res["acc_nodes"]), _ptr(res["acc_len"]),
+                             _ptr(res["bonus"]), _ptr(res["emitted"]), _ptr(res["n_emitted"]), _ptr(res["status"]),
+                             _ptr(ws), ws.numel(), _stream())
+    _check(rc, "ddt_walk_accept")
+    return res
+
+
+# -------------------------------------------------------------------------- commit
+def ddt_commit(acc_nodes, acc_len, prefix_len, *, k_tree=None, v_tree=None, k_cache=None, v_cache=None, x=None,
+               conv_w=None, beta=None, decay=None, S=None, conv_state=None, Hk: int = 1, out=None):
+    """In-place commit of the accepted path into the caches / GDN state / conv state."""
+    lib = _gpu()
+    B, A = acc_nodes.shape
+    dev = acc_nodes.device
+    _need(acc_nodes, (B, A), torch.int32, "acc_nodes")
+    _need(acc_len, (B,), torch.int32, "acc_len")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    N = None
+    if k_cache is not None:
+        La, _, N, Hkv, d = k_tree.shape
+        Pcap = k_cache.shape[3]
+        kdt = k_tree.dtype
+        _need(k_tree, (La, B, N, Hkv, d), kdt, "k_tree")
+        _need(v_tree, (La, B, N, Hkv, d), kdt, "v_tree")
+        _need(k_cache, (La, B, Hkv, Pcap, d), kdt, "k_cache")
+        _need(v_cache, (La, B, Hkv, Pcap, d), kdt, "v_cache")
+        kvd = _DT[kdt]
+    else:
+        La, Hkv, d, Pcap, kvd = 0, 1, 1, 0, F32
+    if S is not None:
+        Lg, _, N2, C = x.shape
+        N = N2 if N is None else N
+        if N2 != N:
+            raise DDTError("tree rows differ between the attention and GDN parts")
+        Hv, dv, dk = S.shape[2], S.shape[3], S.shape[4]
+        K = conv_w.shape[2]
+        _need(x, (Lg, B, N, C), x.dtype, "x")
+        _need(conv_w, (Lg, C, K), x.dtype, "conv_w")
+        _need(conv_state, (Lg, B, K - 1, C), x.dtype, "conv_state")
+        _need(beta, (Lg, B, N, Hv), torch.float32, "beta")
+        _need(decay, (Lg, B, N, Hv), torch.float32, "decay")
+        _need(S, (Lg, B, Hv, dv, dk), torch.float32, "S")
+        xd = _DT[x.dtype]
+    else:
+        Lg, Hv, dk, dv, K, xd = 0, 1, 1, 1, 1, F32
+    if N is None:
+        raise DDTError("ddt_commit needs the attention part, the GDN part, or both")
+    o = out or {}
+    i32 = dict(dtype=torch.int32, device=dev)
+    res = {"src_row": o.get("src_row", torch.empty((B, A), **i32)),
+           "dst_pos": o.get("dst_pos", torch.empty((B, A), **i32)),
+           "status": o.get("status", torch.empty((B,), **i32))}
+    rc = lib.ddt_commit(B, N, A, La, Hkv, d, Pcap, kvd, _ptr(k_tree), _ptr(v_tree), _ptr(k_cache), _ptr(v_cache),
+                        Lg, Hk, Hv, dk, dv, K, xd, _ptr(x), _ptr(conv_w), _ptr(beta), _ptr(decay), _ptr(S),
+                        _ptr(conv_state), _ptr(acc_nodes), _ptr(acc_len), _ptr(prefix_len), _ptr(res["src_row"]),
+                        _ptr(res["dst_pos"]), _ptr(res["status"]), _stream())
+    _check(rc, "ddt_commit")
+    return res
