@@ -42,7 +42,7 @@ def _check_walk(g, o, tree):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_walk_tiny_and_drafter_vocab(dtype):
     for (B, D, V, budget, wl) in [(1, 8, 1024, 16, 1), (3, 15, 151936, 64, 2)]:
-        tree, _ = C.tree_from_logits(wl, B, D, 3000, 8, budget)
+        tree, _ = C.tree_from_logits(wl, B, D, V, 8, budget)
         lens = np.random.default_rng(wl).integers(0, D + 1, B)
         tl = _planted_logits(tree, V, wl, dtype, lens)
         g = _walk_gpu(tree, D, tl=tl)
