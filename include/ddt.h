@@ -27,7 +27,8 @@
  *   - All array pointers are DEVICE pointers, contiguous, C row-major with the
  *     shapes given below (outermost first).  The caller owns and allocates every
  *     buffer, including workspaces; the library allocates no device memory and keeps
- *     no global state.  Calls are thread-safe.
+ *     no global state (ddt_build_tree_noalloc's fixed scratch array aside).  Calls are
+ *     thread-safe.
  *   - Work is enqueued on `stream`; nothing synchronises the host.  Results and the
  *     per-request `status` words are valid once the stream has reached the call.
  *   - Argument errors found on the host (null pointers, unsupported sizes, short
@@ -100,6 +101,30 @@ ddt_status ddt_build_tree(int B, int D, int V, int top_k, int budget, ddt_dtype 
                           int32_t* depth, int32_t* position, int32_t* n_nodes, uint32_t* anc,
                           double* score, int32_t* status, void* workspace, size_t ws_bytes,
                           ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * ddt_build_tree_noalloc -- not part of the method (the pages have no counterpart): the
+ * ddt_build_tree above for callers that cannot allocate device memory, such as a plain
+ * C host without a device allocator, or a plugin inside a process whose GPU memory is
+ * owned by another runtime, or a decode loop that must not call cudaMalloc/cudaFree
+ * because they synchronise the device.  Same arguments and results as ddt_build_tree,
+ * without the workspace: the scratch is a fixed 4 MiB device array inside the library,
+ * present on every GPU that loads the library until the process exits.
+ *   - The first call on a device looks up that array's device address (once per
+ *     device, with the device current); make that first call before any stream capture.
+ *   - Every call on a device shares the array, which keeps the last call's contents:
+ *     calls whose kernels overlap on the GPU race on it and must be ordered by the caller.
+ *   - Returns DDT_ERR_CAPACITY, before launching anything, when the call needs more
+ *     than 4 MiB (ddt_build_tree_workspace(B, D, V, top_k) > 4 MiB), e.g. B = 32,
+ *     D = 15, V = 151936 needs 0.7 MiB with top_k = 8 and 2.4 MiB with top_k = 32.
+ *   - Allocates nothing (no cudaMalloc, no allocating library call).
+ * ------------------------------------------------------------------------------- */
+ddt_status ddt_build_tree_noalloc(int B, int D, int V, int top_k, int budget, ddt_dtype dtype,
+                                  const void* draft_logits, const int32_t* root_token,
+                                  const int32_t* prefix_len, int32_t* token, int32_t* parent,
+                                  int32_t* depth, int32_t* position, int32_t* n_nodes,
+                                  uint32_t* anc, double* score, int32_t* status,
+                                  ddt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * ddt_tree_attn -- [NOTES] "Why hybrid attention makes it hard": each tree row attends

@@ -18,6 +18,8 @@
 #include <float.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -443,3 +445,72 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
 }
 
 }  // namespace ddt
+
+// ---------------------------------------------------------------------------------
+// ddt_build_tree_noalloc: the same tree build for callers that cannot allocate device
+// memory.  Some hosts of this library have no device allocator of their own (a plain C
+// program, or a plugin living inside a process whose GPU memory is owned by another
+// runtime), and some must not call cudaMalloc/cudaFree in their decode loop because
+// those calls synchronise the device.  For them the build's per-chunk partials live in
+// one file-scope device array instead of a caller-supplied workspace.
+//
+// The array is a fixed kStaticScratchBytes (4 MiB) on every GPU that loads this library,
+// held until the process exits.  Its device address is looked up once per device with
+// cudaGetSymbolAddress (on the host the symbol is only a stand-in, never a device
+// pointer); the first call on each device does that lookup, so make it before any
+// stream capture.  All calls on a device share the array: calls whose kernels overlap on
+// the GPU (different streams, or different host threads without ordering) race on it and
+// must be serialised by the caller.  The partial kernel writes every record the tree
+// kernel reads, so nothing in the array has to start at zero.
+namespace ddt {
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+constexpr int kMaxDevices = 64;
+__device__ __align__(256) unsigned char g_build_scratch[kStaticScratchBytes];
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_build_scratch on the current device (looked up once per device).
+cudaError_t static_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_build_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+}  // namespace ddt
+
+extern "C" ddt_status ddt_build_tree_noalloc(int B, int D, int V, int top_k, int budget, ddt_dtype dtype,
+                                             const void* draft_logits, const int32_t* root_token,
+                                             const int32_t* prefix_len, int32_t* token, int32_t* parent,
+                                             int32_t* depth, int32_t* position, int32_t* n_nodes, uint32_t* anc,
+                                             double* score, int32_t* status, ddt_stream_t stream) {
+    using namespace ddt;
+    if (B < 1 || D < 1 || V < 1 || top_k < 1 || budget < 0 || (dtype != DDT_F32 && dtype != DDT_BF16))
+        return DDT_ERR_INVALID_ARG;
+    if (D > kMaxDepth || top_k > kMaxTopK || top_k > V || budget > kMaxBudget) return DDT_ERR_UNSUPPORTED;
+    if (!draft_logits || !root_token || !prefix_len || !token || !parent || !depth || !position || !n_nodes || !anc ||
+        !status)
+        return DDT_ERR_INVALID_ARG;
+    // the partials of this call must fit the static array
+    if (build_ws_bytes(B, D, V, top_k) > kStaticScratchBytes) return DDT_ERR_CAPACITY;
+    if (build_tree_smem(D, top_k, budget) > 200 * 1024) return DDT_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (static_scratch(&scratch) != cudaSuccess) return DDT_ERR_CUDA;
+    const cudaError_t e = launch_build_tree(B, D, V, top_k, budget, dtype, draft_logits, root_token, prefix_len, token,
+                                           parent, depth, position, n_nodes, anc, score, status, scratch,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) return DDT_OK;
+    return e == cudaErrorInvalidValue ? DDT_ERR_UNSUPPORTED : DDT_ERR_CUDA;
+}
+

@@ -34,6 +34,7 @@ _SIGS = {
     "ddt_version": ([], ctypes.c_char_p),
     "ddt_build_tree_workspace": ([_c_int] * 4, _c_size),
     "ddt_build_tree": ([_c_int] * 6 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_build_tree_noalloc": ([_c_int] * 6 + [_c_p] * 11 + [_c_p], _c_int),
     "ddt_tree_attn_workspace": ([_c_int] * 7, _c_size),
     "ddt_tree_attn": ([_c_int] * 9 + [_c_p] * 8 + [_c_float, _c_p, _c_p, _c_p, _c_size, _c_p], _c_int),
     "ddt_tree_gdn_workspace": ([_c_int] * 7, _c_size),
@@ -140,6 +141,30 @@ def ddt_build_tree(draft_logits, root_token, prefix_len, top_k: int, budget: int
                             _ptr(res["score"]), _ptr(res["status"]), _ptr(ws), ws.numel(), _stream())
     _check(rc, "ddt_build_tree")
     return res
+
+
+def ddt_build_tree_noalloc(draft_logits, root_token, prefix_len, top_k: int, budget: int, *, out):
+    """ddt_build_tree for callers that cannot allocate device memory: the scratch is the
+    library's fixed 4 MiB device array, so `out` must hold every preallocated output
+    (token, parent, depth, position, n_nodes, anc, score or None, status).  Calls whose
+    kernels overlap on the GPU share that array and must be ordered by the caller."""
+    lib = _gpu()
+    B, D, V = draft_logits.shape
+    _need(draft_logits, (B, D, V), None, "draft_logits")
+    _need(root_token, (B,), torch.int32, "root_token")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    N = budget + 1
+    for name, shape in (("token", (B, N)), ("parent", (B, N)), ("depth", (B, N)), ("position", (B, N)),
+                        ("n_nodes", (B,)), ("anc", (B, N, (N + 31) // 32)), ("status", (B,))):
+        _need(out.get(name), shape, None, name)
+    if out.get("score") is not None:
+        _need(out["score"], (B, N), torch.float64, "score")
+    rc = lib.ddt_build_tree_noalloc(B, D, V, int(top_k), int(budget), _DT[draft_logits.dtype], _ptr(draft_logits),
+                                    _ptr(root_token), _ptr(prefix_len), _ptr(out["token"]), _ptr(out["parent"]),
+                                    _ptr(out["depth"]), _ptr(out["position"]), _ptr(out["n_nodes"]),
+                                    _ptr(out["anc"]), _ptr(out.get("score")), _ptr(out["status"]), _stream())
+    _check(rc, "ddt_build_tree_noalloc")
+    return out
 
 
 # ----------------------------------------------------------------------- attention
