@@ -98,3 +98,12 @@ def test_attn_tree_verify_workload_sampled():
                                C.f64(inp.v_tree[l, 0, :, g]), tree["anc"][0, i], tree["n_nodes"][0], 1 / 16.0)
         err = np.abs(got[l, 0, i, h] - want).max() / np.abs(want).max()
         assert err <= TOL, (l, i, h, err)
+
+
+def test_attn_bf16_split_kv_and_big_tree():
+    """Long prefix with few work units (split-KV partials + merge) and a 201-row tree
+    (several tree tiles and M-tiles); ragged prefix lengths incl. one shorter than a tile."""
+    tree, inp, N = _case(6, 1, 2, 8, 2, 128, [2000, 37], 200, torch.bfloat16, D=12, V=400, k=6)
+    r = _gpu(tree, inp)
+    _check(r["o"], _oracle(tree, inp, 128), tree)
+    assert r["status"].cpu().tolist() == [0, 0]

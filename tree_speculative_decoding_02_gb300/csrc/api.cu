@@ -62,8 +62,8 @@ ddt_status ddt_build_tree(int B, int D, int V, int top_k, int budget, ddt_dtype 
 
 // ------------------------------------------------------------------------ attention
 size_t ddt_tree_attn_workspace(int n_layers, int B, int N, int Hq, int Hkv, int d, int Pcap) {
-    (void)n_layers; (void)B; (void)N; (void)Hq; (void)Hkv; (void)d; (void)Pcap;
-    return 256;
+    if (n_layers < 1 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Pcap < 0) return 0;
+    return attn_tc_ws_bytes(n_layers, B, N, Hq, Hkv, d, Pcap);
 }
 
 ddt_status ddt_tree_attn(int n_layers, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype in_dtype,
@@ -71,7 +71,6 @@ ddt_status ddt_tree_attn(int n_layers, int B, int N, int Hq, int Hkv, int d, int
                          const void* k_cache, const void* v_cache, const int32_t* prefix_len, const int32_t* n_nodes,
                          const uint32_t* anc, float scale, void* o, int32_t* status, void* workspace,
                          size_t ws_bytes, ddt_stream_t stream) {
-    (void)workspace; (void)ws_bytes;
     if (n_layers < 1 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Pcap < 0 || !dtype_ok(in_dtype) ||
         !dtype_ok(out_dtype))
         return DDT_ERR_INVALID_ARG;
@@ -80,6 +79,17 @@ ddt_status ddt_tree_attn(int n_layers, int B, int N, int Hq, int Hkv, int d, int
     if (!q || !k_tree || !v_tree || (Pcap > 0 && (!k_cache || !v_cache)) || !prefix_len || !n_nodes || !anc || !o ||
         !status)
         return DDT_ERR_INVALID_ARG;
+    // bf16 with a compiled head size runs on the tensor cores; fp32 on the CUDA cores
+    if (attn_tc_supported(d, in_dtype)) {
+        if (!workspace || ws_bytes < attn_tc_ws_bytes(n_layers, B, N, Hq, Hkv, d, Pcap) || !aligned16(workspace))
+            return DDT_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(o) ||
+            (Pcap > 0 && (!aligned16(k_cache) || !aligned16(v_cache))))
+            return DDT_ERR_INVALID_ARG;
+        return from_cuda(launch_attn_tc(n_layers, B, N, Hq, Hkv, d, Pcap, out_dtype, q, k_tree, v_tree, k_cache,
+                                        v_cache, prefix_len, n_nodes, anc, scale, o, status, workspace, ws_bytes,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(launch_attn_simt(n_layers, B, N, Hq, Hkv, d, Pcap, in_dtype, out_dtype, q, k_tree, v_tree,
                                       k_cache, v_cache, prefix_len, n_nodes, anc, scale, o, status,
                                       reinterpret_cast<cudaStream_t>(stream)));

@@ -1,0 +1,680 @@
+// attn_tc.cu -- ddt_tree_attn on the 5th-generation tensor cores (bf16 in, fp32 accumulate).
+//
+// "DDTree on vLLM: candid research notes", section "Why hybrid attention makes it hard":
+// each candidate row sees the committed prefix plus its own ancestors, never its
+// siblings.  "From Tree-Based Speculative Decoding to Drafter Training", section "The
+// Architecture of DDTree": one target pass over the flattened tree with an
+// ancestor-only mask.
+//
+// Work unit (one CTA): a layer, a request, a kv head g, a 128-row M-tile of that head's
+// query rows (row = node * G + head-in-group, G = Hq/Hkv, so the whole GQA group shares
+// one K/V stream), and a chunk of the prefix.  The chunk holding the prefix's end also
+// takes the tree rows as keys.  Keys stream in tiles of 64:
+//   warp 0      TMA producer: K and V tiles into a 4-stage shared-memory ring (128-byte
+//               swizzle).  Prefix tiles come from a 3-D map (d, position, layer*B*Hkv);
+//               the ragged last tile is shifted to end exactly at prefix_len, so no row
+//               past the prefix is ever read (positions < 0 are zero-filled by TMA).
+//               Tree tiles come from a 4-D map (d, kv head, node, layer*B).
+//   warp 1      MMA issuer: S_j = Q K_j^T (bf16) into one of two TMEM buffers; O += P_j V_j
+//               (fp16) with P_j read back from TMEM (written over S_j) and V_j MN-major in
+//               shared memory.
+//   warps 4-7   softmax: one TMEM lane (= query row) per thread, ancestor mask on tree
+//               tiles, running max with lazy O rescaling (only when the max grows by
+//               more than 2^8), P to TMEM as fp16; epilogue O / l to global (or a
+//               split-KV partial that k_attn_merge combines).
+//   warps 8-11  V converters: each landed V tile is rewritten in place from bf16 to fp16
+//               (exact for |v| in [2^-14, 65504]) and padding tree rows are zeroed.  P in
+//               fp16 (11-bit significand) keeps the output within ~5e-4 of exact, where
+//               bf16 P (8 bits) would give ~3e-3; the conversion costs no tensor work.
+// Every mbarrier wait is bounded; on a timeout the CTA drains its copies and MMAs,
+// frees TMEM, and reports DDT_ERR_TIMEOUT in the request's status word.
+#include <cuda.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace ddt {
+
+namespace {
+
+constexpr int kBM = 128;     // query rows per CTA (TMEM lanes)
+constexpr int kBN = 64;      // keys per tile
+constexpr int kStages = 4;   // K/V ring depth (K and V tiles alternate)
+constexpr float kTau = 8.f;  // rescale O only when the row max grows by more than 2^kTau
+
+struct TcParams {
+    int L, B, N, Hq, Hkv, G, MT, S, chunk, Pcap, W;
+    const __nv_bfloat16* q;
+    const int32_t* prefix_len;
+    const int32_t* n_nodes;
+    const uint32_t* anc;
+    const int32_t* perm;  // requests by prefix length, longest first
+    void* o;              // final output (S == 1)
+    float* part_o;        // [S][L][B][Hkv][MT*128][D] unnormalised partial O (S > 1)
+    float2* part_ml;      // [S][L][B][Hkv][MT*128] (row max in log2 units, row sum)
+    int32_t* status;
+    float scale_log2;
+};
+
+constexpr int kThreads = 384;
+
+template <int D>
+struct TcCfg {
+    static constexpr int kBlocks = D / 64;              // 128-byte-swizzle column blocks
+    static constexpr int kQBytes = kBM * D * 2;
+    static constexpr int kStageBytes = kBN * D * 2;
+    static constexpr int kOCol = 2 * kBN;                // O accumulator column in TMEM
+    static constexpr int kTmemCols = (2 * kBN + D) <= 256 ? 256 : 512;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + kBarBytes;
+};
+
+struct Tile {
+    int tree;  // 0 = prefix tile, 1 = tree tile
+    int y;     // first key: prefix position or tree node
+    int lo;    // prefix tiles: keys below lo were handled by the previous tile
+};
+
+__device__ __forceinline__ Tile tile_of(int j, int n_pre, int c0, int c1, bool ragged) {
+    Tile t;
+    if (j < n_pre) {
+        t.tree = 0;
+        t.lo = c0 + j * kBN;
+        t.y = (j == n_pre - 1 && ragged) ? c1 - kBN : t.lo;
+    } else {
+        t.tree = 1;
+        t.y = (j - n_pre) * kBN;
+        t.lo = 0;
+    }
+    return t;
+}
+
+// Bounded wait that ignores the abort flag: used only to drain in-flight work.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!tc::mbar_try(bar, parity))
+        if (clock64() - t0 > tc::kWaitCycles) return;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename Tout>
+__device__ __forceinline__ void store_row32(Tout* dst, const float* v);
+template <>
+__device__ __forceinline__ void store_row32<float>(float* dst, const float* v) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+template <>
+__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        uint4 u;
+        u.x = pack_bf16(v[i], v[i + 1]);
+        u.y = pack_bf16(v[i + 2], v[i + 3]);
+        u.z = pack_bf16(v[i + 4], v[i + 5]);
+        u.w = pack_bf16(v[i + 6], v[i + 7]);
+        *reinterpret_cast<uint4*>(dst + i) = u;
+    }
+}
+
+}  // namespace
+
+template <int D, typename Tout>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_tc(const TcParams p, const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+              const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+    using Cfg = TcCfg<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    unsigned char* sQ = base;
+    unsigned char* sRing = base + Cfg::kQBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * Cfg::kStageBytes);
+    uint64_t* full = bars;                 // [kStages] TMA landed
+    uint64_t* empty = bars + kStages;      // [kStages] MMA done with the stage
+    uint64_t* s_full = bars + 2 * kStages; // [2] S_j in TMEM
+    uint64_t* p_full = s_full + 2;         // [2] P_j in TMEM (128 arrivals)
+    uint64_t* o_done = p_full + 2;         // one completion per PV
+    uint64_t* drain = o_done + 1;
+    uint64_t* v_ready = drain + 1;         // [kStages] V tile converted to fp16 (128 arrivals)
+    // Single-phase barrier for the epilogue: when the softmax reaches it, o_done may
+    // still lack the last two completions, which a parity wait cannot tell apart.
+    uint64_t* o_final = v_ready + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int x = blockIdx.x;
+    const int s = x % p.S;
+    x /= p.S;
+    const int mt = x % p.MT;
+    x /= p.MT;
+    const int g = x % p.Hkv;
+    const int l = x / p.Hkv;
+    const int b = p.perm[blockIdx.y];
+    const long lb = (long)l * p.B + b;
+    const int P = p.prefix_len[b], nn = p.n_nodes[b];
+    const bool bad = P < 0 || P > p.Pcap || nn < 1 || nn > p.N;
+    const long prow0 = ((((long)s * p.L + l) * p.B + b) * p.Hkv + g) * (long)(p.MT * kBM) + mt * kBM;
+
+    if (bad) {
+        if (tid == 0 && s == 0 && mt == 0 && g == 0 && l == 0)
+            p.status[b] = (P < 0 || P > p.Pcap) ? DDT_ERR_CAPACITY : DDT_ERR_TREE;
+        if (p.S == 1) {
+            for (int e = tid; e < kBM * D; e += kThreads) {
+                const int R = mt * kBM + e / D;
+                if (R >= p.N * p.G) continue;
+                const int node = R / p.G, h = g * p.G + R % p.G;
+                static_cast<Tout*>(p.o)[((lb * p.N + node) * p.Hq + h) * D + e % D] = from_f32<Tout>(0.f);
+            }
+        } else if (tid < kBM) {
+            p.part_ml[prow0 + tid] = make_float2(-INFINITY, 0.f);
+        }
+        return;
+    }
+
+    const int c0 = s * p.chunk;
+    const int s_last = P > 0 ? (P - 1) / p.chunk : 0;
+    int n_pre = 0, c1 = c0;
+    if (c0 < P) {
+        c1 = min(c0 + p.chunk, P);
+        n_pre = (c1 - c0 + kBN - 1) / kBN;
+    }
+    const int n_tree = (s == s_last) ? (nn + kBN - 1) / kBN : 0;
+    const int T = n_pre + n_tree;
+    const bool ragged = ((c1 - c0) % kBN) != 0;
+    if (T == 0) {  // an empty split (only when S > 1)
+        if (tid < kBM) p.part_ml[prow0 + tid] = make_float2(-INFINITY, 0.f);
+        return;
+    }
+
+    // ---- setup: barriers, TMEM, Q tile (manual 128-byte swizzle)
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(full + i, 1);
+            tc::mbar_init(empty + i, 1);
+        }
+        tc::mbar_init(s_full, 1);
+        tc::mbar_init(s_full + 1, 1);
+        tc::mbar_init(p_full, 128);
+        tc::mbar_init(p_full + 1, 128);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(drain, 1);
+        for (int i = 0; i < kStages; ++i) tc::mbar_init(v_ready + i, 128);
+        tc::mbar_init(o_final, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, Cfg::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (tid == 64) {
+        tc::prefetch_tmap(&tm_kc);
+        tc::prefetch_tmap(&tm_vc);
+        tc::prefetch_tmap(&tm_kt);
+        tc::prefetch_tmap(&tm_vt);
+    }
+    {
+        constexpr int kChunks = D / 8;  // 16-byte chunks per row
+        for (int e = tid; e < kBM * kChunks; e += kThreads) {
+            const int r = e / kChunks, ch = e % kChunks;
+            const int R = mt * kBM + r;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (R < p.N * p.G) {
+                const int node = R / p.G, h = g * p.G + R % p.G;
+                if (node < nn) v = __ldg(reinterpret_cast<const uint4*>(p.q + ((lb * p.N + node) * p.Hq + h) * D) + ch);
+            }
+            const int blk = ch >> 3, jj = ch & 7;
+            *reinterpret_cast<uint4*>(sQ + blk * (kBM * 128) + r * 128 + ((jj ^ (r & 7)) << 4)) = v;
+        }
+    }
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            const int grp = (int)((lb * p.Hkv) + g);
+            int issued = 0;
+            for (int j = 0; j < T && !*abort_flag; ++j) {
+                const Tile t = tile_of(j, n_pre, c0, c1, ragged);
+                bool ok = true;
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int u = 2 * j + kv, st = u % kStages;
+                    if (!tc::mbar_wait(empty + st, ((u / kStages) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::mbar_expect_tx(full + st, Cfg::kStageBytes);
+                    unsigned char* dst = sRing + st * Cfg::kStageBytes;
+#pragma unroll
+                    for (int blk = 0; blk < Cfg::kBlocks; ++blk) {
+                        if (!t.tree)
+                            tc::tma_load_3d(dst + blk * (kBN * 128), kv ? &tm_vc : &tm_kc, full + st, blk * 64, t.y, grp);
+                        else
+                            tc::tma_load_4d(dst + blk * (kBN * 128), kv ? &tm_vt : &tm_kt, full + st, blk * 64, g, t.y,
+                                            (int)lb);
+                    }
+                    issued = u + 1;
+                }
+                if (!ok) break;
+            }
+            for (int u = max(0, issued - kStages); u < issued; ++u) drain_wait(full + u % kStages, (u / kStages) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, false, false);
+            constexpr uint32_t idesc_pv = tc::idesc_f16(kBM, D, false, true);
+            const uint32_t sQa = tc::smem_u32(sQ), sRa = tc::smem_u32(sRing);
+            auto pv = [&](int i) -> bool {
+                if (!tc::mbar_wait(p_full + (i & 1), (i >> 1) & 1, abort_flag)) return false;
+                const int u = 2 * i + 1, st = u % kStages;
+                if (!tc::mbar_wait(v_ready + st, (u / kStages) & 1, abort_flag)) return false;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    // V tile: 16 keys = two 8-row swizzle atoms down the K dimension
+                    const uint64_t bdesc = tc::desc_sw128(sRa + st * Cfg::kStageBytes + kk * 2048, kBN * 128, 1024);
+                    tc::mma_f16_ts(tmem + Cfg::kOCol, tmem + (i & 1) * kBN + kk * 8, bdesc, idesc_pv,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(empty + st);
+                tc::mma_commit(o_done);
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < T && ok; ++j) {
+                const int u = 2 * j, st = u % kStages;
+                if (!tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qoff = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+                    tc::mma_f16_ss(tmem + (j & 1) * kBN, tc::desc_sw128(sQa + qoff, 16, 1024),
+                                   tc::desc_sw128(sRa + st * Cfg::kStageBytes + koff, 16, 1024), idesc_qk,
+                                   kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(empty + st);
+                tc::mma_commit(s_full + (j & 1));
+                if (j >= 1) ok = pv(j - 1);
+            }
+            if (ok && pv(T - 1)) tc::mma_commit(o_final);
+            tc::mma_commit(drain);
+            drain_wait(drain, 0);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------------ softmax
+        const int ws = warp - 4, r = 32 * ws + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * ws) << 16;
+        const int R = mt * kBM + r;
+        const bool in_rows = R < p.N * p.G;
+        const int node = in_rows ? R / p.G : 0;
+        const int h = g * p.G + (in_rows ? R % p.G : 0);
+        const bool live = in_rows && node < nn;
+        const uint32_t* anc_row = p.anc + ((long)b * p.N + node) * p.W;
+        float m_used = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < T; ++j) {
+            const Tile t = tile_of(j, n_pre, c0, c1, ragged);
+            ok = tc::mbar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag);
+            if (!__all_sync(kFull, ok)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            uint32_t sr[2][32];
+            tc::tmem_ld32(tmem + lane_base + (j & 1) * kBN, sr[0]);
+            tc::tmem_ld32(tmem + lane_base + (j & 1) * kBN + 32, sr[1]);
+            tc::tmem_wait_ld();
+            uint64_t vis;
+            if (!t.tree) {
+                const int skip = t.lo - t.y;  // leading keys already seen (ragged last tile)
+                vis = skip <= 0 ? ~0ull : (~0ull << skip);
+            } else if (live) {
+                const int w0 = t.y >> 5;
+                const uint32_t lo32 = anc_row[w0];
+                const uint32_t hi32 = (w0 + 1 < p.W) ? anc_row[w0 + 1] : 0u;
+                vis = static_cast<uint64_t>(lo32) | (static_cast<uint64_t>(hi32) << 32);
+            } else {
+                vis = 0ull;
+            }
+            float sv[64];
+            float mtile = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float raw = __uint_as_float(sr[c >> 5][c & 31]);
+                sv[c] = ((vis >> c) & 1ull) ? raw * p.scale_log2 : -INFINITY;
+                mtile = fmaxf(mtile, sv[c]);
+            }
+            // lazy rescale: only when the max grows by more than 2^kTau
+            const bool grow = mtile > m_used + kTau;
+            const bool need = grow && (m_used != -INFINITY);  // O already holds this row's data
+            if (__any_sync(kFull, need)) {
+                ok = tc::mbar_wait(o_done, (j - 1) & 1, abort_flag);
+                if (!__all_sync(kFull, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const float f = need ? tc::ex2(m_used - mtile) : 1.f;
+#pragma unroll 1
+                for (int cb = 0; cb < D; cb += 32) {
+                    uint32_t ov[32];
+                    tc::tmem_ld32(tmem + lane_base + Cfg::kOCol + cb, ov);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+                    tc::tmem_st32(tmem + lane_base + Cfg::kOCol + cb, ov);
+                }
+                tc::tmem_wait_st();
+                if (need) l_run *= f;
+            }
+            if (grow) m_used = mtile;
+            uint32_t pk[32];
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                const float a = (sv[c] == -INFINITY) ? 0.f : tc::ex2(sv[c] - m_used);
+                const float bb = (sv[c + 1] == -INFINITY) ? 0.f : tc::ex2(sv[c + 1] - m_used);
+                sum += a + bb;
+                pk[c >> 1] = pack_f16(a, bb);
+            }
+            l_run += sum;
+            tc::tmem_st32(tmem + lane_base + (j & 1) * kBN, pk);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            tc::mbar_arrive(p_full + (j & 1));
+        }
+        if (ok) {
+            ok = tc::mbar_wait(o_final, 0, abort_flag);
+            ok = __all_sync(kFull, ok);
+        }
+        if (ok) {
+            tc::tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t ov[32];
+                tc::tmem_ld32(tmem + lane_base + Cfg::kOCol + cb, ov);
+                tc::tmem_wait_ld();
+                float f[32];
+                if (p.S == 1) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = live ? __uint_as_float(ov[i]) * inv : 0.f;
+                    if (in_rows)
+                        store_row32<Tout>(static_cast<Tout*>(p.o) + ((lb * p.N + node) * p.Hq + h) * D + cb, f);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(ov[i]);
+                    store_row32<float>(p.part_o + (prow0 + r) * D + cb, f);
+                }
+            }
+            if (p.S > 1) p.part_ml[prow0 + r] = make_float2(m_used, l_run);
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------------ V converters
+        const int ct = tid - 256;  // 0..127
+        constexpr int kVec = kBN * D / 8;  // 16-byte chunks per V tile
+        int overflow = 0;
+        for (int j = 0; j < T; ++j) {
+            const Tile t = tile_of(j, n_pre, c0, c1, ragged);
+            const int u = 2 * j + 1, st = u % kStages;
+            const bool ok = tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag);
+            if (!__all_sync(kFull, ok)) break;
+            unsigned char* vst = sRing + st * Cfg::kStageBytes;
+            // padding tree rows (node >= n_nodes) may hold anything: they become zeros
+            const int first = t.tree ? max(0, nn - t.y) : kBN;
+#pragma unroll 4
+            for (int e = ct; e < kVec; e += 128) {
+                const int row = (e % (kBN * 8)) / 8;  // row within its 64-row column block
+                uint4* ptr = reinterpret_cast<uint4*>(vst) + e;
+                uint4 v = *ptr;
+                if (row >= first) {
+                    v = make_uint4(0, 0, 0, 0);
+                } else {
+                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+                        overflow |= (fabsf(lo) >= 65520.f) | (fabsf(hi) >= 65520.f);
+                        w[i] = pack_f16(lo, hi);
+                    }
+                    v = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                *ptr = v;
+            }
+            tc::fence_proxy_async();
+            tc::mbar_arrive(v_ready + st);
+        }
+        if (__any_sync(kFull, overflow) && lane == 0) atomicExch(p.status + b, (int)DDT_ERR_UNSUPPORTED);
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+    if (tid == 0 && *abort_flag) atomicExch(p.status + b, (int)DDT_ERR_TIMEOUT);
+}
+
+// Combines split-KV partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+template <int D, typename Tout>
+__global__ void __launch_bounds__(D) k_attn_merge(const TcParams p) {
+    const int row = blockIdx.x;  // node * Hq + head
+    const int lbi = blockIdx.y;
+    const int l = lbi / p.B, b = lbi % p.B;
+    const int node = row / p.Hq, hq = row % p.Hq;
+    const int g = hq / p.G, R = node * p.G + hq % p.G;
+    const int c = threadIdx.x;
+    const int P = p.prefix_len[b], nn = p.n_nodes[b];
+    Tout* out = static_cast<Tout*>(p.o) + (((long)l * p.B + b) * p.N * p.Hq + row) * D + c;
+    if (P < 0 || P > p.Pcap || nn < 1 || nn > p.N || node >= nn) {
+        *out = from_f32<Tout>(0.f);
+        return;
+    }
+    const long stride_s = (long)p.L * p.B * p.Hkv * p.MT * kBM;
+    const long r0 = ((((long)l * p.B + b) * p.Hkv + g) * (long)(p.MT * kBM)) + R;
+    float M = -INFINITY;
+    for (int s = 0; s < p.S; ++s) {
+        const float2 ml = p.part_ml[s * stride_s + r0];
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+    float acc = 0.f, lsum = 0.f;
+    for (int s = 0; s < p.S; ++s) {
+        const float2 ml = p.part_ml[s * stride_s + r0];
+        if (!(ml.y > 0.f)) continue;
+        const float w = tc::ex2(ml.x - M);
+        lsum += w * ml.y;
+        acc += w * p.part_o[(s * stride_s + r0) * D + c];
+    }
+    *out = from_f32<Tout>(lsum > 0.f ? acc / lsum : 0.f);
+}
+
+// Requests ordered by prefix length, longest first (ties by index): long units start
+// first.  Also clears the status words, which the attention CTAs only ever set to errors.
+__global__ void k_attn_order(int B, const int32_t* __restrict__ prefix_len, int32_t* __restrict__ perm,
+                             int32_t* __restrict__ status) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        status[b] = DDT_OK;
+        const int pb = prefix_len[b];
+        int rank = 0;
+        for (int o = 0; o < B; ++o) {
+            const int po = prefix_len[o];
+            rank += (po > pb) || (po == pb && o < b);
+        }
+        perm[rank] = b;
+    }
+}
+
+// ------------------------------------------------------------------------------ host
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+int sm_count() {
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+}
+
+// Split of the prefix into `S` chunks so that small batches still fill the GPU.
+void choose_split(int L, int B, int Hkv, int MT, int Pcap, int n_sms, int* S, int* chunk) {
+    const long base = (long)L * B * Hkv * MT;
+    int s = 1;
+    if (base < 2L * n_sms && Pcap > 0) {
+        s = (int)((4L * n_sms + base - 1) / base);
+        s = min(s, max(1, (Pcap + 511) / 512));
+    }
+    int c = Pcap > 0 ? (Pcap + s - 1) / s : kBN;
+    c = ((c + kBN - 1) / kBN) * kBN;
+    *chunk = c;
+    *S = Pcap > 0 ? (Pcap + c - 1) / c : 1;
+}
+
+}  // namespace
+
+size_t attn_tc_ws_bytes(int L, int B, int N, int Hq, int Hkv, int d, int Pcap) {
+    const int G = Hq / Hkv;
+    const int MT = (N * G + kBM - 1) / kBM;
+    int S, chunk;
+    choose_split(L, B, Hkv, MT, Pcap, 256, &S, &chunk);  // 256 bounds the SM count from above
+    size_t bytes = ((size_t)B * sizeof(int32_t) + 255) & ~(size_t)255;
+    if (S > 1) {
+        const size_t rows = (size_t)S * L * B * Hkv * MT * kBM;
+        bytes += rows * d * sizeof(float) + rows * sizeof(float2);
+    }
+    return bytes + 256;
+}
+
+bool attn_tc_supported(int d, ddt_dtype in) { return in == DDT_BF16 && (d == 64 || d == 128 || d == 256); }
+
+template <int D, typename Tout>
+static cudaError_t attn_tc_go(const TcParams& prm, const CUtensorMap* maps, cudaStream_t st) {
+    using Cfg = TcCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tc<D, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(prm.S * prm.MT * prm.Hkv * prm.L, prm.B);
+    k_attn_tc<D, Tout><<<grid, kThreads, Cfg::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3]);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (prm.S > 1) {
+        k_attn_merge<D, Tout><<<dim3(prm.N * prm.Hq, prm.L * prm.B), D, 0, st>>>(prm);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out, const void* q,
+                           const void* k_tree, const void* v_tree, const void* k_cache, const void* v_cache,
+                           const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
+                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    TcParams prm;
+    prm.L = L;
+    prm.B = B;
+    prm.N = N;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.G = Hq / Hkv;
+    prm.MT = (N * prm.G + kBM - 1) / kBM;
+    prm.Pcap = Pcap;
+    prm.W = (N + 31) / 32;
+    choose_split(L, B, Hkv, prm.MT, Pcap, sm_count(), &prm.S, &prm.chunk);
+    if (ws_bytes < attn_tc_ws_bytes(L, B, N, Hq, Hkv, d, Pcap)) return cudaErrorInvalidValue;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    int32_t* perm = reinterpret_cast<int32_t*>(w);
+    prm.perm = perm;
+    const size_t perm_bytes = ((size_t)B * sizeof(int32_t) + 255) & ~(size_t)255;
+    const size_t rows = (size_t)prm.S * L * B * Hkv * prm.MT * kBM;
+    prm.part_o = reinterpret_cast<float*>(w + perm_bytes);
+    prm.part_ml = reinterpret_cast<float2*>(w + perm_bytes + (prm.S > 1 ? rows * d * sizeof(float) : 0));
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.prefix_len = prefix_len;
+    prm.n_nodes = n_nodes;
+    prm.anc = anc;
+    prm.o = o;
+    prm.status = status;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+
+    // tensor maps: caches (d, position, layer*B*Hkv), tree rows (d, kv head, node, layer*B)
+    CUtensorMap maps[4];
+    const cuuint32_t box3[3] = {64, (cuuint32_t)kBN, 1};
+    const cuuint32_t es3[3] = {1, 1, 1};
+    const cuuint64_t dims3[3] = {(cuuint64_t)d, (cuuint64_t)(Pcap > 0 ? Pcap : 1), (cuuint64_t)L * B * Hkv};
+    const cuuint64_t str3[2] = {(cuuint64_t)d * 2, (cuuint64_t)(Pcap > 0 ? Pcap : 1) * d * 2};
+    const cuuint32_t box4[4] = {64, 1, (cuuint32_t)kBN, 1};
+    const cuuint32_t es4[4] = {1, 1, 1, 1};
+    const cuuint64_t dims4[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)N, (cuuint64_t)L * B};
+    const cuuint64_t str4[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2, (cuuint64_t)N * Hkv * d * 2};
+    const void* kc = Pcap > 0 ? k_cache : k_tree;  // with no prefix the cache maps are never used
+    const void* vc = Pcap > 0 ? v_cache : v_tree;
+    CUresult r = CUDA_SUCCESS;
+    r = r != CUDA_SUCCESS ? r
+                          : enc(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kc), dims3, str3, box3,
+                                es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = r != CUDA_SUCCESS ? r
+                          : enc(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(vc), dims3, str3, box3,
+                                es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = r != CUDA_SUCCESS ? r
+                          : enc(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k_tree), dims4, str4,
+                                box4, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = r != CUDA_SUCCESS ? r
+                          : enc(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v_tree), dims4, str4,
+                                box4, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    k_attn_order<<<1, 256, 0, st>>>(B, prefix_len, perm, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const bool bf = out == DDT_BF16;
+    switch (d) {
+        case 64: return bf ? attn_tc_go<64, __nv_bfloat16>(prm, maps, st) : attn_tc_go<64, float>(prm, maps, st);
+        case 128: return bf ? attn_tc_go<128, __nv_bfloat16>(prm, maps, st) : attn_tc_go<128, float>(prm, maps, st);
+        case 256: return bf ? attn_tc_go<256, __nv_bfloat16>(prm, maps, st) : attn_tc_go<256, float>(prm, maps, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ddt

@@ -35,6 +35,13 @@ cudaError_t launch_attn_simt(int L, int B, int N, int Hq, int Hkv, int d, int Pc
                              const void* v_cache, const int32_t* prefix_len, const int32_t* n_nodes,
                              const uint32_t* anc, float scale, void* o, int32_t* status, cudaStream_t st);
 
+size_t attn_tc_ws_bytes(int L, int B, int N, int Hq, int Hkv, int d, int Pcap);
+bool attn_tc_supported(int d, ddt_dtype in);
+cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out, const void* q,
+                           const void* k_tree, const void* v_tree, const void* k_cache, const void* v_cache,
+                           const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
+                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st);
+
 size_t gdn_smem_bytes(int N, int dk, int dv);
 cudaError_t launch_gdn_tree(int L, int B, int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in,
                             ddt_dtype out, const void* x, const void* conv_w, const void* conv_state,
