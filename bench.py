@@ -164,6 +164,19 @@ def round_bytes(r):
     return float(total)
 
 
+def workload_desc(c):
+    parts = [c["name"] + ":", f"B={c['B']}, D={c['D']}, V={c['V']}, budget {c['budget']}, top-k {c['top_k']}"]
+    if "P_lo" in c:
+        parts.append(f"P~U[{c['P_lo']},{c['P_hi']}]")
+    elif c.get("P"):
+        parts.append(f"P={c['P']}")
+    if c.get("Lf"):
+        parts.append(f"{c['Lf']} attn layers Hq{c['Hq']}/Hkv{c['Hkv']}/d{c['d']}")
+    if c.get("Lg"):
+        parts.append(f"{c['Lg']} GDN layers Hk{c['Hk']}/Hv{c['Hv']}/dk=dv={c['dk']}")
+    return ", ".join(parts)
+
+
 # --------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local):
     from tree_speculative_decoding_02_gb300 import ddt, synth
@@ -177,7 +190,8 @@ def run_ours(args, rank, world, local):
     st = torch.cuda.current_stream()
     ev = {k: [] for k in KERNELS}
 
-    # split the five calls so each can be bracketed by events on the launching stream
+    # the five calls, each bracketed by events on the launching stream; a workload
+    # without attention (or GDN) layers has no such call in its round
     def step(timed):
         r.restore_prefix()
         marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if timed else None
@@ -188,24 +202,28 @@ def run_ours(args, rank, world, local):
                            workspace=r.build_ws)
         if timed:
             marks[1].record(st)
-        a = r.attn
-        ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, r.prefix_len, r.tree["n_nodes"],
-                          r.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out=r.attn_o, status=r.attn_status,
-                          workspace=r.attn_ws)
+        kw = {}
+        if r.Lf:
+            a = r.attn
+            ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, r.prefix_len, r.tree["n_nodes"],
+                              r.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out=r.attn_o, status=r.attn_status,
+                              workspace=r.attn_ws)
+            kw.update(k_tree=a.k_tree, v_tree=a.v_tree, k_cache=a.k_cache, v_cache=a.v_cache)
         if timed:
             marks[2].record(st)
-        g = r.gdn
-        ddt.ddt_tree_gdn(g.x, g.conv_w, g.conv_state, g.beta, g.decay, g.S, r.tree["parent"], r.tree["n_nodes"],
-                         Hk=c["Hk"], out=r.gdn_o, status=r.gdn_status)
+        if r.Lg:
+            g = r.gdn
+            ddt.ddt_tree_gdn(g.x, g.conv_w, g.conv_state, g.beta, g.decay, g.S, r.tree["parent"],
+                             r.tree["n_nodes"], Hk=c["Hk"], out=r.gdn_o, status=r.gdn_status)
+            kw.update(x=g.x, conv_w=g.conv_w, beta=g.beta, decay=g.decay, S=g.S, conv_state=g.conv_state,
+                      Hk=c["Hk"])
         if timed:
             marks[3].record(st)
         ddt.ddt_walk_accept(r.tree["token"], r.tree["parent"], r.tree["n_nodes"], r.A - 1,
                             target_logits=r.target_logits, out=r.walk, workspace=r.walk_ws)
         if timed:
             marks[4].record(st)
-        ddt.ddt_commit(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, out=r.commit, k_tree=a.k_tree,
-                       v_tree=a.v_tree, k_cache=a.k_cache, v_cache=a.v_cache, x=g.x, conv_w=g.conv_w, beta=g.beta,
-                       decay=g.decay, S=g.S, conv_state=g.conv_state, Hk=c["Hk"])
+        ddt.ddt_commit(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, out=r.commit, **kw)
         if timed:
             marks[5].record(st)
             for i, k in enumerate(KERNELS):
@@ -283,17 +301,16 @@ def run_ours(args, rank, world, local):
         peaks = json.load(open(pk_path))
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     tc_peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
-    fl, by = attn_flops_bytes(r)
+    fl, by = attn_flops_bytes(r) if r.Lf else (0.0, 0.0)
     attn_ms = per_kernel["attn"]
-    tflops = fl / (attn_ms / 1e3) / 1e12
+    tflops = fl / (attn_ms / 1e3) / 1e12 if r.Lf else 0.0
     rb = round_bytes(r)
     step_ms = ms / args.steps
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "batched-round-bf16: B=32, D=15, V=151936, budget 64, top-k 8, "
-                               "P~U[1024,32768], 16 attn layers Hq24/Hkv4/d256, 48 GDN layers Hk16/Hv48/dk=dv=128",
+        "config": {"workload": workload_desc(cfg),
                    "B": cfg["B"], "budget": cfg["budget"], "nodes_per_round": nodes_per_step,
                    "prefix_total": int(r.prefix0.sum()),
                    "l2": "inputs larger than L2 (tens of GB per round)", "parallelism": f"replicas x{world}"},
@@ -307,7 +324,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": 10 * args.steps,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg:
         out["cpu_baseline"] = cpu_baseline(r, seconds=args.cpu_seconds)
     return out
 

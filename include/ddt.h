@@ -172,8 +172,11 @@ ddt_status ddt_tree_attn(int n_layers, int B, int N, int Hq, int Hkv, int d, int
  *   beta, decay [L][B][N][Hv] fp32;  S [L][B][Hv][dv][dk] fp32 (read only)
  *   parent [B][N], n_nodes [B] as written by ddt_build_tree
  *   o [L][B][N][Hv][dv] (out_dtype); padding rows are zeros.
- *   status [B]: DDT_ERR_TREE for a malformed parent array (outputs then zero).
- * Limits: dk, dv in {32, 64, 128}; 1 <= K <= 8; N <= 128; tree depth <= 32.
+ *   status [B]: DDT_ERR_TREE for a malformed parent array, DDT_ERR_UNSUPPORTED for a
+ *     tree deeper than the head-128 limit below (that request's outputs are then zero).
+ * Limits: dk, dv in {32, 64, 128} (dk = dv = 128 runs on the tensor cores and takes
+ * trees of depth <= 16, i.e. drafter depth <= 16; other sizes take depth <= 32);
+ * 1 <= K <= 8; N <= 128.
  * ------------------------------------------------------------------------------- */
 size_t ddt_tree_gdn_workspace(int n_layers, int B, int N, int Hk, int Hv, int dk, int dv);
 ddt_status ddt_tree_gdn(int n_layers, int B, int N, int Hk, int Hv, int dk, int dv, int conv_k,

@@ -86,3 +86,32 @@ def test_gdn_tree_workload_sampled():
                             tree["n_nodes"][0], 16, 48, h)
         err = normwise(got[l, 0, :, h], u["o"], axes=-1)
         assert err.max() <= TOL, (l, h, err.max())
+
+
+@pytest.mark.parametrize("Hk,Hv,dtype,budget", [(2, 2, torch.bfloat16, 16), (1, 4, torch.float32, 64),
+                                                 (3, 6, torch.bfloat16, 0)])
+def test_gdn_head128_variants(Hk, Hv, dtype, budget):
+    """Head size 128 (tensor-core path): one or several value heads per key head, fp32 or
+    bf16 inputs, root-only trees."""
+    tree, _ = C.tree_from_logits(4, 2, 15, 3000, 8, budget)
+    gi = synth.gdn_inputs(2, 2, budget + 1, Hk, Hv, 128, 128, 4, workload=4, dtype=dtype)
+    r = _gpu(tree, gi, Hk)
+    _check(r["o"], _oracle(tree, gi, Hk), tree)
+    assert (r["status"].cpu() == 0).all()
+
+
+def test_gdn_head128_deep_chain():
+    """A 17-node chain (depth 16, the head-128 path's limit) runs; a 20-node chain (depth
+    19) is refused for that request."""
+    for n in (17, 20):
+        parent = np.array([[-1] + list(range(n - 1))], np.int32)
+        tree = {"parent": parent, "n_nodes": np.array([n], np.int32), "token": np.zeros((1, n), np.int32),
+                "depth": np.arange(n, dtype=np.int32)[None], "position": np.arange(n, dtype=np.int32)[None],
+                "anc": np.zeros((1, n, (n + 31) // 32), np.uint32)}
+        gi = synth.gdn_inputs(1, 1, n, 1, 2, 128, 128, 4, workload=4, dtype=torch.bfloat16)
+        r = _gpu(tree, gi, 1)
+        if n <= 17:
+            _check(r["o"], _oracle(tree, gi, 1), tree)
+            assert int(r["status"][0]) == 0
+        else:
+            assert int(r["status"][0]) == 2   # deeper than this path supports: refused per request

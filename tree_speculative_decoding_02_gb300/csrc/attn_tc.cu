@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
     using Cfg = TcCfg<D>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                           ~static_cast<uintptr_t>(1023));
+    // align to 1024 B by pointer arithmetic on the shared array (keeps the address space)
+    unsigned char* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* sQ = base;
     unsigned char* sRing = base + Cfg::kQBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * Cfg::kStageBytes);

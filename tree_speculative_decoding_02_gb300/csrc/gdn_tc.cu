@@ -1,0 +1,547 @@
+// gdn_tc.cu -- ddt_tree_gdn with the dense part on the tensor cores (kind::tf32).
+//
+// "DDTree on vLLM: candid research notes", sections "Why hybrid attention makes it hard"
+// and "Where the next step is": each node reads its parent's GDN and conv state and
+// writes scratch, never the committed state.  Rule: gated delta rule of Yang, Kautz and
+// Hatamizadeh, "Gated Delta Networks" (ICLR 2025), in the tree-masked "WY" form
+// described in gdn.cu (every term runs over the node's own ancestors only):
+//   u_t = b_t (v_t - g_t S0 k_t) - sum_{s in anc(t)} b_t G_ts (k_s . k_t) u_s
+//   o_t = g_t S0 q_t + sum_{s in anc(t)+t} G_ts (k_s . q_t) u_s
+// One CTA owns a (layer, request, key head) and the Hv/Hk value heads that read it:
+//   all warps   conv + SiLU + L2 norm of q and k for every node, written once as a tf32
+//               K-major tile [k rows | q rows] (128-byte swizzle); the (k_s . k_t) and
+//               (k_s . q_t) dot products along every ancestor chain.
+//   warp 0      TMA: each value head's committed state S0 (dv x dk fp32, key channel
+//               contiguous) into shared memory.
+//   warp 1      tcgen05.mma kind::tf32: D = S0 [k | q]^T, i.e. S0 k_t and S0 q_t for every
+//               node, into one of two TMEM buffers (lane = value channel).
+//   warps 4-7   per value channel (= TMEM lane): v_t by the conv along the path,
+//               u_t by forward substitution down the tree, o_t; written to global.
+// S0 is read once from HBM; no node state ever exists.  Waits are bounded.
+#include <cuda.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace ddt {
+
+namespace {
+
+constexpr int kDK = 128, kDV = 128;  // head sizes of this path
+constexpr int kMD = 16;              // deepest tree this path takes (drafter depth <= 16)
+constexpr int kThr = 384;   // warps 0 TMA, 1 MMA, 2-3 setup only, 4-11 epilogue
+constexpr int kEpi = 256;   // epilogue threads
+constexpr int kMaxK = 8;    // widest short conv
+
+struct GdnTcParams {
+    int L, B, N, Hk, Hv, R, K, C, QOFF, NPAD;
+    const void* x;
+    const void* conv_w;
+    const void* conv_state;
+    const float* beta;
+    const float* decay;
+    const int32_t* parent;
+    const int32_t* n_nodes;
+    void* o;
+    int32_t* status;
+};
+
+struct GdnSmem {
+    size_t s0, kq, u, kk, qk, ca, cb, tt, alist, small, bars, total;
+};
+
+__host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD) {
+    GdnSmem L;
+    size_t off = 0;
+    L.s0 = off;
+    off += (size_t)kDV * kDK * 4;            // S0 tile (64 KiB)
+    L.kq = off;
+    off += (size_t)NPAD * kDK * 4;           // [k | q] tile
+    L.u = off;
+    off += (size_t)N * kDV * 4;              // R -> u, one column per value channel
+    L.kk = off;
+    off += (size_t)N * kMD * 4;
+    L.qk = off;
+    off += (size_t)N * kMD * 4;
+    L.ca = off;
+    off += (size_t)N * kMD * 4;
+    L.cb = off;
+    off += (size_t)N * kMD * 4;
+    L.tt = off;
+    off += (size_t)N * kMaxK * 8;            // conv input row pointers
+    L.alist = off;
+    off += (size_t)N * kMD * 4;
+    L.small = off;
+    off += (size_t)N * 4 * 7;                // dep, par, qself, gcum, beta, decay, spare
+    off = (off + 7) & ~(size_t)7;
+    L.bars = off;
+    off += 128;
+    L.total = off + 1024;                    // alignment slack
+    return L;
+}
+
+__device__ __forceinline__ float silu_g(float z) { return z / (1.f + __expf(-z)); }
+
+// byte offset of element (row, col) of a K-major fp32 tile with 128-byte swizzle whose
+// column blocks of 32 elements are `rows * 128` bytes apart
+__device__ __forceinline__ uint32_t sw_off(int row, int col, int rows) {
+    const int blk = col >> 5, chunk = (col & 31) >> 2;
+    return blk * (rows * 128) + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 3) * 4;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+}  // namespace
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const __grid_constant__ CUtensorMap tm_s) {
+    extern __shared__ unsigned char smem_raw[];
+    // align to 1024 B by pointer arithmetic on the shared array (keeps the address space)
+    unsigned char* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int N = p.N;
+    const GdnSmem lay = gdn_tc_layout(N, p.NPAD);
+    unsigned char* sS0 = base + lay.s0;
+    unsigned char* sKQ = base + lay.kq;
+    float* ubuf = reinterpret_cast<float*>(base + lay.u);
+    float* skk = reinterpret_cast<float*>(base + lay.kk);
+    float* sqk = reinterpret_cast<float*>(base + lay.qk);
+    float* sca = reinterpret_cast<float*>(base + lay.ca);
+    float* scb = reinterpret_cast<float*>(base + lay.cb);
+    const Tin** taps = reinterpret_cast<const Tin**>(base + lay.tt);  // [N][K] conv input rows
+    int* alist = reinterpret_cast<int*>(base + lay.alist);
+    int* sdep = reinterpret_cast<int*>(base + lay.small);
+    int* spar = sdep + N;
+    float* sqself = reinterpret_cast<float*>(spar + N);
+    float* sg = sqself + N;
+    float* sbeta = sg + N;
+    float* sdec = sbeta + N;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + lay.bars);
+    uint64_t* full = bars;        // S0 landed
+    uint64_t* s_free = bars + 1;  // MMA done reading S0
+    uint64_t* d_full = bars + 2;  // [2] D ready
+    uint64_t* d_free = bars + 4;  // [2] epilogue done with D (kEpi arrivals)
+    uint64_t* drain = bars + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    int* err = abort_flag + 1;
+
+    const int g = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long lb = (long)l * p.B + b;
+    const int C = p.C, K = p.K;
+    const int nn = p.n_nodes[b];
+    const Tin* xb = static_cast<const Tin*>(p.x) + lb * N * C;
+    const Tin* csb = static_cast<const Tin*>(p.conv_state) + lb * (K - 1) * C;
+    const Tin* wl = static_cast<const Tin*>(p.conv_w) + (long)l * C * K;
+
+    if (tid == 0) {
+        *err = (nn < 1 || nn > N) ? DDT_ERR_TREE : DDT_OK;
+        *abort_flag = 0;
+    }
+    __syncthreads();
+    const int nv = (*err == DDT_OK) ? nn : 0;
+    // ---- tree check, ancestor lists, conv input rows (the node's path, newest last,
+    //      continued by the committed conv state past the root)
+    for (int n = tid; n < nv; n += kThr) {
+        const int pr = p.parent[(long)b * N + n];
+        spar[n] = pr;
+        if ((n == 0 && pr != -1) || (n > 0 && (pr < 0 || pr >= n))) atomicExch(err, DDT_ERR_TREE);
+    }
+    __syncthreads();
+    if (*err == DDT_OK) {
+        for (int n = tid; n < nn; n += kThr) {
+            int d = 0;
+            for (int a = spar[n]; a >= 0; a = spar[a]) {
+                if (d >= kMD) {
+                    atomicExch(err, DDT_ERR_UNSUPPORTED);
+                    break;
+                }
+                alist[n * kMD + d++] = a;
+            }
+            sdep[n] = d;
+            for (int q = 0; q < K; ++q) {
+                const int back = K - 1 - q;
+                const Tin* row;
+                if (back == 0) row = xb + (long)n * C;
+                else if (back <= d) row = xb + (long)alist[n * kMD + back - 1] * C;
+                else row = csb + (long)(K - 1 - (back - d)) * C;
+                taps[n * K + q] = row;
+            }
+        }
+    }
+    __syncthreads();
+    Tout* obase = static_cast<Tout*>(p.o) + lb * N * p.Hv * kDV;
+    if (*err != DDT_OK) {
+        if (tid == 0 && g == 0 && l == 0) p.status[b] = *err;
+        for (int hi = 0; hi < p.R; ++hi) {
+            const int h = g * p.R + hi;
+            for (int e = tid; e < N * kDV; e += kThr)
+                obase[((long)(e / kDV) * p.Hv + h) * kDV + e % kDV] = from_f32<Tout>(0.f);
+        }
+        return;
+    }
+
+    // ---- setup: barriers, TMEM, first S0 load
+    if (tid == 0) {
+        tc::mbar_init(full, 1);
+        tc::mbar_init(s_free, 1);
+        tc::mbar_init(d_full, 1);
+        tc::mbar_init(d_full + 1, 1);
+        tc::mbar_init(d_free, kEpi);
+        tc::mbar_init(d_free + 1, kEpi);
+        tc::mbar_init(drain, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    const int srow0 = (int)((lb * p.Hv + (long)g * p.R) * kDV);
+    if (tid == 0) {
+        tc::prefetch_tmap(&tm_s);
+        tc::mbar_expect_tx(full, kDV * kDK * 4);
+        for (int blk = 0; blk < kDK / 32; ++blk)
+            tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0);
+    }
+
+    // ---- conv + SiLU + L2 norm of q and k: half-warp per (node, q|k), 8 channels a lane
+    {
+        const int half = lane >> 4, sub = lane & 15;
+        const int c0 = (half == 0 ? g * kDK : p.Hk * kDK + g * kDK) + sub * 8;
+        float w[8][kMaxK];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+            for (int q = 0; q < kMaxK; ++q) w[ch][q] = (q < K) ? to_f32(wl[(long)(c0 + ch) * K + q]) : 0.f;
+        for (int n = warp; n < N; n += kThr / 32) {
+            float y[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) y[ch] = 0.f;
+            if (n < nn) {
+#pragma unroll
+                for (int q = 0; q < kMaxK; ++q) {
+                    if (q < K) {
+                        float in[8];
+                        load8(taps[n * K + q] + c0, in);
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) y[ch] = fmaf(w[ch][q], in[ch], y[ch]);
+                    }
+                }
+                float ss = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    y[ch] = silu_g(y[ch]);
+                    ss = fmaf(y[ch], y[ch], ss);
+                }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+                const float sc = rsqrtf(ss + 1e-6f) * (half == 0 ? rsqrtf((float)kDK) : 1.f);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) y[ch] *= sc;
+            }
+            const int row = half == 0 ? p.QOFF + n : n;
+            const int col = sub * 8;
+            *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(y[0], y[1], y[2], y[3]);
+            *reinterpret_cast<float4*>(sKQ + sw_off(row, col + 4, p.NPAD)) = make_float4(y[4], y[5], y[6], y[7]);
+        }
+        // padding rows of the tile
+        for (int e = tid; e < p.NPAD * (kDK / 4); e += kThr) {
+            const int row = e / (kDK / 4), col = (e % (kDK / 4)) * 4;
+            const bool used = row < N || (row >= p.QOFF && row < p.QOFF + N);
+            if (!used) *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    tc::fence_proxy_async();
+    __syncthreads();
+
+    // ---- dot products along ancestor chains (k_s . k_t, k_s . q_t; self q_t . k_t)
+    for (int e = tid; e < nn * (kMD + 1); e += kThr) {
+        const int t = e / (kMD + 1), m = e % (kMD + 1);
+        const int dep = sdep[t];
+        if (m > dep) continue;
+        const int s = (m == dep) ? t : alist[t * kMD + m];
+        float dkk = 0.f, dqk = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < kDK; c += 4) {
+            const float4 ks = *reinterpret_cast<const float4*>(sKQ + sw_off(s, c, p.NPAD));
+            const float4 kt = *reinterpret_cast<const float4*>(sKQ + sw_off(t, c, p.NPAD));
+            const float4 qt = *reinterpret_cast<const float4*>(sKQ + sw_off(p.QOFF + t, c, p.NPAD));
+            dkk = fmaf(ks.x, kt.x, fmaf(ks.y, kt.y, fmaf(ks.z, kt.z, fmaf(ks.w, kt.w, dkk))));
+            dqk = fmaf(ks.x, qt.x, fmaf(ks.y, qt.y, fmaf(ks.z, qt.z, fmaf(ks.w, qt.w, dqk))));
+        }
+        if (m == dep) {
+            sqself[t] = dqk;
+        } else {
+            skk[t * kMD + m] = dkk;
+            sqk[t * kMD + m] = dqk;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ S0 loads
+        if (lane == 0) {
+            for (int hi = 1; hi < p.R; ++hi) {
+                if (!tc::mbar_wait(s_free, (hi - 1) & 1, abort_flag)) break;
+                tc::mbar_expect_tx(full, kDV * kDK * 4);
+                for (int blk = 0; blk < kDK / 32; ++blk)
+                    tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0 + hi * kDV);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_tf32(128, p.NPAD, false, false);
+            const uint32_t sSa = tc::smem_u32(sS0), sKa = tc::smem_u32(sKQ);
+            for (int hi = 0; hi < p.R; ++hi) {
+                const int db = hi & 1;
+                if (!tc::mbar_wait(full, hi & 1, abort_flag)) break;
+                if (hi >= 2 && !tc::mbar_wait(d_free + db, ((hi - 2) >> 1) & 1, abort_flag)) break;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kDK / 8; ++kk) {
+                    const uint32_t aoff = (kk >> 2) * (kDV * 128) + (kk & 3) * 32;
+                    const uint32_t boff = (kk >> 2) * (p.NPAD * 128) + (kk & 3) * 32;
+                    tc::mma_tf32_ss(tmem + db * p.NPAD, tc::desc_sw128(sSa + aoff, 16, 1024),
+                                    tc::desc_sw128(sKa + boff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(s_free);
+                tc::mma_commit(d_full + db);
+            }
+            tc::mma_commit(drain);
+            const long long t0 = clock64();
+            while (!tc::mbar_try(drain, 0) && clock64() - t0 < tc::kWaitCycles) {
+            }
+        }
+    } else if (warp >= 4) {
+        // --------------------------------------------------------------- epilogue (8 warps)
+        const int e = tid - 128;
+        const int j = e & (kDV - 1);  // value channel = TMEM lane
+        const int quad = e >> 7;      // which half of the nodes
+        const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        bool dead = false;
+        for (int hi = 0; hi < p.R; ++hi) {
+            const int h = g * p.R + hi, db = hi & 1;
+            // gates of this head; per-node decay products and chain coefficients
+            //   A(t, s_m) = b_t G(t, s_m) (k_s.k_t),  B(t, s_m) = G(t, s_m) (k_s.q_t)
+            if (e < nn) {
+                sdec[e] = p.decay[(lb * N + e) * p.Hv + h];
+                sbeta[e] = p.beta[(lb * N + e) * p.Hv + h];
+            }
+            named_bar(1, kEpi);
+            if (e < nn) {
+                const int dep = sdep[e];
+                float gam = sdec[e];
+                const float bt = sbeta[e];
+                for (int m = 0; m < dep; ++m) {
+                    const int s = alist[e * kMD + m];
+                    sca[e * kMD + m] = bt * gam * skk[e * kMD + m];
+                    scb[e * kMD + m] = gam * sqk[e * kMD + m];
+                    gam *= sdec[s];
+                }
+                sg[e] = gam;
+            }
+            named_bar(1, kEpi);
+            // M = B (I + A)^-1 one row per node, by back substitution along the node's own
+            // path p_0 = t, p_k = k-th ancestor:  M(t, p_k) = B(t, p_k) - sum_{i<k} M(t, p_i)
+            // A(p_i, p_k), M(t, t) = q_t.k_t.  Then o_t = g_t S0 q_t + sum_k M(t, p_k) R_{p_k}.
+            if (e < nn) {
+                const int dep = sdep[e];
+                float mrow[kMD + 1];
+                mrow[0] = sqself[e];
+#pragma unroll
+                for (int k = 1; k <= kMD; ++k) {
+                    if (k > dep) break;
+                    float acc = scb[e * kMD + k - 1];
+                    acc = fmaf(-mrow[0], sca[e * kMD + k - 1], acc);
+#pragma unroll
+                    for (int i = 1; i < k; ++i) {
+                        const int pi = alist[e * kMD + i - 1];
+                        acc = fmaf(-mrow[i], sca[pi * kMD + (k - i - 1)], acc);
+                    }
+                    mrow[k] = acc;
+                }
+#pragma unroll
+                for (int k = 1; k <= kMD; ++k) {
+                    if (k > dep) break;
+                    scb[e * kMD + k - 1] = mrow[k];  // own row only: B(t, .) is not read by others
+                }
+            }
+            named_bar(1, kEpi);
+            // after a timeout the warp keeps meeting the named barriers but does no work
+            if (!dead) dead = !__all_sync(kFull, tc::mbar_wait(d_full + db, (hi >> 1) & 1, abort_flag));
+            if (dead) {
+                named_bar(1, kEpi);
+                named_bar(1, kEpi);
+                continue;
+            }
+            tc::tc_fence_after();
+            const uint32_t dcol = tmem + lane_base + db * p.NPAD;
+            // pass A: R_t = b_t (v_t - g_t (S0 k_t)); v_t by the conv along the node's path
+            const int cv = 2 * p.Hk * kDK + h * kDV + j;
+            float wv[kMaxK];
+#pragma unroll
+            for (int q = 0; q < kMaxK; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
+            for (int t0 = 0; t0 < nn; t0 += 16) {
+                uint32_t ks[16];
+                tmem_ld16(dcol + t0, ks);
+                float vin[8][kMaxK];
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    const int t = min(t0 + 2 * uu + quad, nn - 1);
+#pragma unroll
+                    for (int q = 0; q < kMaxK; ++q) vin[uu][q] = (q < K) ? to_f32(taps[t * K + q][cv]) : 0.f;
+                }
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    const int t = t0 + 2 * uu + quad;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kMaxK; ++q) acc = fmaf(wv[q], vin[uu][q], acc);
+                    if (t < nn)
+                        ubuf[t * kDV + j] = sbeta[t] * (silu_g(acc) - sg[t] * __uint_as_float(ks[2 * uu + quad]));
+                }
+            }
+            named_bar(1, kEpi);
+            // pass C: outputs as independent sums over each node's own path
+            for (int t0 = 0; t0 < N; t0 += 16) {
+                uint32_t qs[16];
+                if (t0 < nn) {
+                    tmem_ld16(dcol + p.QOFF + t0, qs);
+                    tc::tmem_wait_ld();
+                }
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    const int t = t0 + 2 * uu + quad;
+                    if (t >= N) break;
+                    float ot = 0.f;
+                    if (t < nn) {
+                        const int dep = sdep[t];
+                        ot = fmaf(sg[t], __uint_as_float(qs[2 * uu + quad]), sqself[t] * ubuf[t * kDV + j]);
+                        for (int a = 0; a < dep; ++a)
+                            ot = fmaf(scb[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot);
+                    }
+                    obase[((long)t * p.Hv + h) * kDV + j] = from_f32<Tout>(ot);
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(d_free + db);
+            named_bar(1, kEpi);  // ubuf and the per-head arrays are rewritten by the next head
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+    if (tid == 0 && *abort_flag) atomicExch(p.status + b, (int)DDT_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------------------ host
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn_gdn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+int qoff_of(int N) { return (N + 15) / 16 * 16; }
+int npad_of(int N) { return (qoff_of(N) + N + 15) / 16 * 16; }
+
+}  // namespace
+
+bool gdn_tc_supported(int N, int Hk, int Hv, int dk, int dv, int K) {
+    if (dk != kDK || dv != kDV || K < 1 || K > kMaxK || Hv % Hk != 0 || N > kEpi) return false;
+    if (npad_of(N) > 256) return false;
+    return gdn_tc_layout(N, npad_of(N)).total <= 227 * 1024;
+}
+
+template <typename Tin, typename Tout>
+static cudaError_t gdn_tc_go(const GdnTcParams& prm, const CUtensorMap& map, cudaStream_t st) {
+    const size_t smem = gdn_tc_layout(prm.N, prm.NPAD).total;
+    cudaError_t e = cudaFuncSetAttribute(k_gdn_tc<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_gdn_tc<Tin, Tout><<<dim3(prm.Hk, prm.B, prm.L), kThr, smem, st>>>(prm, map);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype in, ddt_dtype out, const void* x,
+                          const void* conv_w, const void* conv_state, const float* beta, const float* decay,
+                          const float* S, const int32_t* parent, const int32_t* n_nodes, void* o, int32_t* status,
+                          cudaStream_t st) {
+    EncodeTiledFn enc = encode_fn_gdn();
+    if (!enc) return cudaErrorNotSupported;
+    GdnTcParams prm;
+    prm.L = L;
+    prm.B = B;
+    prm.N = N;
+    prm.Hk = Hk;
+    prm.Hv = Hv;
+    prm.R = Hv / Hk;
+    prm.K = K;
+    prm.C = 2 * Hk * kDK + Hv * kDV;
+    prm.QOFF = qoff_of(N);
+    prm.NPAD = npad_of(N);
+    prm.x = x;
+    prm.conv_w = conv_w;
+    prm.conv_state = conv_state;
+    prm.beta = beta;
+    prm.decay = decay;
+    prm.parent = parent;
+    prm.n_nodes = n_nodes;
+    prm.o = o;
+    prm.status = status;
+    // committed states as a 2-D fp32 tensor: rows (layer, request, value head, value
+    // channel), columns the key channel; boxes of 32 columns x 128 rows
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)L * B * Hv * kDV};
+    const cuuint64_t strides[1] = {(cuuint64_t)kDK * 4};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kDV};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(S), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // status words start at DDT_OK; CTAs only ever write errors into them
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t) * B, st);
+    if (e != cudaSuccess) return e;
+    const bool ib = in == DDT_BF16, ob = out == DDT_BF16;
+    if (ib && ob) return gdn_tc_go<__nv_bfloat16, __nv_bfloat16>(prm, map, st);
+    if (ib) return gdn_tc_go<__nv_bfloat16, float>(prm, map, st);
+    if (ob) return gdn_tc_go<float, __nv_bfloat16>(prm, map, st);
+    return gdn_tc_go<float, float>(prm, map, st);
+}
+
+}  // namespace ddt

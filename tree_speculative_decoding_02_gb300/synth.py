@@ -24,9 +24,9 @@ WORKLOADS = {
     2: dict(name="build-walk-bf16", B=1, D=15, V=151936, top_k=8, budgets=(32, 64),
             dtype=torch.bfloat16, logit_std=3.0, boost=6.0),
     3: dict(name="tree-attn-bf16", B=1, P=4096, Lf=16, Hq=24, Hkv=4, d=256, budget=64,
-            D=15, V=151936, top_k=8, dtype=torch.bfloat16),
-    4: dict(name="tree-gdn-bf16", B=1, Lg=48, Hk=16, Hv=48, dk=128, dv=128, conv_k=4, budget=64,
-            D=15, V=151936, top_k=8, dtype=torch.bfloat16),
+            D=15, V=151936, top_k=8, dtype=torch.bfloat16, logit_std=3.0, boost=6.0),
+    4: dict(name="tree-gdn-bf16", B=1, P=0, Lg=48, Hk=16, Hv=48, dk=128, dv=128, conv_k=4, budget=64,
+            D=15, V=151936, top_k=8, dtype=torch.bfloat16, logit_std=3.0, boost=6.0),
     5: dict(name="batched-round-bf16", B=32, P_lo=1024, P_hi=32768, D=15, V=151936, top_k=8, budget=64,
             Lf=16, Hq=24, Hkv=4, d=256, Lg=48, Hk=16, Hv=48, dk=128, dv=128, conv_k=4,
             dtype=torch.bfloat16, logit_std=3.0, boost=6.0),
