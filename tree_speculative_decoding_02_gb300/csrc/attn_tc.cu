@@ -15,17 +15,17 @@
 //               the ragged last tile is shifted to end exactly at prefix_len, so no row
 //               past the prefix is ever read (positions < 0 are zero-filled by TMA).
 //               Tree tiles come from a 4-D map (d, kv head, node, layer*B).
-//   warp 1      MMA issuer: S_j = Q K_j^T (bf16) into one of two TMEM buffers; O += P_j V_j
-//               (fp16) with P_j read back from TMEM (written over S_j) and V_j MN-major in
-//               shared memory.
-//   warps 4-7   softmax: one TMEM lane (= query row) per thread, ancestor mask on tree
-//               tiles, running max with lazy O rescaling (only when the max grows by
-//               more than 2^8), P to TMEM as fp16; epilogue O / l to global (or a
+//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers (Q is the A operand,
+//               kept in TMEM); O += P_j V_j with P_j read back from TMEM (written over S_j)
+//               and V_j MN-major in shared memory.  P_j is stored as two bf16 parts,
+//               P = P_hi + P_lo, and both are applied (two MMAs): bf16 P alone would leave
+//               ~3e-3 relative error in O, the pair ~1e-5.  The tensor core has the time:
+//               this kernel is bound by the softmax and data movement, not the MMAs.
+//   warps 4-11  softmax: two warpgroups per row set, each taking half of every S tile's
+//               columns and half of O's; ancestor mask on tree tiles, running max with
+//               lazy O rescaling (only when the max grows by more than 2^8); zeroes V rows
+//               of padding tree nodes before their MMA; epilogue O / l to global (or a
 //               split-KV partial that k_attn_merge combines).
-//   warps 8-11  V converters: each landed V tile is rewritten in place from bf16 to fp16
-//               (exact for |v| in [2^-14, 65504]) and padding tree rows are zeroed.  P in
-//               fp16 (11-bit significand) keeps the output within ~5e-4 of exact, where
-//               bf16 P (8 bits) would give ~3e-3; the conversion costs no tensor work.
 // Every mbarrier wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees TMEM, and reports DDT_ERR_TIMEOUT in the request's status word.
 #include <cuda.h>
@@ -43,7 +43,6 @@ namespace {
 
 constexpr int kBM = 128;     // query rows per CTA (TMEM lanes)
 constexpr int kBN = 64;      // keys per tile
-constexpr int kStages = 4;   // K/V ring depth (K and V tiles alternate)
 constexpr float kTau = 8.f;  // rescale O only when the row max grows by more than 2^kTau
 
 struct TcParams {
@@ -60,17 +59,23 @@ struct TcParams {
     float scale_log2;
 };
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;  // 0 TMA, 1 MMA, 2-3 setup, 4-11 softmax
 
 template <int D>
 struct TcCfg {
     static constexpr int kBlocks = D / 64;              // 128-byte-swizzle column blocks
-    static constexpr int kQBytes = kBM * D * 2;
     static constexpr int kStageBytes = kBN * D * 2;
-    static constexpr int kOCol = 2 * kBN;                // O accumulator column in TMEM
-    static constexpr int kTmemCols = (2 * kBN + D) <= 256 ? 256 : 512;
-    static constexpr int kBarBytes = 256;
-    static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + kBarBytes;
+    // K/V ring depth (K and V tiles alternate): as deep as shared memory allows, so that
+    // about three tiles of keys are in flight per CTA
+    static constexpr int kStages = D == 256 ? 6 : 8;
+    // TMEM columns: S double buffer [0, 2 kBN), O [kOCol, kOCol + D), Q (bf16, two per
+    // column, the A operand of S = Q K^T) [kQCol, kQCol + D/2)
+    static constexpr int kOCol = 2 * kBN;
+    static constexpr int kQCol = kOCol + D;
+    static constexpr int kTmemCols = (kQCol + D / 2) <= 256 ? 256 : 512;
+    static constexpr int kBarBytes = 512;
+    static constexpr int kXchBytes = 4096;  // softmax halves: tile row max (x2 parity), row sum
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kXchBytes;
 };
 
 struct Tile {
@@ -104,10 +109,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
 
 template <typename Tout>
 __device__ __forceinline__ void store_row32(Tout* dst, const float* v);
@@ -139,8 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     // align to 1024 B by pointer arithmetic on the shared array (keeps the address space)
     unsigned char* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    unsigned char* sQ = base;
-    unsigned char* sRing = base + Cfg::kQBytes;
+    constexpr int kStages = Cfg::kStages;
+    unsigned char* sRing = base;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * Cfg::kStageBytes);
     uint64_t* full = bars;                 // [kStages] TMA landed
     uint64_t* empty = bars + kStages;      // [kStages] MMA done with the stage
@@ -148,12 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 2;         // [2] P_j in TMEM (128 arrivals)
     uint64_t* o_done = p_full + 2;         // one completion per PV
     uint64_t* drain = o_done + 1;
-    uint64_t* v_ready = drain + 1;         // [kStages] V tile converted to fp16 (128 arrivals)
     // Single-phase barrier for the epilogue: when the softmax reaches it, o_done may
     // still lack the last two completions, which a parity wait cannot tell apart.
-    uint64_t* o_final = v_ready + kStages;
+    uint64_t* o_final = drain + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    float* xch = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bars) + Cfg::kBarBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int x = blockIdx.x;
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    // ---- setup: barriers, TMEM, Q tile (manual 128-byte swizzle)
+    // ---- setup: barriers, TMEM, Q rows into TMEM
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             tc::mbar_init(full + i, 1);
@@ -208,11 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::mbar_init(s_full, 1);
         tc::mbar_init(s_full + 1, 1);
-        tc::mbar_init(p_full, 128);
-        tc::mbar_init(p_full + 1, 128);
+        tc::mbar_init(p_full, 256);
+        tc::mbar_init(p_full + 1, 256);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(drain, 1);
-        for (int i = 0; i < kStages; ++i) tc::mbar_init(v_ready + i, 128);
         tc::mbar_init(o_final, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -227,25 +227,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::prefetch_tmap(&tm_kt);
         tc::prefetch_tmap(&tm_vt);
     }
-    {
-        constexpr int kChunks = D / 8;  // 16-byte chunks per row
-        for (int e = tid; e < kBM * kChunks; e += kThreads) {
-            const int r = e / kChunks, ch = e % kChunks;
-            const int R = mt * kBM + r;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (R < p.N * p.G) {
-                const int node = R / p.G, h = g * p.G + R % p.G;
-                if (node < nn) v = __ldg(reinterpret_cast<const uint4*>(p.q + ((lb * p.N + node) * p.Hq + h) * D) + ch);
-            }
-            const int blk = ch >> 3, jj = ch & 7;
-            *reinterpret_cast<uint4*>(sQ + blk * (kBM * 128) + r * 128 + ((jj ^ (r & 7)) << 4)) = v;
-        }
-    }
-    tc::fence_proxy_async();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Q rows into TMEM (lane = query row): the softmax warps, half hf writes columns
+    // [hf D/4, (hf+1) D/4) of the packed bf16 row
+    if (warp >= 4 && warp < 12) {
+        const int hf = (warp - 4) >> 2, ws = (warp - 4) & 3, r = 32 * ws + lane;
+        const int R = mt * kBM + r;
+        const __nv_bfloat16* qrow = nullptr;
+        if (R < p.N * p.G) {
+            const int node = R / p.G, h = g * p.G + R % p.G;
+            if (node < nn) qrow = p.q + ((lb * p.N + node) * p.Hq + h) * D;
+        }
+        const uint32_t qaddr = tmem + (static_cast<uint32_t>(32 * ws) << 16) + Cfg::kQCol + hf * (D / 4);
+#pragma unroll
+        for (int cb = 0; cb < D / 4; cb += 16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (qrow) v = __ldg(reinterpret_cast<const uint4*>(qrow + hf * (D / 2) + 2 * (cb + i)));
+                w[i] = v.x;
+                w[i + 1] = v.y;
+                w[i + 2] = v.z;
+                w[i + 3] = v.w;
+            }
+            tc::tmem_st16(qaddr + cb, w);
+        }
+        tc::tmem_wait_st();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
@@ -281,19 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, false, false);
-            constexpr uint32_t idesc_pv = tc::idesc_f16(kBM, D, false, true);
-            const uint32_t sQa = tc::smem_u32(sQ), sRa = tc::smem_u32(sRing);
+            constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, D, false, true);
+            const uint32_t sRa = tc::smem_u32(sRing);
             auto pv = [&](int i) -> bool {
                 if (!tc::mbar_wait(p_full + (i & 1), (i >> 1) & 1, abort_flag)) return false;
                 const int u = 2 * i + 1, st = u % kStages;
-                if (!tc::mbar_wait(v_ready + st, (u / kStages) & 1, abort_flag)) return false;
+                if (!tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag)) return false;
                 tc::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // V tile: 16 keys = two 8-row swizzle atoms down the K dimension
-                    const uint64_t bdesc = tc::desc_sw128(sRa + st * Cfg::kStageBytes + kk * 2048, kBN * 128, 1024);
-                    tc::mma_f16_ts(tmem + Cfg::kOCol, tmem + (i & 1) * kBN + kk * 8, bdesc, idesc_pv,
-                                   (i > 0 || kk > 0) ? 1u : 0u);
+                for (int part = 0; part < 2; ++part) {  // P_hi, then P_lo
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        // V tile: 16 keys = two 8-row swizzle atoms down the K dimension
+                        const uint64_t bdesc =
+                            tc::desc_sw128(sRa + st * Cfg::kStageBytes + kk * 2048, kBN * 128, 1024);
+                        tc::mma_f16_ts(tmem + Cfg::kOCol, tmem + (i & 1) * kBN + part * (kBN / 2) + kk * 8, bdesc,
+                                       idesc_pv, (i > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 tc::mma_commit(empty + st);
                 tc::mma_commit(o_done);
@@ -309,9 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qoff = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                     const uint32_t koff = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-                    tc::mma_f16_ss(tmem + (j & 1) * kBN, tc::desc_sw128(sQa + qoff, 16, 1024),
+                    tc::mma_f16_ts(tmem + (j & 1) * kBN, tmem + Cfg::kQCol + kk * 8,
                                    tc::desc_sw128(sRa + st * Cfg::kStageBytes + koff, 16, 1024), idesc_qk,
                                    kk > 0 ? 1u : 0u);
                 }
@@ -323,9 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(drain);
             drain_wait(drain, 0);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------------ softmax
-        const int ws = warp - 4, r = 32 * ws + lane;
+        // Two warpgroups share each row: half hf takes key columns [32 hf, 32 hf + 32) of
+        // every S tile and value columns [hf D/2, (hf+1) D/2) of O.  The tile's row max is
+        // exchanged through shared memory, so both halves keep the same reference max.
+        const int hf = (warp - 4) >> 2, ws = (warp - 4) & 3, r = 32 * ws + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * ws) << 16;
         const int R = mt * kBM + r;
         const bool in_rows = R < p.N * p.G;
@@ -337,49 +359,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < T; ++j) {
             const Tile t = tile_of(j, n_pre, c0, c1, ragged);
-            ok = tc::mbar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag);
-            if (!__all_sync(kFull, ok)) {
-                ok = false;
-                break;
-            }
-            tc::tc_fence_after();
-            uint32_t sr[2][32];
-            tc::tmem_ld32(tmem + lane_base + (j & 1) * kBN, sr[0]);
-            tc::tmem_ld32(tmem + lane_base + (j & 1) * kBN + 32, sr[1]);
-            tc::tmem_wait_ld();
-            uint64_t vis;
-            if (!t.tree) {
-                const int skip = t.lo - t.y;  // leading keys already seen (ragged last tile)
-                vis = skip <= 0 ? ~0ull : (~0ull << skip);
-            } else if (live) {
-                const int w0 = t.y >> 5;
-                const uint32_t lo32 = anc_row[w0];
-                const uint32_t hi32 = (w0 + 1 < p.W) ? anc_row[w0 + 1] : 0u;
-                vis = static_cast<uint64_t>(lo32) | (static_cast<uint64_t>(hi32) << 32);
-            } else {
-                vis = 0ull;
-            }
-            float sv[64];
+            if (ok) ok = tc::mbar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag);
+            ok = __all_sync(kFull, ok);
+            float sv[32];
             float mtile = -INFINITY;
+            if (ok) {
+                tc::tc_fence_after();
+                uint32_t sr[32];
+                tc::tmem_ld32(tmem + lane_base + (j & 1) * kBN + 32 * hf, sr);
+                tc::tmem_wait_ld();
+                uint32_t vis;
+                if (!t.tree) {
+                    const int skip = t.lo - t.y - 32 * hf;  // keys of this half already seen
+                    vis = skip <= 0 ? ~0u : (skip >= 32 ? 0u : (~0u << skip));
+                } else {
+                    const int w = (t.y >> 5) + hf;
+                    vis = (live && w < p.W) ? anc_row[w] : 0u;
+                }
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float raw = __uint_as_float(sr[c >> 5][c & 31]);
-                sv[c] = ((vis >> c) & 1ull) ? raw * p.scale_log2 : -INFINITY;
-                mtile = fmaxf(mtile, sv[c]);
+                for (int c = 0; c < 32; ++c) {
+                    sv[c] = ((vis >> c) & 1u) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
+                    mtile = fmaxf(mtile, sv[c]);
+                }
             }
+            // row max of the whole tile: exchange with the other half
+            float* xm = xch + (j & 1) * 256;
+            xm[hf * 128 + r] = mtile;
+            tc::named_bar(1, 256);
+            mtile = fmaxf(mtile, xm[(hf ^ 1) * 128 + r]);
+            if (!ok) continue;
             // lazy rescale: only when the max grows by more than 2^kTau
             const bool grow = mtile > m_used + kTau;
             const bool need = grow && (m_used != -INFINITY);  // O already holds this row's data
             if (__any_sync(kFull, need)) {
-                ok = tc::mbar_wait(o_done, (j - 1) & 1, abort_flag);
-                if (!__all_sync(kFull, ok)) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(kFull, tc::mbar_wait(o_done, (j - 1) & 1, abort_flag));
+                if (!ok) continue;
                 tc::tc_fence_after();
                 const float f = need ? tc::ex2(m_used - mtile) : 1.f;
 #pragma unroll 1
-                for (int cb = 0; cb < D; cb += 32) {
+                for (int cb = hf * (D / 2); cb < (hf + 1) * (D / 2); cb += 32) {
                     uint32_t ov[32];
                     tc::tmem_ld32(tmem + lane_base + Cfg::kOCol + cb, ov);
                     tc::tmem_wait_ld();
@@ -391,30 +409,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (need) l_run *= f;
             }
             if (grow) m_used = mtile;
-            uint32_t pk[32];
+            uint32_t phi[16], plo[16];
             float sum = 0.f;
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < 32; c += 2) {
                 const float a = (sv[c] == -INFINITY) ? 0.f : tc::ex2(sv[c] - m_used);
                 const float bb = (sv[c + 1] == -INFINITY) ? 0.f : tc::ex2(sv[c + 1] - m_used);
                 sum += a + bb;
-                pk[c >> 1] = pack_f16(a, bb);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(a, bb);
+                phi[c >> 1] = *reinterpret_cast<const uint32_t*>(&hi);
+                plo[c >> 1] = pack_bf16(a - __low2float(hi), bb - __high2float(hi));
             }
             l_run += sum;
-            tc::tmem_st32(tmem + lane_base + (j & 1) * kBN, pk);
+            if (t.tree) {
+                // V rows of padding nodes may hold anything: zero them before the MMA reads
+                const int u = 2 * j + 1, st = u % kStages;
+                ok = __all_sync(kFull, tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag));
+                const int first = max(0, nn - t.y);
+                if (ok && first < kBN) {
+                    unsigned char* vst = sRing + st * Cfg::kStageBytes;
+                    const int per_blk = (kBN - first) * 8;
+                    for (int e = hf * 128 + r; e < per_blk * Cfg::kBlocks; e += 256) {
+                        const int blk = e / per_blk, rem = e % per_blk;
+                        *reinterpret_cast<uint4*>(vst + blk * (kBN * 128) + (first + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    tc::fence_proxy_async();
+                }
+                if (!ok) continue;
+            }
+            tc::tmem_st16(tmem + lane_base + (j & 1) * kBN + 16 * hf, phi);
+            tc::tmem_st16(tmem + lane_base + (j & 1) * kBN + kBN / 2 + 16 * hf, plo);
             tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(p_full + (j & 1));
         }
-        if (ok) {
-            ok = tc::mbar_wait(o_final, 0, abort_flag);
-            ok = __all_sync(kFull, ok);
-        }
+        if (ok) ok = tc::mbar_wait(o_final, 0, abort_flag);
+        ok = __all_sync(kFull, ok);
+        // row sum of both halves
+        xch[512 + hf * 128 + r] = l_run;
+        tc::named_bar(1, 256);
+        const float l_tot = l_run + xch[512 + (hf ^ 1) * 128 + r];
         if (ok) {
             tc::tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
 #pragma unroll 1
-            for (int cb = 0; cb < D; cb += 32) {
+            for (int cb = hf * (D / 2); cb < (hf + 1) * (D / 2); cb += 32) {
                 uint32_t ov[32];
                 tc::tmem_ld32(tmem + lane_base + Cfg::kOCol + cb, ov);
                 tc::tmem_wait_ld();
@@ -430,44 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_row32<float>(p.part_o + (prow0 + r) * D + cb, f);
                 }
             }
-            if (p.S > 1) p.part_ml[prow0 + r] = make_float2(m_used, l_run);
+            if (p.S > 1 && hf == 0) p.part_ml[prow0 + r] = make_float2(m_used, l_tot);
         }
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------------ V converters
-        const int ct = tid - 256;  // 0..127
-        constexpr int kVec = kBN * D / 8;  // 16-byte chunks per V tile
-        int overflow = 0;
-        for (int j = 0; j < T; ++j) {
-            const Tile t = tile_of(j, n_pre, c0, c1, ragged);
-            const int u = 2 * j + 1, st = u % kStages;
-            const bool ok = tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag);
-            if (!__all_sync(kFull, ok)) break;
-            unsigned char* vst = sRing + st * Cfg::kStageBytes;
-            // padding tree rows (node >= n_nodes) may hold anything: they become zeros
-            const int first = t.tree ? max(0, nn - t.y) : kBN;
-#pragma unroll 4
-            for (int e = ct; e < kVec; e += 128) {
-                const int row = (e % (kBN * 8)) / 8;  // row within its 64-row column block
-                uint4* ptr = reinterpret_cast<uint4*>(vst) + e;
-                uint4 v = *ptr;
-                if (row >= first) {
-                    v = make_uint4(0, 0, 0, 0);
-                } else {
-                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-                        overflow |= (fabsf(lo) >= 65520.f) | (fabsf(hi) >= 65520.f);
-                        w[i] = pack_f16(lo, hi);
-                    }
-                    v = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                *ptr = v;
-            }
-            tc::fence_proxy_async();
-            tc::mbar_arrive(v_ready + st);
-        }
-        if (__any_sync(kFull, overflow) && lane == 0) atomicExch(p.status + b, (int)DDT_ERR_UNSUPPORTED);
     }
 
     tc::tc_fence_before();
