@@ -299,21 +299,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, D, false, true);
             const uint32_t sRa = tc::smem_u32(sRing);
+            // Descriptors are built once; a k-step or a ring stage only moves the start
+            // address, i.e. adds (byte offset >> 4) to the low 14-bit field, which cannot
+            // overflow for addresses inside this CTA's shared memory.  Keeping the per-MMA
+            // work to one add matters: the single issuing thread, not the tensor core, was
+            // the bound when every MMA rebuilt its 64-bit descriptor.
+            const uint64_t kdesc0 = tc::desc_sw128(sRa, 16, 1024);
+            const uint64_t vdesc0 = tc::desc_sw128(sRa, kBN * 128, 1024);
             auto pv = [&](int i) -> bool {
                 if (!tc::mbar_wait(p_full + (i & 1), (i >> 1) & 1, abort_flag)) return false;
                 const int u = 2 * i + 1, st = u % kStages;
                 if (!tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag)) return false;
                 tc::tc_fence_after();
+                const uint64_t vd = vdesc0 + static_cast<uint64_t>((st * Cfg::kStageBytes) >> 4);
+                const uint32_t pa = tmem + (i & 1) * kBN;
+                // first MMA of the chunk may start the accumulator, the rest accumulate
+                tc::mma_f16_ts(tmem + Cfg::kOCol, pa, vd, idesc_pv, i > 0 ? 1u : 0u);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {  // P_hi, then P_lo
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        // V tile: 16 keys = two 8-row swizzle atoms down the K dimension
-                        const uint64_t bdesc =
-                            tc::desc_sw128(sRa + st * Cfg::kStageBytes + kk * 2048, kBN * 128, 1024);
-                        tc::mma_f16_ts(tmem + Cfg::kOCol, tmem + (i & 1) * kBN + part * (kBN / 2) + kk * 8, bdesc,
-                                       idesc_pv, (i > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                    }
+                for (int q = 1; q < 2 * (kBN / 16); ++q) {  // P_hi k-steps, then P_lo k-steps
+                    const int part = q / (kBN / 16), kk = q % (kBN / 16);
+                    // V tile: 16 keys = two 8-row swizzle atoms down the K dimension
+                    tc::mma_f16_ts_acc(tmem + Cfg::kOCol, pa + part * (kBN / 2) + kk * 8,
+                                       vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv);
                 }
                 tc::mma_commit(empty + st);
                 tc::mma_commit(o_done);
@@ -327,12 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc::tc_fence_after();
+                const uint64_t kd = kdesc0 + static_cast<uint64_t>((st * Cfg::kStageBytes) >> 4);
+                const uint32_t sd = tmem + (j & 1) * kBN, qa = tmem + Cfg::kQCol;
+                tc::mma_f16_ts(sd, qa, kd, idesc_qk, 0u);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 1; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-                    tc::mma_f16_ts(tmem + (j & 1) * kBN, tmem + Cfg::kQCol + kk * 8,
-                                   tc::desc_sw128(sRa + st * Cfg::kStageBytes + koff, 16, 1024), idesc_qk,
-                                   kk > 0 ? 1u : 0u);
+                    tc::mma_f16_ts_acc(sd, qa + kk * 8, kd + static_cast<uint64_t>(koff >> 4), idesc_qk);
                 }
                 tc::mma_commit(empty + st);
                 tc::mma_commit(s_full + (j & 1));
