@@ -57,12 +57,20 @@ struct GdnSmem {
 __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD) {
     GdnSmem L;
     size_t off = 0;
-    L.s0 = off;
-    off += (size_t)kDV * kDK * 4;            // S0 tile (64 KiB)
+    // [k | q] tile (tf32 high parts): NPAD rows in four 32-column chunks; the Gram MMA
+    // reads 128 rows of every chunk, so the last chunk's reads reach 128 rows past its start
+    const size_t kq_bytes = (size_t)(3 * NPAD + (NPAD > 128 ? NPAD : 128)) * 128;
     L.kq = off;
-    off += (size_t)NPAD * kDK * 4;           // [k | q] tile
+    off += kq_bytes;
+    // S0 tile (64 KiB) followed by R.  Until the Gram MMA has finished, the same bytes
+    // hold the low parts of the [k | q] tile (same layout as the high parts).
+    L.s0 = off;
+    off += (size_t)kDV * kDK * 4;
     L.u = off;
-    off += (size_t)N * kDV * 4;              // R -> u, one column per value channel
+    // R (one column per value channel), first used for the Gram rows [N][2N]
+    size_t ub = (size_t)N * (kDV > 2 * N ? kDV : 2 * N) * 4;
+    if (L.u + ub < L.s0 + kq_bytes) ub = L.s0 + kq_bytes - L.u;
+    off += ub;
     L.kk = off;
     off += (size_t)N * kMD * 4;
     L.qk = off;
@@ -84,7 +92,7 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD) {
     return L;
 }
 
-__device__ __forceinline__ float silu_g(float z) { return z / (1.f + __expf(-z)); }
+__device__ __forceinline__ float silu_g(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 // byte offset of element (row, col) of a K-major fp32 tile with 128-byte swizzle whose
 // column blocks of 32 elements are `rows * 128` bytes apart
@@ -114,6 +122,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     const GdnSmem lay = gdn_tc_layout(N, p.NPAD);
     unsigned char* sS0 = base + lay.s0;
     unsigned char* sKQ = base + lay.kq;
+    unsigned char* sLO = sS0;  // low parts of [k | q], until the Gram MMA is done
     float* ubuf = reinterpret_cast<float*>(base + lay.u);
     float* skk = reinterpret_cast<float*>(base + lay.kk);
     float* sqk = reinterpret_cast<float*>(base + lay.qk);
@@ -133,7 +142,8 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     uint64_t* d_full = bars + 2;  // [2] D ready
     uint64_t* d_free = bars + 4;  // [2] epilogue done with D (kEpi arrivals)
     uint64_t* drain = bars + 6;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+    uint64_t* g_done = bars + 7;  // Gram-matrix MMA done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     int* err = abort_flag + 1;
 
@@ -202,6 +212,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
         tc::mbar_init(d_free, kEpi);
         tc::mbar_init(d_free + 1, kEpi);
         tc::mbar_init(drain, 1);
+        tc::mbar_init(g_done, 1);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -210,12 +221,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     }
     __syncthreads();
     const int srow0 = (int)((lb * p.Hv + (long)g * p.R) * kDV);
-    if (tid == 0) {
-        tc::prefetch_tmap(&tm_s);
-        tc::mbar_expect_tx(full, kDV * kDK * 4);
-        for (int blk = 0; blk < kDK / 32; ++blk)
-            tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0);
-    }
+    if (tid == 0) tc::prefetch_tmap(&tm_s);
 
     // ---- conv + SiLU + L2 norm of q and k: half-warp per (node, q|k), 8 channels a lane
     {
@@ -254,45 +260,104 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             }
             const int row = half == 0 ? p.QOFF + n : n;
             const int col = sub * 8;
+            // y = hi + lo, hi rounded to tf32: the dense MMAs read hi, the Gram reads both
+            float lo[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const float hv = tc::tf32_rn(y[ch]);
+                lo[ch] = y[ch] - hv;
+                y[ch] = hv;
+            }
             *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(y[0], y[1], y[2], y[3]);
             *reinterpret_cast<float4*>(sKQ + sw_off(row, col + 4, p.NPAD)) = make_float4(y[4], y[5], y[6], y[7]);
+            *reinterpret_cast<float4*>(sLO + sw_off(row, col, p.NPAD)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<float4*>(sLO + sw_off(row, col + 4, p.NPAD)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
         }
         // padding rows of the tile
         for (int e = tid; e < p.NPAD * (kDK / 4); e += kThr) {
             const int row = e / (kDK / 4), col = (e % (kDK / 4)) * 4;
             const bool used = row < N || (row >= p.QOFF && row < p.QOFF + N);
-            if (!used) *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!used) {
+                *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(sLO + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     }
     tc::fence_proxy_async();
     __syncthreads();
 
-    // ---- dot products along ancestor chains (k_s . k_t, k_s . q_t; self q_t . k_t)
+    // ---- dot products along ancestor chains: the Gram matrix G[t][c] = k_t . kq_c for tile
+    //      rows t < 128 and every [k | q] column c holds all k_s . k_t and k_s . q_t.  It is
+    //      taken as three tf32 MMAs, hi.hi + lo.hi + hi.lo, which keeps it near fp32 accuracy
+    //      (one tf32 product loses too much in the chains of the delta rule).  The lanes of
+    //      rows t < n_nodes copy [k.k | k.q] to shared memory, then each node gathers the
+    //      entries of its own ancestor chain.
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t gcol = 0;           // D buffer 0, free until the first head's MMA
+    float* gram = ubuf;                // [N][2N]: k_t.k_s | k_t.q_s
+    if (tid == 32) {
+        const uint32_t idesc = tc::idesc_tf32(128, p.NPAD, false, false);
+        const uint64_t dh = tc::desc_sw128(tc::smem_u32(sKQ), 16, 1024);
+        const uint64_t dl = tc::desc_sw128(tc::smem_u32(sLO), 16, 1024);
+#pragma unroll
+        for (int pass = 0; pass < 3; ++pass) {
+            const uint64_t da = pass == 1 ? dl : dh, db = pass == 2 ? dl : dh;
+#pragma unroll
+            for (int kk = 0; kk < kDK / 8; ++kk) {
+                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (p.NPAD * 128) + (kk & 3) * 32) >> 4);
+                tc::mma_tf32_ss(tmem + gcol, da + off, db + off, idesc, (pass | kk) ? 1u : 0u);
+            }
+        }
+        tc::mma_commit(g_done);
+    }
+    if (tid == 0) {
+        // the low parts are dead once the Gram MMAs are done: load the first S0 over them
+        if (tc::mbar_wait(g_done, 0, abort_flag)) {
+            tc::mbar_expect_tx(full, kDV * kDK * 4);
+            for (int blk = 0; blk < kDK / 32; ++blk)
+                tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0);
+        }
+    }
+    if (warp >= 4 && warp < 8) {
+        const int t = tid - 128;
+        const bool gok = __all_sync(kFull, tc::mbar_wait(g_done, 0, abort_flag));
+        if (gok) {
+            tc::tc_fence_after();
+            const uint32_t rowaddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + gcol;
+            for (int c0 = 0; c0 < p.QOFF + N; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(rowaddr + c0, v);
+                tc::tmem_wait_ld();
+                if (t < nn) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int c = c0 + i;
+                        if (c < N) gram[t * 2 * N + c] = __uint_as_float(v[i]);
+                        else if (c >= p.QOFF && c < p.QOFF + N) gram[t * 2 * N + N + (c - p.QOFF)] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
     for (int e = tid; e < nn * (kMD + 1); e += kThr) {
         const int t = e / (kMD + 1), m = e % (kMD + 1);
         const int dep = sdep[t];
         if (m > dep) continue;
-        const int s = (m == dep) ? t : alist[t * kMD + m];
-        float dkk = 0.f, dqk = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < kDK; c += 4) {
-            const float4 ks = *reinterpret_cast<const float4*>(sKQ + sw_off(s, c, p.NPAD));
-            const float4 kt = *reinterpret_cast<const float4*>(sKQ + sw_off(t, c, p.NPAD));
-            const float4 qt = *reinterpret_cast<const float4*>(sKQ + sw_off(p.QOFF + t, c, p.NPAD));
-            dkk = fmaf(ks.x, kt.x, fmaf(ks.y, kt.y, fmaf(ks.z, kt.z, fmaf(ks.w, kt.w, dkk))));
-            dqk = fmaf(ks.x, qt.x, fmaf(ks.y, qt.y, fmaf(ks.z, qt.z, fmaf(ks.w, qt.w, dqk))));
-        }
         if (m == dep) {
-            sqself[t] = dqk;
+            sqself[t] = gram[t * 2 * N + N + t];  // k_t . q_t
         } else {
-            skk[t * kMD + m] = dkk;
-            sqk[t * kMD + m] = dqk;
+            const int s = alist[t * kMD + m];
+            skk[t * kMD + m] = gram[t * 2 * N + s];      // k_t . k_s
+            sqk[t * kMD + m] = gram[s * 2 * N + N + t];  // k_s . q_t
         }
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ S0 loads

@@ -214,5 +214,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// fp32 -> tf32 rounded to nearest (ties away from zero), kept in an fp32 register; a
+// kind::tf32 MMA would otherwise drop the low 13 mantissa bits of its operands.
+__device__ __forceinline__ float tf32_rn(float x) {
+    uint32_t y;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+    return __uint_as_float(y);
+}
+
 }  // namespace tc
 }  // namespace ddt
