@@ -164,6 +164,33 @@ def round_bytes(r):
     return float(total)
 
 
+# DRAM bytes (read + write) of one k_attn_tc launch, from an ncu capture of the bench's
+# own timed launch (dram__bytes_read.sum + dram__bytes_write.sum, one pass, full size),
+# keyed by the SHA-256 of the kernel's sources: once they change, the figure is stale
+# and the bench reports null until it is captured again.
+ATTN_TRAFFIC = {
+    # ncu: dram__bytes_read.sum 40.35 GB + dram__bytes_write.sum 402.61 MB, batched round
+    "51b97e022bc50a663363ccd404af2087c653ab1306d0c826604471f038c7a718": {"workload": 5, "bytes": 40.75261e9},
+}
+ATTN_SOURCES = ("attn_tc.cu", "tc.cuh")
+
+
+def attn_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "tree_speculative_decoding_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def attn_traffic(workload):
+    rec = ATTN_TRAFFIC.get(attn_source_hash())
+    if rec is None or rec["workload"] != workload:
+        return None
+    return rec["bytes"]
+
+
 def workload_desc(c):
     parts = [c["name"] + ":", f"B={c['B']}, D={c['D']}, V={c['V']}, budget {c['budget']}, top-k {c['top_k']}"]
     if "P_lo" in c:
@@ -247,10 +274,12 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = ddt.ddt_launch_count()
     t0.record(st)
     for _ in range(args.steps):
         step(True)
     t1.record(st)
+    launches = ddt.ddt_launch_count() - launches0
     torch.cuda.synchronize()
     barrier(world)
     ms = t0.elapsed_time(t1)
@@ -318,10 +347,10 @@ def run_ours(args, rank, world, local):
         "hbm_frac_round": rb / (step_ms / 1e3) / 1e9 / hbm_peak,
         "per_kernel_ms": per_kernel,
         "roofline": {"bound": "tensor", "kernel": "ddt_tree_attn", "achieved": tflops, "peak": tc_peak,
-                     "unit": "TFLOP/s", "frac": tflops / tc_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": tflops / tc_peak, "traffic": attn_traffic(args.workload),
                      "algorithmic_flops": fl, "algorithmic_bytes": by, "peak_note": "of measured (sustained)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 10 * args.steps,
+        "gpu_launches": launches,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg:

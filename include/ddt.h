@@ -72,6 +72,12 @@ const char* ddt_status_string(ddt_status s);
 /* Library version, e.g. "ddt 0.1 sm_103a". */
 const char* ddt_version(void);
 
+/* Number of kernel launches the library has issued in this process so far, over all
+ * threads, streams and devices (launches that CUDA rejected included).  A caller takes
+ * the difference around a region to count the kernels that region launched.  No
+ * counterpart in the pages: bookkeeping for measurement. */
+uint64_t ddt_launch_count(void);
+
 /* ---------------------------------------------------------------------------------
  * ddt_build_tree -- [ARCH] best-first tree construction and flattening; [CHALL] 2.
  *

@@ -38,6 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_library_is_in_tree_and_versioned(lib):
     assert os.path.dirname(build_ext.LIB).startswith(ROOT)
     assert lib.ddt_version().decode().endswith("sm_103a")
+    assert lib.ddt_launch_count() >= 0
     for code, text in [(0, "ok"), (3, "cache capacity exceeded"), (6, "non-finite logits"), (7, "malformed tree")]:
         assert lib.ddt_status_string(code).decode() == text
 
@@ -53,6 +54,7 @@ def test_host_checks_fail_fast(lib):
     """Bad sizes / null pointers are refused on the host before any launch."""
     p = ctypes.c_void_p(16)
     nul = None
+    launched = lib.ddt_launch_count()
     # build: B = 0, top_k > 32, null workspace
     assert lib.ddt_build_tree(0, 1, 10, 1, 1, 1, *([p] * 11), p, 1 << 20, nul) == 1
     assert lib.ddt_build_tree(1, 1, 100, 33, 1, 1, *([p] * 11), p, 1 << 20, nul) == 2
@@ -66,6 +68,7 @@ def test_host_checks_fail_fast(lib):
     # walk / commit: bad sizes
     assert lib.ddt_walk_accept(0, 5, 10, 4, 1, *([p] * 11), p, 256, nul) == 1
     assert lib.ddt_commit(1, 5, 0, 0, 1, 64, 10, 1, p, p, p, p, 0, 1, 1, 32, 32, 4, 1, *([p] * 12), nul) == 1
+    assert lib.ddt_launch_count() == launched   # refused before any launch
 
 
 def test_workspace_queries(lib):

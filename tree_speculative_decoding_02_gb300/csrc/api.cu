@@ -3,10 +3,17 @@
 // synchronisation happens; data errors found on the device go to the status words.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "ddt.h"
 #include "kernels.h"
 
 using namespace ddt;
+
+namespace ddt {
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace ddt
 
 namespace {
 
@@ -37,6 +44,8 @@ const char* ddt_status_string(ddt_status s) {
 }
 
 const char* ddt_version(void) { return "ddt 0.1 sm_103a"; }
+
+uint64_t ddt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // ------------------------------------------------------------------------- build
 size_t ddt_build_tree_workspace(int B, int D, int V, int top_k) {

@@ -174,7 +174,7 @@ static cudaError_t attn_simt_go(int L, int B, int N, int Hq, int Hkv, int Pcap, 
     if (e != cudaSuccess) return e;
     const int G = Hq / Hkv;
     dim3 grid((N * G + kRows - 1) / kRows, Hkv, L * B);
-    k_attn_simt<Tin, Tout, D><<<grid, 256, smem, st>>>(
+    k_attn_simt<Tin, Tout, D><<<counted(grid), 256, smem, st>>>(
         B, N, Hq, Hkv, Pcap, static_cast<const Tin*>(q), static_cast<const Tin*>(kt), static_cast<const Tin*>(vt),
         static_cast<const Tin*>(kc), static_cast<const Tin*>(vc), pl, nn, anc, scale, static_cast<Tout*>(o), status);
     return cudaGetLastError();

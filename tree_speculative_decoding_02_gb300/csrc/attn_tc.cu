@@ -604,10 +604,10 @@ static cudaError_t attn_tc_go(const TcParams& prm, const CUtensorMap* maps, cuda
     cudaError_t e = cudaFuncSetAttribute(k_attn_tc<D, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(prm.S * prm.MT * prm.Hkv * prm.L, prm.B);
-    k_attn_tc<D, Tout><<<grid, kThreads, Cfg::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3]);
+    k_attn_tc<D, Tout><<<counted(grid), kThreads, Cfg::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3]);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (prm.S > 1) {
-        k_attn_merge<D, Tout><<<dim3(prm.N * prm.Hq, prm.L * prm.B), D, 0, st>>>(prm);
+        k_attn_merge<D, Tout><<<counted(dim3(prm.N * prm.Hq, prm.L * prm.B)), D, 0, st>>>(prm);
         e = cudaGetLastError();
     }
     return e;
@@ -677,7 +677,7 @@ cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-    k_attn_order<<<1, 256, 0, st>>>(B, prefix_len, perm, status);
+    k_attn_order<<<counted(1), 256, 0, st>>>(B, prefix_len, perm, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const bool bf = out == DDT_BF16;

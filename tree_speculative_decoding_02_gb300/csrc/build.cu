@@ -427,10 +427,10 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
     dim3 g1(nch, D, B);
     const int vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
     if (dtype == DDT_BF16)
-        k_build_partial<__nv_bfloat16><<<g1, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), D, V, k, nch,
+        k_build_partial<__nv_bfloat16><<<counted(g1), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), D, V, k, nch,
                                                           vec, part, pv, pid);
     else
-        k_build_partial<float><<<g1, 256, 0, st>>>(static_cast<const float*>(logits), D, V, k, nch, vec, part, pv,
+        k_build_partial<float><<<counted(g1), 256, 0, st>>>(static_cast<const float*>(logits), D, V, k, nch, vec, part, pv,
                                                   pid);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -439,7 +439,7 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
         e = cudaFuncSetAttribute(k_build_tree<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return e;
     }
-    k_build_tree<512><<<B, 512, sm, st>>>(D, V, k, budget, nch, part, pv, pid, root_token, prefix_len, token,
+    k_build_tree<512><<<counted(B), 512, sm, st>>>(D, V, k, budget, nch, part, pv, pid, root_token, prefix_len, token,
                                           parent, depth, position, n_nodes, anc, score, status);
     return cudaGetLastError();
 }

@@ -198,7 +198,7 @@ static cudaError_t commit_gdn_go(int B, int N, int A, int Lg, int Hk, int Hv, in
     cudaError_t e = cudaFuncSetAttribute(k_commit_gdn<Tx, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    k_commit_gdn<Tx, DK, DV><<<dim3(Hv, B, Lg), 256, smem, st>>>(
+    k_commit_gdn<Tx, DK, DV><<<counted(dim3(Hv, B, Lg)), 256, smem, st>>>(
         B, N, A, Hk, Hv, K, cap, Pcap, static_cast<const Tx*>(x), static_cast<const Tx*>(w),
         static_cast<const Tx*>(cs), beta, decay, S, an, al, pl);
     return cudaGetLastError();
@@ -237,12 +237,12 @@ cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap,
                         (reinterpret_cast<uintptr_t>(v_cache) % 16 == 0);
         dim3 grid(A, La * Hkv, B);
         if (kv_dtype == DDT_BF16)
-            k_commit_kv<__nv_bfloat16><<<grid, 64, 0, st>>>(
+            k_commit_kv<__nv_bfloat16><<<counted(grid), 64, 0, st>>>(
                 B, N, A, Hkv, d, Pcap, vec, static_cast<const __nv_bfloat16*>(k_tree),
                 static_cast<const __nv_bfloat16*>(v_tree), static_cast<__nv_bfloat16*>(k_cache),
                 static_cast<__nv_bfloat16*>(v_cache), acc_nodes, acc_len, prefix_len);
         else
-            k_commit_kv<float><<<grid, 64, 0, st>>>(B, N, A, Hkv, d, Pcap, vec, static_cast<const float*>(k_tree),
+            k_commit_kv<float><<<counted(grid), 64, 0, st>>>(B, N, A, Hkv, d, Pcap, vec, static_cast<const float*>(k_tree),
                                                     static_cast<const float*>(v_tree), static_cast<float*>(k_cache),
                                                     static_cast<float*>(v_cache), acc_nodes, acc_len, prefix_len);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -254,7 +254,7 @@ cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap,
                                                decay, S, acc_nodes, acc_len, prefix_len, st);
             if (e != cudaSuccess) return e;
             if (K > 1)
-                k_commit_conv<__nv_bfloat16><<<dim3(Lg, B), 256, 0, st>>>(
+                k_commit_conv<__nv_bfloat16><<<counted(dim3(Lg, B)), 256, 0, st>>>(
                     B, N, A, C, K, cap, Pcap, static_cast<const __nv_bfloat16*>(x),
                     static_cast<__nv_bfloat16*>(conv_state), acc_nodes, acc_len, prefix_len);
         } else {
@@ -262,13 +262,13 @@ cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap,
                                        S, acc_nodes, acc_len, prefix_len, st);
             if (e != cudaSuccess) return e;
             if (K > 1)
-                k_commit_conv<float><<<dim3(Lg, B), 256, 0, st>>>(B, N, A, C, K, cap, Pcap, static_cast<const float*>(x),
+                k_commit_conv<float><<<counted(dim3(Lg, B)), 256, 0, st>>>(B, N, A, C, K, cap, Pcap, static_cast<const float*>(x),
                                                                   static_cast<float*>(conv_state), acc_nodes, acc_len,
                                                                   prefix_len);
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    k_commit_final<<<(B + 127) / 128, 128, 0, st>>>(B, N, A, cap, Pcap, acc_nodes, acc_len, prefix_len, src_row,
+    k_commit_final<<<counted((B + 127) / 128), 128, 0, st>>>(B, N, A, cap, Pcap, acc_nodes, acc_len, prefix_len, src_row,
                                                     dst_pos, status);
     return cudaGetLastError();
 }

@@ -246,7 +246,7 @@ static cudaError_t gdn_go(int L, int B, int N, int Hk, int Hv, int K, const void
         cudaFuncSetAttribute(k_gdn_tree<Tin, Tout, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(Hv, B, L);
-    k_gdn_tree<Tin, Tout, DK, DV><<<grid, 256, smem, st>>>(
+    k_gdn_tree<Tin, Tout, DK, DV><<<counted(grid), 256, smem, st>>>(
         B, N, Hk, Hv, K, static_cast<const Tin*>(x), static_cast<const Tin*>(w), static_cast<const Tin*>(cs), beta,
         decay, S, parent, nn, static_cast<Tout*>(o), status);
     return cudaGetLastError();

@@ -558,7 +558,7 @@ static cudaError_t gdn_tc_go(const GdnTcParams& prm, const CUtensorMap& map, cud
     const size_t smem = gdn_tc_layout(prm.N, prm.NPAD).total;
     cudaError_t e = cudaFuncSetAttribute(k_gdn_tc<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_gdn_tc<Tin, Tout><<<dim3(prm.Hk, prm.B, prm.L), kThr, smem, st>>>(prm, map);
+    k_gdn_tc<Tin, Tout><<<counted(dim3(prm.Hk, prm.B, prm.L)), kThr, smem, st>>>(prm, map);
     return cudaGetLastError();
 }
 

@@ -17,6 +17,15 @@ constexpr int kMaxRows = 1024;     // N = budget + 1
 constexpr int kGdnMaxNodes = 128;
 constexpr int kGdnMaxDepth = 32;
 
+// Launch counter: every launch site passes its grid through counted(), so that
+// ddt_launch_count() can report how many kernels this library has put on streams.
+void note_launch();
+template <typename G>
+inline G counted(G grid) {
+    note_launch();
+    return grid;
+}
+
 size_t build_ws_bytes(int B, int D, int V, int k);
 size_t build_tree_smem(int D, int k, int budget);
 cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype dtype, const void* logits,

@@ -220,14 +220,14 @@ cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void*
         dim3 g(nch, N, B);
         const int vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
         if (dtype == DDT_BF16)
-            k_walk_argmax<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), N, V, nch,
+            k_walk_argmax<__nv_bfloat16><<<counted(g), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), N, V, nch,
                                                             vec, n_nodes, part);
         else
-            k_walk_argmax<float><<<g, 256, 0, st>>>(static_cast<const float*>(logits), N, V, nch, vec, n_nodes, part);
+            k_walk_argmax<float><<<counted(g), 256, 0, st>>>(static_cast<const float*>(logits), N, V, nch, vec, n_nodes, part);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    k_walk_descend<<<B, 256, 0, st>>>(N, V, A, nch, logits != nullptr, part, targ, token, parent, n_nodes, acc_nodes,
+    k_walk_descend<<<counted(B), 256, 0, st>>>(N, V, A, nch, logits != nullptr, part, targ, token, parent, n_nodes, acc_nodes,
                                       acc_len, bonus, emitted, n_emitted, status);
     return cudaGetLastError();
 }

@@ -32,6 +32,7 @@ _c_int, _c_size, _c_p, _c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 _SIGS = {
     "ddt_status_string": ([_c_int], ctypes.c_char_p),
     "ddt_version": ([], ctypes.c_char_p),
+    "ddt_launch_count": ([], ctypes.c_uint64),
     "ddt_build_tree_workspace": ([_c_int] * 4, _c_size),
     "ddt_build_tree": ([_c_int] * 6 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_build_tree_noalloc": ([_c_int] * 6 + [_c_p] * 11 + [_c_p], _c_int),
@@ -72,6 +73,11 @@ def load(build_if_missing: bool = True):
             fn.restype = res
         _lib = lib
         return lib
+
+
+def ddt_launch_count() -> int:
+    """Kernel launches the library has issued in this process so far."""
+    return int(load().ddt_launch_count())
 
 
 def _gpu():
