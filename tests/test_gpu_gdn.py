@@ -89,10 +89,12 @@ def test_gdn_tree_workload_sampled():
 
 
 @pytest.mark.parametrize("Hk,Hv,dtype,budget", [(2, 2, torch.bfloat16, 16), (1, 4, torch.float32, 64),
-                                                 (3, 6, torch.bfloat16, 0)])
+                                                 (2, 4, torch.float32, 32), (3, 6, torch.bfloat16, 0),
+                                                 (1, 3, torch.bfloat16, 66)])
 def test_gdn_head128_variants(Hk, Hv, dtype, budget):
-    """Head size 128 (tensor-core path): one or several value heads per key head, fp32 or
-    bf16 inputs, root-only trees."""
+    """Head size 128: one or several value heads per key head, fp32 or bf16 inputs, root-only
+    trees, and the largest tree the tensor-core path stages for bf16 (67 rows); larger
+    fp32 trees take the CUDA-core path."""
     tree, _ = C.tree_from_logits(4, 2, 15, 3000, 8, budget)
     gi = synth.gdn_inputs(2, 2, budget + 1, Hk, Hv, 128, 128, 4, workload=4, dtype=dtype)
     r = _gpu(tree, gi, Hk)
@@ -115,3 +117,13 @@ def test_gdn_head128_deep_chain():
             assert int(r["status"][0]) == 0
         else:
             assert int(r["status"][0]) == 2   # deeper than this path supports: refused per request
+
+
+@pytest.mark.parametrize("K", [1, 2, 6])
+def test_gdn_head128_conv_widths(K):
+    """Conv widths other than 4 (the generic tensor-core instance), including no conv state."""
+    tree, _ = C.tree_from_logits(4, 2, 15, 3000, 8, 24)
+    gi = synth.gdn_inputs(1, 2, 25, 2, 4, 128, 128, K, workload=4, dtype=torch.bfloat16)
+    r = _gpu(tree, gi, 2)
+    _check(r["o"], _oracle(tree, gi, 2), tree)
+    assert (r["status"].cpu() == 0).all()

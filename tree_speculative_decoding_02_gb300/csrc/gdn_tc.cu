@@ -51,10 +51,11 @@ struct GdnTcParams {
 };
 
 struct GdnSmem {
-    size_t s0, kq, u, kk, qk, ca, cb, tt, alist, small, bars, total;
+    size_t s0, kq, u, kk, qk, ca, cb, tt, tr, alist, small, sv, bars, total;
 };
 
-__host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD) {
+// esz = bytes per input element (the staged v rows keep the input type)
+__host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     GdnSmem L;
     size_t off = 0;
     // [k | q] tile (tf32 high parts): NPAD rows in four 32-column chunks; the Gram MMA
@@ -81,10 +82,15 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD) {
     off += (size_t)N * kMD * 4;
     L.tt = off;
     off += (size_t)N * kMaxK * 8;            // conv input row pointers
+    L.tr = off;
+    off += (size_t)N * kMaxK * 4;            // conv input rows as staging-row indices
     L.alist = off;
     off += (size_t)N * kMD * 4;
     L.small = off;
     off += (size_t)N * 4 * 7;                // dep, par, qself, gcum, beta, decay, spare
+    off = (off + 15) & ~(size_t)15;
+    L.sv = off;                              // one value head's v channels: node rows, then conv-state rows
+    off += (size_t)(N + K - 1) * kDV * esz;
     off = (off + 7) & ~(size_t)7;
     L.bars = off;
     off += 128;
@@ -111,15 +117,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
+
+// 16-byte global -> shared copy that completes asynchronously (both addresses 16-byte aligned)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 }  // namespace
 
-template <typename Tin, typename Tout>
+// KT: compile-time conv width (K == KT), or kMaxK for any K <= kMaxK given at run time
+template <typename Tin, typename Tout, int KT>
 __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const __grid_constant__ CUtensorMap tm_s) {
     extern __shared__ unsigned char smem_raw[];
     // align to 1024 B by pointer arithmetic on the shared array (keeps the address space)
     unsigned char* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int N = p.N;
-    const GdnSmem lay = gdn_tc_layout(N, p.NPAD);
+    const GdnSmem lay = gdn_tc_layout(N, p.NPAD, p.K, (int)sizeof(Tin));
     unsigned char* sS0 = base + lay.s0;
     unsigned char* sKQ = base + lay.kq;
     unsigned char* sLO = sS0;  // low parts of [k | q], until the Gram MMA is done
@@ -129,6 +145,8 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     float* sca = reinterpret_cast<float*>(base + lay.ca);
     float* scb = reinterpret_cast<float*>(base + lay.cb);
     const Tin** taps = reinterpret_cast<const Tin**>(base + lay.tt);  // [N][K] conv input rows
+    int* trow = reinterpret_cast<int*>(base + lay.tr);                // [N][K] the same rows in sv
+    Tin* sv = reinterpret_cast<Tin*>(base + lay.sv);                  // [N + K - 1][kDV]
     int* alist = reinterpret_cast<int*>(base + lay.alist);
     int* sdep = reinterpret_cast<int*>(base + lay.small);
     int* spar = sdep + N;
@@ -150,12 +168,29 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     const int g = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long lb = (long)l * p.B + b;
-    const int C = p.C, K = p.K;
+    const int C = p.C, K = KT < kMaxK ? KT : p.K;
     const int nn = p.n_nodes[b];
     const Tin* xb = static_cast<const Tin*>(p.x) + lb * N * C;
     const Tin* csb = static_cast<const Tin*>(p.conv_state) + lb * (K - 1) * C;
     const Tin* wl = static_cast<const Tin*>(p.conv_w) + (long)l * C * K;
 
+    // warm L2 with every x row the CTA will read (q and k channels of its key head and v
+    // channels of its value heads, for each node and each conv-state row), so the conv
+    // loads below wait on L2 rather than DRAM
+    {
+        const int nr = min(max(nn, 0), N);
+        const int lq = (kDK * (int)sizeof(Tin) + 127) / 128, lv = (p.R * kDV * (int)sizeof(Tin) + 127) / 128;
+        const int per = 2 * lq + lv, step = 128 / (int)sizeof(Tin);
+        for (int e = tid; e < (nr + K - 1) * per; e += kThr) {
+            const int r = e / per, sgm = e % per;
+            const Tin* row = r < nr ? xb + (long)r * C : csb + (long)(r - nr) * C;
+            long off;
+            if (sgm < lq) off = (long)g * kDK + sgm * step;
+            else if (sgm < 2 * lq) off = (long)(p.Hk + g) * kDK + (sgm - lq) * step;
+            else off = 2L * p.Hk * kDK + (long)g * p.R * kDV + (sgm - 2 * lq) * step;
+            prefetch_l2(row + off);
+        }
+    }
     if (tid == 0) {
         *err = (nn < 1 || nn > N) ? DDT_ERR_TREE : DDT_OK;
         *abort_flag = 0;
@@ -183,11 +218,9 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             sdep[n] = d;
             for (int q = 0; q < K; ++q) {
                 const int back = K - 1 - q;
-                const Tin* row;
-                if (back == 0) row = xb + (long)n * C;
-                else if (back <= d) row = xb + (long)alist[n * kMD + back - 1] * C;
-                else row = csb + (long)(K - 1 - (back - d)) * C;
-                taps[n * K + q] = row;
+                const int r = back == 0 ? n : (back <= d ? alist[n * kMD + back - 1] : N + (K - 1 - (back - d)));
+                taps[n * K + q] = r < N ? xb + (long)r * C : csb + (long)(r - N) * C;
+                trow[n * K + q] = r;
             }
         }
     }
@@ -227,29 +260,42 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     {
         const int half = lane >> 4, sub = lane & 15;
         const int c0 = (half == 0 ? g * kDK : p.Hk * kDK + g * kDK) + sub * 8;
-        float w[8][kMaxK];
+        float w[8][KT];
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
 #pragma unroll
-            for (int q = 0; q < kMaxK; ++q) w[ch][q] = (q < K) ? to_f32(wl[(long)(c0 + ch) * K + q]) : 0.f;
-        for (int n = warp; n < N; n += kThr / 32) {
+            for (int q = 0; q < KT; ++q) w[ch][q] = (q < K) ? to_f32(wl[(long)(c0 + ch) * K + q]) : 0.f;
+        // two nodes per pass, so their loads are in flight together
+        constexpr int kW = kThr / 32;
+        for (int n0 = warp; n0 < N; n0 += 2 * kW) {
+            float yy[2][8];
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const int nc = min(n0 + s2 * kW, nn - 1);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) yy[s2][ch] = 0.f;
+#pragma unroll
+                for (int q = 0; q < KT; ++q) {
+                    if (q < K) {
+                        float in[8];
+                        load8(taps[nc * K + q] + c0, in);
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) yy[s2][ch] = fmaf(w[ch][q], in[ch], yy[s2][ch]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+            const int n = n0 + s2 * kW;
+            if (n >= N) break;
             float y[8];
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) y[ch] = 0.f;
             if (n < nn) {
-#pragma unroll
-                for (int q = 0; q < kMaxK; ++q) {
-                    if (q < K) {
-                        float in[8];
-                        load8(taps[n * K + q] + c0, in);
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) y[ch] = fmaf(w[ch][q], in[ch], y[ch]);
-                    }
-                }
                 float ss = 0.f;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    y[ch] = silu_g(y[ch]);
+                    y[ch] = silu_g(yy[s2][ch]);
                     ss = fmaf(y[ch], y[ch], ss);
                 }
 #pragma unroll
@@ -272,6 +318,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             *reinterpret_cast<float4*>(sKQ + sw_off(row, col + 4, p.NPAD)) = make_float4(y[4], y[5], y[6], y[7]);
             *reinterpret_cast<float4*>(sLO + sw_off(row, col, p.NPAD)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             *reinterpret_cast<float4*>(sLO + sw_off(row, col + 4, p.NPAD)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
+            }
         }
         // padding rows of the tile
         for (int e = tid; e < p.NPAD * (kDK / 4); e += kThr) {
@@ -405,6 +452,19 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             const int h = g * p.R + hi, db = hi & 1;
             // gates of this head; per-node decay products and chain coefficients
             //   A(t, s_m) = b_t G(t, s_m) (k_s.k_t),  B(t, s_m) = G(t, s_m) (k_s.q_t)
+            // stage this head's v channels of the node rows and conv-state rows (16-byte
+            // cp.async); the copies land while the gates and chain coefficients are computed
+            {
+                constexpr int kVec = kDV * (int)sizeof(Tin) / 16;
+                const long cv0 = 2L * p.Hk * kDK + (long)h * kDV;
+                for (int i = e; i < (nn + K - 1) * kVec; i += kEpi) {
+                    const int r = i / kVec, c = i % kVec;
+                    const Tin* src = (r < nn ? xb + (long)r * C : csb + (long)(r - nn) * C) + cv0 + c * (16 / (int)sizeof(Tin));
+                    const int rs = r < nn ? r : N + (r - nn);
+                    cp_async16(reinterpret_cast<unsigned char*>(sv + (long)rs * kDV) + c * 16, src);
+                }
+                cp_async_commit();
+            }
             if (e < nn) {
                 sdec[e] = p.decay[(lb * N + e) * p.Hv + h];
                 sbeta[e] = p.beta[(lb * N + e) * p.Hv + h];
@@ -448,6 +508,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                     scb[e * kMD + k - 1] = mrow[k];  // own row only: B(t, .) is not read by others
                 }
             }
+            cp_async_wait_all();
             named_bar(1, kEpi);
             // after a timeout the warp keeps meeting the named barriers but does no work
             if (!dead) dead = !__all_sync(kFull, tc::mbar_wait(d_full + db, (hi >> 1) & 1, abort_flag));
@@ -460,18 +521,18 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             const uint32_t dcol = tmem + lane_base + db * p.NPAD;
             // pass A: R_t = b_t (v_t - g_t (S0 k_t)); v_t by the conv along the node's path
             const int cv = 2 * p.Hk * kDK + h * kDV + j;
-            float wv[kMaxK];
+            float wv[KT];
 #pragma unroll
-            for (int q = 0; q < kMaxK; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
+            for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
             for (int t0 = 0; t0 < nn; t0 += 16) {
                 uint32_t ks[16];
                 tmem_ld16(dcol + t0, ks);
-                float vin[8][kMaxK];
+                float vin[8][KT];
 #pragma unroll
                 for (int uu = 0; uu < 8; ++uu) {
                     const int t = min(t0 + 2 * uu + quad, nn - 1);
 #pragma unroll
-                    for (int q = 0; q < kMaxK; ++q) vin[uu][q] = (q < K) ? to_f32(taps[t * K + q][cv]) : 0.f;
+                    for (int q = 0; q < KT; ++q) vin[uu][q] = (q < K) ? to_f32(sv[trow[t * K + q] * kDV + j]) : 0.f;
                 }
                 tc::tmem_wait_ld();
 #pragma unroll
@@ -479,31 +540,45 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                     const int t = t0 + 2 * uu + quad;
                     float acc = 0.f;
 #pragma unroll
-                    for (int q = 0; q < kMaxK; ++q) acc = fmaf(wv[q], vin[uu][q], acc);
+                    for (int q = 0; q < KT; ++q) acc = fmaf(wv[q], vin[uu][q], acc);
                     if (t < nn)
                         ubuf[t * kDV + j] = sbeta[t] * (silu_g(acc) - sg[t] * __uint_as_float(ks[2 * uu + quad]));
                 }
             }
             named_bar(1, kEpi);
-            // pass C: outputs as independent sums over each node's own path
+            // pass C: outputs as independent sums over each node's own path; the 8 nodes of
+            // a chunk advance one ancestor level at a time, so their loads overlap
             for (int t0 = 0; t0 < N; t0 += 16) {
                 uint32_t qs[16];
                 if (t0 < nn) {
                     tmem_ld16(dcol + p.QOFF + t0, qs);
                     tc::tmem_wait_ld();
                 }
+                float ot[8];
+                int dp[8];
+                int md = 0;
 #pragma unroll
                 for (int uu = 0; uu < 8; ++uu) {
                     const int t = t0 + 2 * uu + quad;
-                    if (t >= N) break;
-                    float ot = 0.f;
+                    dp[uu] = 0;
+                    ot[uu] = 0.f;
                     if (t < nn) {
-                        const int dep = sdep[t];
-                        ot = fmaf(sg[t], __uint_as_float(qs[2 * uu + quad]), sqself[t] * ubuf[t * kDV + j]);
-                        for (int a = 0; a < dep; ++a)
-                            ot = fmaf(scb[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot);
+                        dp[uu] = sdep[t];
+                        ot[uu] = fmaf(sg[t], __uint_as_float(qs[2 * uu + quad]), sqself[t] * ubuf[t * kDV + j]);
                     }
-                    obase[((long)t * p.Hv + h) * kDV + j] = from_f32<Tout>(ot);
+                    md = max(md, dp[uu]);
+                }
+                for (int a = 0; a < md; ++a) {
+#pragma unroll
+                    for (int uu = 0; uu < 8; ++uu) {
+                        const int t = t0 + 2 * uu + quad;
+                        if (a < dp[uu]) ot[uu] = fmaf(scb[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot[uu]);
+                    }
+                }
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    const int t = t0 + 2 * uu + quad;
+                    if (t < N) obase[((long)t * p.Hv + h) * kDV + j] = from_f32<Tout>(ot[uu]);
                 }
             }
             tc::tc_fence_before();
@@ -547,19 +622,25 @@ int npad_of(int N) { return (qoff_of(N) + N + 15) / 16 * 16; }
 
 }  // namespace
 
-bool gdn_tc_supported(int N, int Hk, int Hv, int dk, int dv, int K) {
+bool gdn_tc_supported(int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in) {
     if (dk != kDK || dv != kDV || K < 1 || K > kMaxK || Hv % Hk != 0 || N > kEpi) return false;
     if (npad_of(N) > 256) return false;
-    return gdn_tc_layout(N, npad_of(N)).total <= 227 * 1024;
+    return gdn_tc_layout(N, npad_of(N), K, in == DDT_BF16 ? 2 : 4).total <= 227 * 1024;
 }
 
+template <typename Tin, typename Tout, int KT>
+static cudaError_t gdn_tc_go_k(const GdnTcParams& prm, const CUtensorMap& map, cudaStream_t st) {
+    const size_t smem = gdn_tc_layout(prm.N, prm.NPAD, prm.K, (int)sizeof(Tin)).total;
+    cudaError_t e = cudaFuncSetAttribute(k_gdn_tc<Tin, Tout, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_gdn_tc<Tin, Tout, KT><<<counted(dim3(prm.Hk, prm.B, prm.L)), kThr, smem, st>>>(prm, map);
+    return cudaGetLastError();
+}
+
+// the common conv width 4 gets its own instance; any other width up to kMaxK the generic one
 template <typename Tin, typename Tout>
 static cudaError_t gdn_tc_go(const GdnTcParams& prm, const CUtensorMap& map, cudaStream_t st) {
-    const size_t smem = gdn_tc_layout(prm.N, prm.NPAD).total;
-    cudaError_t e = cudaFuncSetAttribute(k_gdn_tc<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_gdn_tc<Tin, Tout><<<counted(dim3(prm.Hk, prm.B, prm.L)), kThr, smem, st>>>(prm, map);
-    return cudaGetLastError();
+    return prm.K == 4 ? gdn_tc_go_k<Tin, Tout, 4>(prm, map, st) : gdn_tc_go_k<Tin, Tout, kMaxK>(prm, map, st);
 }
 
 cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype in, ddt_dtype out, const void* x,
