@@ -68,10 +68,10 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     L.s0 = off;
     off += (size_t)kDV * kDK * 4;
     L.u = off;
-    // R (one column per value channel), first used for the Gram rows [N][2N]
-    size_t ub = (size_t)N * (kDV > 2 * N ? kDV : 2 * N) * 4;
+    // R (one column per value channel), first used for the Gram rows [N][2N + 1]
+    size_t ub = (size_t)N * (kDV > 2 * N + 1 ? kDV : 2 * N + 1) * 4;
     if (L.u + ub < L.s0 + kq_bytes) ub = L.s0 + kq_bytes - L.u;
-    off += ub;
+    off += (ub + 15) & ~(size_t)15;
     L.kk = off;
     off += (size_t)N * kMD * 4;
     L.qk = off;
@@ -82,7 +82,8 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     off += (size_t)N * kMD * 4;
     L.tt = off;
     off += (size_t)N * kMaxK * 8;            // conv input row pointers
-    L.tr = off;
+    off = (off + 15) & ~(size_t)15;
+    L.tr = off;                              // 16-byte aligned: four taps load as one int4
     off += (size_t)N * kMaxK * 4;            // conv input rows as staging-row indices
     L.alist = off;
     off += (size_t)N * kMD * 4;
@@ -344,7 +345,8 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t gcol = 0;           // D buffer 0, free until the first head's MMA
-    float* gram = ubuf;                // [N][2N]: k_t.k_s | k_t.q_s
+    float* gram = ubuf;                // [N][2N + 1]: k_t.k_s | k_t.q_s, odd stride (no bank conflicts)
+    const int gs = 2 * N + 1;
     if (tid == 32) {
         const uint32_t idesc = tc::idesc_tf32(128, p.NPAD, false, false);
         const uint64_t dh = tc::desc_sw128(tc::smem_u32(sKQ), 16, 1024);
@@ -374,16 +376,25 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
         if (gok) {
             tc::tc_fence_after();
             const uint32_t rowaddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + gcol;
-            for (int c0 = 0; c0 < p.QOFF + N; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(rowaddr + c0, v);
-                tc::tmem_wait_ld();
-                if (t < nn) {
+            // the k columns [0, N) then the q columns [QOFF, QOFF + N), 32 at a time
+            for (int part = 0; part < 2; ++part) {
+                const int cb = part ? p.QOFF : 0, ob = part ? N : 0;
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    uint32_t v0[16], v1[16];
+                    const bool two = c0 + 16 < N;
+                    tmem_ld16(rowaddr + cb + c0, v0);
+                    if (two) tmem_ld16(rowaddr + cb + c0 + 16, v1);
+                    tc::tmem_wait_ld();
+                    if (t < nn) {
+                        float* gr = gram + t * gs + ob + c0;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int c = c0 + i;
-                        if (c < N) gram[t * 2 * N + c] = __uint_as_float(v[i]);
-                        else if (c >= p.QOFF && c < p.QOFF + N) gram[t * 2 * N + N + (c - p.QOFF)] = __uint_as_float(v[i]);
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i < N) gr[i] = __uint_as_float(v0[i]);
+                        if (two) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (c0 + 16 + i < N) gr[16 + i] = __uint_as_float(v1[i]);
+                        }
                     }
                 }
             }
@@ -395,11 +406,11 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
         const int dep = sdep[t];
         if (m > dep) continue;
         if (m == dep) {
-            sqself[t] = gram[t * 2 * N + N + t];  // k_t . q_t
+            sqself[t] = gram[t * gs + N + t];  // k_t . q_t
         } else {
             const int s = alist[t * kMD + m];
-            skk[t * kMD + m] = gram[t * 2 * N + s];      // k_t . k_s
-            sqk[t * kMD + m] = gram[s * 2 * N + N + t];  // k_s . q_t
+            skk[t * kMD + m] = gram[t * gs + s];      // k_t . k_s
+            sqk[t * kMD + m] = gram[s * gs + N + t];  // k_s . q_t
         }
     }
     tc::tc_fence_before();
@@ -524,60 +535,71 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             float wv[KT];
 #pragma unroll
             for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
-            for (int t0 = 0; t0 < nn; t0 += 16) {
+            // each thread takes whole 16-node chunks (its half's chunks alternate with the
+            // other half's), so all 16 loaded columns are used and 16 nodes are in flight
+            for (int c = quad; c * 16 < nn; c += 2) {
+                const int t0 = c * 16;
                 uint32_t ks[16];
                 tmem_ld16(dcol + t0, ks);
-                float vin[8][KT];
+                float vin[16][KT];
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = min(t0 + 2 * uu + quad, nn - 1);
+                for (int uu = 0; uu < 16; ++uu) {
+                    const int t = min(t0 + uu, nn - 1);
+                    if constexpr (KT == 4) {
+                        const int4 r4 = *reinterpret_cast<const int4*>(trow + t * 4);
+                        vin[uu][0] = to_f32(sv[r4.x * kDV + j]);
+                        vin[uu][1] = to_f32(sv[r4.y * kDV + j]);
+                        vin[uu][2] = to_f32(sv[r4.z * kDV + j]);
+                        vin[uu][3] = to_f32(sv[r4.w * kDV + j]);
+                    } else {
 #pragma unroll
-                    for (int q = 0; q < KT; ++q) vin[uu][q] = (q < K) ? to_f32(sv[trow[t * K + q] * kDV + j]) : 0.f;
+                        for (int q = 0; q < KT; ++q) vin[uu][q] = (q < K) ? to_f32(sv[trow[t * K + q] * kDV + j]) : 0.f;
+                    }
                 }
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = t0 + 2 * uu + quad;
+                for (int uu = 0; uu < 16; ++uu) {
+                    const int t = t0 + uu;
                     float acc = 0.f;
 #pragma unroll
                     for (int q = 0; q < KT; ++q) acc = fmaf(wv[q], vin[uu][q], acc);
-                    if (t < nn)
-                        ubuf[t * kDV + j] = sbeta[t] * (silu_g(acc) - sg[t] * __uint_as_float(ks[2 * uu + quad]));
+                    if (t < nn) ubuf[t * kDV + j] = sbeta[t] * (silu_g(acc) - sg[t] * __uint_as_float(ks[uu]));
                 }
             }
             named_bar(1, kEpi);
-            // pass C: outputs as independent sums over each node's own path; the 8 nodes of
+            // pass C: outputs as independent sums over each node's own path; the 16 nodes of
             // a chunk advance one ancestor level at a time, so their loads overlap
-            for (int t0 = 0; t0 < N; t0 += 16) {
+            for (int c = quad; c * 16 < N; c += 2) {
+                const int t0 = c * 16;
                 uint32_t qs[16];
                 if (t0 < nn) {
                     tmem_ld16(dcol + p.QOFF + t0, qs);
                     tc::tmem_wait_ld();
                 }
-                float ot[8];
-                int dp[8];
+                float ot[16];
+                int dp[16];
                 int md = 0;
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = t0 + 2 * uu + quad;
+                for (int uu = 0; uu < 16; ++uu) {
+                    const int t = t0 + uu;
                     dp[uu] = 0;
                     ot[uu] = 0.f;
                     if (t < nn) {
                         dp[uu] = sdep[t];
-                        ot[uu] = fmaf(sg[t], __uint_as_float(qs[2 * uu + quad]), sqself[t] * ubuf[t * kDV + j]);
+                        ot[uu] = fmaf(sg[t], __uint_as_float(qs[uu]), sqself[t] * ubuf[t * kDV + j]);
                     }
                     md = max(md, dp[uu]);
                 }
                 for (int a = 0; a < md; ++a) {
 #pragma unroll
-                    for (int uu = 0; uu < 8; ++uu) {
-                        const int t = t0 + 2 * uu + quad;
+                    for (int uu = 0; uu < 16; ++uu) {
+                        const int t = t0 + uu;
                         if (a < dp[uu]) ot[uu] = fmaf(scb[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot[uu]);
                     }
                 }
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = t0 + 2 * uu + quad;
+                for (int uu = 0; uu < 16; ++uu) {
+                    const int t = t0 + uu;
                     if (t < N) obase[((long)t * p.Hv + h) * kDV + j] = from_f32<Tout>(ot[uu]);
                 }
             }
