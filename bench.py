@@ -204,6 +204,13 @@ def workload_desc(c):
     return ", ".join(parts)
 
 
+def arm_config(cfg, prefix_total, nodes_per_round, world):
+    """The `config` object both arms print."""
+    return {"workload": workload_desc(cfg), "B": cfg["B"], "budget": cfg["budget"],
+            "nodes_per_round": nodes_per_round, "prefix_total": prefix_total,
+            "l2": "inputs larger than L2 (tens of GB per round)", "parallelism": f"replicas x{world}"}
+
+
 # --------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local):
     from tree_speculative_decoding_02_gb300 import ddt, synth
@@ -289,38 +296,58 @@ def run_ours(args, rank, world, local):
     value = nodes_total / (ms_max / 1e3)
     per_kernel = {k: statistics.mean(a.elapsed_time(b) for a, b in ev[k]) for k in KERNELS}
 
-    # end to end through the public API: per-round inputs from pinned host memory,
-    # emitted tokens back to the host, inside the timed region
-    ins = r.round_inputs()
-    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in ins.items()}
-    for k, v in ins.items():
+    # end to end through the public API: each round's inputs are copied from pinned host
+    # memory and its emitted tokens copied back, inside the timed region.  The inputs are
+    # double-buffered: round i+1's copy runs on a copy stream while round i computes, the
+    # way a serving loop overlaps them; the first round's copy is not hidden.
+    slots = [r.round_inputs()]
+    slots.append({k: torch.empty_like(v) for k, v in slots[0].items()})
+    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in slots[0].items()}
+    for k, v in slots[0].items():
         host[k].copy_(v)
     outs = r.round_outputs()
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    cs = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k, v in ins.items():
-            v.copy_(host[k], non_blocking=True)
-        r.restore_prefix()
-        r.step()
-        for k, v in outs.items():
-            host_out[k].copy_(v, non_blocking=True)
+    def copy_in(slot):
+        with torch.cuda.stream(cs):
+            cs.wait_event(free[slot])
+            for k, v in slots[slot].items():
+                v.copy_(host[k], non_blocking=True)
+            copied[slot].record(cs)
 
-    for _ in range(max(1, min(args.warmup, 2))):
-        e2e_step()
+    def e2e_run(n):
+        for sl in range(2):
+            free[sl].record(st)
+        copy_in(0)
+        for i in range(n):
+            sl = i % 2
+            if i + 1 < n:
+                copy_in(1 - sl)
+            st.wait_event(copied[sl])
+            r.bind_inputs(slots[sl])
+            r.restore_prefix()
+            r.step()
+            free[sl].record(st)
+            for k, v in outs.items():
+                host_out[k].copy_(v, non_blocking=True)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    n_e2e = max(2, min(args.steps, 5))
+    n_e2e = max(2, args.steps)
     e0.record(st)
-    for _ in range(n_e2e):
-        e2e_step()
+    e2e_run(n_e2e)
     e1.record(st)
     torch.cuda.synchronize()
     barrier(world)
+    r.bind_inputs(slots[0])
     e_ms = all_max(e0.elapsed_time(e1), world, dev)
     e2e_value = all_sum(nodes_per_step * n_e2e, world, dev) / (e_ms / 1e3)
 
@@ -339,17 +366,15 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg),
-                   "B": cfg["B"], "budget": cfg["budget"], "nodes_per_round": nodes_per_step,
-                   "prefix_total": int(r.prefix0.sum()),
-                   "l2": "inputs larger than L2 (tens of GB per round)", "parallelism": f"replicas x{world}"},
+        "config": arm_config(cfg, int(r.prefix0.sum()), nodes_per_step, world),
         "hbm_gbs_round": rb / (step_ms / 1e3) / 1e9,
         "hbm_frac_round": rb / (step_ms / 1e3) / 1e9 / hbm_peak,
         "per_kernel_ms": per_kernel,
         "roofline": {"bound": "tensor", "kernel": "ddt_tree_attn", "achieved": tflops, "peak": tc_peak,
                      "unit": "TFLOP/s", "frac": tflops / tc_peak, "traffic": attn_traffic(args.workload),
                      "algorithmic_flops": fl, "algorithmic_bytes": by, "peak_note": "of measured (sustained)"},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "inputs": "pinned host, double-buffered: round i+1 copied on a copy stream during round i"},
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -376,20 +401,30 @@ def request_from_round(r, b):
             "S": np.swapaxes(_f64(g.S[:, b:b + 1]), -1, -2)}
 
 
-def request_synth(cfg, b, workload):
+def workload_prefixes(cfg, workload):
+    """The committed prefix lengths of the workload's requests (as the GPU round draws them)."""
+    from tree_speculative_decoding_02_gb300 import synth
+
+    if "P" in cfg:
+        return np.full(cfg["B"], cfg["P"], np.int64)
+    return synth.prefix_lengths(cfg["B"], cfg["P_lo"], cfg["P_hi"], g=synth.gen(workload, 2)).numpy().astype(np.int64)
+
+
+def request_synth(cfg, b, workload, Lf=None, Lg=None):
     """One request of the workload drawn directly with the synth module (B = 1), for the
-    reference arm, which must not touch the CUDA library."""
+    reference arm, which must not touch the CUDA library.  Lf / Lg: how many attention /
+    GDN layers to draw (default: all)."""
     from tree_speculative_decoding_02_gb300 import synth
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     wl = 100 * workload + b
-    P = int(synth.prefix_lengths(cfg["B"], cfg["P_lo"], cfg["P_hi"], g=synth.gen(workload, 2))[b])
+    P = int(workload_prefixes(cfg, workload)[b])
     N = cfg["budget"] + 1
     dt = cfg["dtype"]
-    a = synth.attn_inputs(cfg["Lf"], 1, N, cfg["Hq"], cfg["Hkv"], cfg["d"], P, [P], workload=wl, dtype=dt,
+    a = synth.attn_inputs(Lf or cfg["Lf"], 1, N, cfg["Hq"], cfg["Hkv"], cfg["d"], P, [P], workload=wl, dtype=dt,
                           device=dev, poison=False)
-    g = synth.gdn_inputs(cfg["Lg"], 1, N, cfg["Hk"], cfg["Hv"], cfg["dk"], cfg["dv"], cfg["conv_k"], workload=wl,
-                         dtype=dt, device=dev)
+    g = synth.gdn_inputs(Lg or cfg["Lg"], 1, N, cfg["Hk"], cfg["Hv"], cfg["dk"], cfg["dv"], cfg["conv_k"],
+                         workload=wl, dtype=dt, device=dev)
     return {"P": P, "draft_logits": _f64(synth.draft_logits(1, cfg["D"], cfg["V"], std=cfg["logit_std"],
                                                            boost=cfg["boost"], g=synth.gen(wl, 1), dtype=dt)),
             "root": np.array([b], np.int32),
@@ -400,24 +435,35 @@ def request_synth(cfg, b, workload):
 
 
 def oracle_round(cfg, q):
-    """One request's full round (build, attention, GDN, walk, commit) through the plain
-    oracle; returns (drafted nodes, seconds spent in the oracle)."""
+    """One request's round (build, attention, GDN, walk, commit) through the plain oracle
+    on the layers present in `q`; the attention and GDN stages and the commit are scaled
+    to the workload's full layer counts (the work is the same for every layer).  Returns
+    (drafted nodes, seconds)."""
     import oracle
 
-    t = time.perf_counter()
     P = q["P"]
+    sa = cfg["Lf"] / q["q"].shape[0]
+    sg = cfg["Lg"] / q["x"].shape[0]
+    t0 = time.perf_counter()
     tree = oracle.build_tree(q["draft_logits"], q["root"], [P], cfg["top_k"], cfg["budget"])
+    t1 = time.perf_counter()
     oracle.tree_attn(q["q"], q["k_tree"], q["v_tree"], q["k_cache"], q["v_cache"], [P], tree["n_nodes"],
                      tree["anc"], 1.0 / math.sqrt(cfg["d"]))
+    t2 = time.perf_counter()
     oracle.tree_gdn(q["x"], q["conv_w"], q["conv_state"], q["beta"], q["decay"], q["S"], tree["parent"],
                     tree["n_nodes"], cfg["Hk"])
+    t3 = time.perf_counter()
     wk = oracle.walk(tree["token"], tree["parent"], tree["n_nodes"], cfg["D"], target_logits=q["target_logits"])
+    t4 = time.perf_counter()
     pad = ((0, 0), (0, 0), (0, 0), (0, cfg["D"] + 1), (0, 0))
-    oracle.commit(wk["acc_nodes"], wk["acc_len"], [P], k_tree=q["k_tree"], v_tree=q["v_tree"],
-                  k_cache=np.pad(q["k_cache"], pad), v_cache=np.pad(q["v_cache"], pad), x=q["x"],
-                  conv_w=q["conv_w"], beta=q["beta"], decay=q["decay"], S=q["S"], conv_state=q["conv_state"],
-                  Hk=cfg["Hk"])
-    return int(tree["n_nodes"][0]) - 1, time.perf_counter() - t
+    kc, vc = np.pad(q["k_cache"], pad), np.pad(q["v_cache"], pad)
+    t5 = time.perf_counter()
+    oracle.commit(wk["acc_nodes"], wk["acc_len"], [P], k_tree=q["k_tree"], v_tree=q["v_tree"], k_cache=kc,
+                  v_cache=vc, x=q["x"], conv_w=q["conv_w"], beta=q["beta"], decay=q["decay"], S=q["S"],
+                  conv_state=q["conv_state"], Hk=cfg["Hk"])
+    t6 = time.perf_counter()
+    el = (t1 - t0) + sa * (t2 - t1) + sg * (t3 - t2) + (t4 - t3) + max(sa, sg) * (t6 - t5)
+    return int(tree["n_nodes"][0]) - 1, el
 
 
 def cpu_baseline(r, seconds=15.0, max_requests=8):
@@ -440,7 +486,8 @@ def cpu_baseline(r, seconds=15.0, max_requests=8):
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the plain CPU oracle, one request's full round per step."""
+    """The reference arm: the plain CPU oracle.  Each step is one request's round on a
+    quarter of the attention and GDN layers, scaled to the full layer counts."""
     if rank != 0:
         return None
     import oracle
@@ -450,21 +497,28 @@ def run_reference(args, rank, world):
     oracle.set_threads(cores)
     oracle.build()
     cfg = dict(synth.WORKLOADS[args.workload])
+    lf, lg = max(1, cfg.get("Lf", 0) // 4), max(1, cfg.get("Lg", 0) // 4)
+
+    def one(i):
+        return oracle_round(cfg, request_synth(cfg, i % cfg["B"], args.workload, Lf=lf, Lg=lg))
+
     for i in range(args.warmup):
-        oracle_round(cfg, request_synth(cfg, i % cfg["B"], args.workload))
+        one(i)
     nodes, el = 0, 0.0
     for i in range(args.steps):
-        n, t = oracle_round(cfg, request_synth(cfg, (args.warmup + i) % cfg["B"], args.workload))
+        n, t = one(args.warmup + i)
         nodes += n
         el += t
     v = nodes / el
+    sample = (f"per step one request's round (budget {cfg['budget']}), build and walk in full, {lf} of "
+              f"{cfg['Lf']} attention and {lg} of {cfg['Lg']} GDN layers timed and scaled to all layers; "
+              f"fp64 oracle time only")
+    prefix = workload_prefixes(cfg, args.workload)
     return {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "batched-round-bf16, one request's full round per step", "B": 1,
-                       "budget": cfg["budget"]},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "one request's full round per step (oracle time only)"},
+            "config": arm_config(cfg, int(prefix.sum()), cfg["B"] * cfg["budget"], world),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

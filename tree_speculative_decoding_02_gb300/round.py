@@ -124,5 +124,15 @@ class Round:
             ins.update(x=self.gdn.x, beta=self.gdn.beta, decay=self.gdn.decay)
         return ins
 
+    def bind_inputs(self, ins: dict):
+        """Point the round at another set of per-round input tensors (same keys, shapes and
+        dtypes as `round_inputs()`), e.g. the other half of a double buffer."""
+        self.draft_logits, self.root_token, self.target_logits = ins["draft_logits"], ins["root_token"], \
+            ins["target_logits"]
+        if self.Lf:
+            self.attn.q, self.attn.k_tree, self.attn.v_tree = ins["q"], ins["k_tree"], ins["v_tree"]
+        if self.Lg:
+            self.gdn.x, self.gdn.beta, self.gdn.decay = ins["x"], ins["beta"], ins["decay"]
+
     def round_outputs(self):
         return {"emitted": self.walk["emitted"], "n_emitted": self.walk["n_emitted"]}
