@@ -9,9 +9,10 @@
 //
 //   k_commit_kv     grid (A, La*Hkv, B): 16-byte vector copy of one tree row into the
 //                   cache at prefix_len + j.
-//   k_commit_gdn    grid (Hv, B, Lg): the committed state (dv x dk fp32) is staged in
-//                   shared memory once, advanced along the accepted path (<= A rank-one
-//                   delta steps) and written back in place: one HBM read and one write.
+//   k_commit_gdn    grid (Hv, B, Lg): the committed state (dv x dk fp32) is held in
+//                   registers (two threads per row), advanced along the accepted path
+//                   (<= A rank-one delta steps) and written back in place: one HBM read
+//                   and one write.
 //   k_commit_conv   grid (Lg, B): last K-1 raw inputs of [conv state ; path inputs].
 //   k_commit_final  prefix_len, commit indices and status (runs last: the kernels above
 //                   read the old prefix_len).
@@ -67,17 +68,26 @@ __global__ void k_commit_kv(int B, int N, int A, int Hkv, int d, int Pcap, int v
 
 __device__ __forceinline__ float silu_c(float z) { return z / (1.f + __expf(-z)); }
 
+// One CTA per (value head, request, layer), 2 threads per state row (DV rows): the state
+// lives in registers, DK/2 entries a thread.  Prologue: conv + SiLU of the k and v
+// channels of every accepted node (all loads in flight together), k norms and gates into
+// shared memory.  Then the a + 1 delta steps need no barrier: each row's S k is a pair
+// of partial dots joined by one shuffle, and the rank-one update is in registers.
 template <typename Tx, int DK, int DV>
-__global__ void __launch_bounds__(256) k_commit_gdn(int B, int N, int A, int Hk, int Hv, int K, int cap_check,
-                                                     int Pcap, const Tx* __restrict__ x, const Tx* __restrict__ conv_w,
-                                                     const Tx* __restrict__ conv_state,
-                                                     const float* __restrict__ beta, const float* __restrict__ decay,
-                                                     float* __restrict__ S, const int32_t* __restrict__ acc_nodes,
-                                                     const int32_t* __restrict__ acc_len,
-                                                     const int32_t* __restrict__ prefix_len) {
-    extern __shared__ __align__(16) float sS[];  // [DV][DK + 4]
-    __shared__ float s_k[DK], s_v[DV], s_u[DV];
-    __shared__ float s_red[8];
+__global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, int Hk, int Hv, int K, int cap_check,
+                                                       int Pcap, const Tx* __restrict__ x,
+                                                       const Tx* __restrict__ conv_w,
+                                                       const Tx* __restrict__ conv_state,
+                                                       const float* __restrict__ beta,
+                                                       const float* __restrict__ decay, float* __restrict__ S,
+                                                       const int32_t* __restrict__ acc_nodes,
+                                                       const int32_t* __restrict__ acc_len,
+                                                       const int32_t* __restrict__ prefix_len) {
+    constexpr int kT = 2 * DV, kH = DK / 2;
+    extern __shared__ __align__(16) float sm[];
+    float* s_k = sm;                 // [A][DK]  normalised k of each accepted node
+    float* s_v = s_k + A * DK;       // [A][DV]
+    float* s_g = s_v + A * DV;       // [A][2]   decay, beta
     __shared__ int s_ok;
     const int h = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -88,64 +98,91 @@ __global__ void __launch_bounds__(256) k_commit_gdn(int B, int N, int A, int Hk,
     const int C = 2 * Hk * DK + Hv * DV;
     const int g = h / (Hv / Hk);
     const long lb = (long)l * B + b;
-    float* Sg = S + (lb * Hv + h) * (long)DV * DK;
-    for (int e = tid; e < DV * DK / 4; e += 256) {
-        const int r = e / (DK / 4), c4 = e % (DK / 4);
-        *reinterpret_cast<float4*>(sS + r * (DK + 4) + c4 * 4) = reinterpret_cast<const float4*>(Sg)[e];
-    }
     const int32_t* path = acc_nodes + (long)b * A;
     const Tx* xb = x + lb * N * C;
     const Tx* cs = conv_state + lb * (K - 1) * C;
     const Tx* wl = conv_w + (long)l * C * K;
-    for (int t = 0; t <= a; ++t) {
-        // conv + SiLU of the k and v channels, window along the accepted path
-        for (int e = tid; e < DK + DV; e += 256) {
-            const int c = (e < DK) ? (Hk * DK + g * DK + e) : (2 * Hk * DK + h * DV + e - DK);
-            float acc = 0.f;
-            for (int j = 0; j < K; ++j) {
-                const int back = K - 1 - j;
-                const float in = (back <= t) ? to_f32(xb[(long)path[t - back] * C + c])
-                                             : to_f32(cs[(long)(K - 1 - (back - t)) * C + c]);
-                acc = fmaf(to_f32(wl[(long)c * K + j]), in, acc);
-            }
-            const float y = silu_c(acc);
-            if (e < DK) s_k[e] = y;
-            else s_v[e - DK] = y;
-        }
-        __syncthreads();
-        float part = 0.f;
-        for (int i = tid; i < DK; i += 256) part = fmaf(s_k[i], s_k[i], part);
-        part = warp_sum(part);
-        if (lane == 0) s_red[warp] = part;
-        __syncthreads();
-        float nk = 0.f;
+
+    // conv + SiLU of the k and v channels along the accepted path
+    for (int e = tid; e < DK + DV; e += kT) {
+        const int c = (e < DK) ? (Hk * DK + g * DK + e) : (2 * Hk * DK + h * DV + e - DK);
+        float w[8];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) nk += s_red[w];
-        const float rk = rsqrtf(nk + 1e-6f);
-        const float at = decay[(lb * N + path[t]) * Hv + h];
-        const float bt = beta[(lb * N + path[t]) * Hv + h];
-        // u = b (v - a S k^)
-        for (int j = tid; j < DV; j += 256) {
-            float pred = 0.f;
-            const float* row = sS + j * (DK + 4);
-            for (int i = 0; i < DK; i += 4) {
-                const float4 s4 = *reinterpret_cast<const float4*>(row + i);
-                pred = fmaf(s4.x, s_k[i], fmaf(s4.y, s_k[i + 1], fmaf(s4.z, s_k[i + 2], fmaf(s4.w, s_k[i + 3], pred))));
+        for (int q = 0; q < 8; ++q) w[q] = q < K ? to_f32(wl[(long)c * K + q]) : 0.f;
+#pragma unroll 2
+        for (int t = 0; t <= a; ++t) {
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (q < K) {
+                    const int back = K - 1 - q;
+                    const float in = (back <= t) ? to_f32(xb[(long)path[t - back] * C + c])
+                                                 : to_f32(cs[(long)(K - 1 - (back - t)) * C + c]);
+                    acc = fmaf(w[q], in, acc);
+                }
             }
-            s_u[j] = bt * (s_v[j] - at * pred * rk);
+            if (e < DK) s_k[t * DK + e] = silu_c(acc);
+            else s_v[t * DV + e - DK] = silu_c(acc);
         }
-        __syncthreads();
-        // S <- a S + u k^T
-        for (int e = tid; e < DV * DK; e += 256) {
-            const int j = e / DK, i = e % DK;
-            sS[j * (DK + 4) + i] = fmaf(at, sS[j * (DK + 4) + i], s_u[j] * s_k[i] * rk);
+    }
+    for (int t = tid; t <= a; t += kT) {
+        s_g[2 * t] = decay[(lb * N + path[t]) * Hv + h];
+        s_g[2 * t + 1] = beta[(lb * N + path[t]) * Hv + h];
+    }
+    __syncthreads();
+    // the state rows (their loads overlap the k normalisation): row j = tid / 2,
+    // columns 8m + 4 (tid & 1) .. + 3 for m < DK / 8
+    const int j = tid >> 1, hf = tid & 1;
+    float* Sg = S + (lb * Hv + h) * (long)DV * DK;
+    float sr[kH];
+#pragma unroll
+    for (int m = 0; m < DK / 8; ++m) {
+        const float4 v4 = *reinterpret_cast<const float4*>(Sg + (long)j * DK + 8 * m + 4 * hf);
+        sr[4 * m] = v4.x;
+        sr[4 * m + 1] = v4.y;
+        sr[4 * m + 2] = v4.z;
+        sr[4 * m + 3] = v4.w;
+    }
+
+    // k normalisation: one warp per node
+    for (int t = warp; t <= a; t += kT / 32) {
+        float ss = 0.f;
+        for (int i = lane; i < DK; i += 32) ss = fmaf(s_k[t * DK + i], s_k[t * DK + i], ss);
+        ss = warp_sum(ss);
+        const float rk = rsqrtf(ss + 1e-6f);
+        __syncwarp();
+        for (int i = lane; i < DK; i += 32) s_k[t * DK + i] *= rk;
+    }
+    __syncthreads();
+
+    for (int t = 0; t <= a; ++t) {
+        const float* kt = s_k + t * DK;
+        const float at = s_g[2 * t], bt = s_g[2 * t + 1];
+        float part = 0.f;
+#pragma unroll
+        for (int m = 0; m < DK / 8; ++m) {
+            const float4 k4 = *reinterpret_cast<const float4*>(kt + 8 * m + 4 * hf);
+            part = fmaf(sr[4 * m], k4.x, part);
+            part = fmaf(sr[4 * m + 1], k4.y, part);
+            part = fmaf(sr[4 * m + 2], k4.z, part);
+            part = fmaf(sr[4 * m + 3], k4.w, part);
         }
-        __syncthreads();
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        const float u = bt * (s_v[t * DV + j] - at * part);   // u = b (v - a S k^)
+        __syncwarp();  // re-read k below rather than keep DK/2 more values live
+#pragma unroll
+        for (int m = 0; m < DK / 8; ++m) {                     // S <- a S + u k^T
+            const float4 k4 = *reinterpret_cast<const float4*>(kt + 8 * m + 4 * hf);
+            sr[4 * m] = fmaf(at, sr[4 * m], u * k4.x);
+            sr[4 * m + 1] = fmaf(at, sr[4 * m + 1], u * k4.y);
+            sr[4 * m + 2] = fmaf(at, sr[4 * m + 2], u * k4.z);
+            sr[4 * m + 3] = fmaf(at, sr[4 * m + 3], u * k4.w);
+        }
     }
-    for (int e = tid; e < DV * DK / 4; e += 256) {
-        const int r = e / (DK / 4), c4 = e % (DK / 4);
-        reinterpret_cast<float4*>(Sg)[e] = *reinterpret_cast<const float4*>(sS + r * (DK + 4) + c4 * 4);
-    }
+#pragma unroll
+    for (int m = 0; m < DK / 8; ++m)
+        *reinterpret_cast<float4*>(Sg + (long)j * DK + 8 * m + 4 * hf) =
+            make_float4(sr[4 * m], sr[4 * m + 1], sr[4 * m + 2], sr[4 * m + 3]);
 }
 
 template <typename Tx>
@@ -194,11 +231,11 @@ static cudaError_t commit_gdn_go(int B, int N, int A, int Lg, int Hk, int Hv, in
                                  const void* x, const void* w, const void* cs, const float* beta,
                                  const float* decay, float* S, const int32_t* an, const int32_t* al,
                                  const int32_t* pl, cudaStream_t st) {
-    const size_t smem = sizeof(float) * DV * (DK + 4);
+    const size_t smem = sizeof(float) * (size_t)A * (DK + DV + 2);
     cudaError_t e = cudaFuncSetAttribute(k_commit_gdn<Tx, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    k_commit_gdn<Tx, DK, DV><<<counted(dim3(Hv, B, Lg)), 256, smem, st>>>(
+    k_commit_gdn<Tx, DK, DV><<<counted(dim3(Hv, B, Lg)), 2 * DV, smem, st>>>(
         B, N, A, Hk, Hv, K, cap, Pcap, static_cast<const Tx*>(x), static_cast<const Tx*>(w),
         static_cast<const Tx*>(cs), beta, decay, S, an, al, pl);
     return cudaGetLastError();
