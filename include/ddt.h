@@ -160,6 +160,34 @@ ddt_status ddt_tree_attn(int n_layers, int B, int N, int Hq, int Hkv, int d, int
                          void* workspace, size_t ws_bytes, ddt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * ddt_tree_attn_paged -- ddt_tree_attn over a paged prefix cache ([NOTES] "Where the
+ * next step is": fused ancestor-mask branch attention over paged KV blocks).
+ *
+ * Same result as ddt_tree_attn where request b's prefix row p (p < prefix_len[b]) is
+ *   k_pages[l][block_table[b][p / page_size]][g][p % page_size][:]   (same for v).
+ *   k_pages, v_pages [L][num_pages][Hkv][page_size][d] (bf16; head-major pages).
+ *   block_table [B][max_pages] int32: physical page of each logical page; only the
+ *     first ceil(prefix_len[b] / page_size) entries are read.  Rows of the last page past
+ *     prefix_len[b] may hold anything (they are masked, and their V rows are zeroed
+ *     before use, so NaN there does no harm).
+ *   page_size: 8, 16, 32, or a multiple of 64.  Capacity is max_pages * page_size.
+ *   status [B]: as ddt_tree_attn, plus DDT_ERR_INVALID_ARG when a block-table entry
+ *     the prefix needs is outside [0, num_pages) (that request's rows are then zero).
+ * bf16 inputs, d in {64, 128, 256} only (DDT_ERR_UNSUPPORTED otherwise).
+ * workspace: ddt_tree_attn_paged_workspace(...) bytes, 16-byte aligned.
+ * ------------------------------------------------------------------------------- */
+size_t ddt_tree_attn_paged_workspace(int n_layers, int B, int N, int Hq, int Hkv, int d,
+                                     int page_size, int max_pages);
+ddt_status ddt_tree_attn_paged(int n_layers, int B, int N, int Hq, int Hkv, int d,
+                               int page_size, int num_pages, int max_pages,
+                               ddt_dtype in_dtype, ddt_dtype out_dtype, const void* q,
+                               const void* k_tree, const void* v_tree, const void* k_pages,
+                               const void* v_pages, const int32_t* block_table,
+                               const int32_t* prefix_len, const int32_t* n_nodes,
+                               const uint32_t* anc, float scale, void* o, int32_t* status,
+                               void* workspace, size_t ws_bytes, ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * ddt_tree_gdn -- [NOTES] "Why hybrid attention makes it hard" / "Where the next step
  * is": each node reads the GDN and conv state of its parent and writes scratch, never
  * the committed state; [GDN] the gated delta rule.
@@ -244,6 +272,22 @@ ddt_status ddt_commit(int B, int N, int A,
                       const float* decay, float* S, void* conv_state,
                       const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len,
                       int32_t* src_row, int32_t* dst_pos, int32_t* status, ddt_stream_t stream);
+
+/* ddt_commit_paged -- ddt_commit for paged KV caches (the layout of ddt_tree_attn_paged):
+ * accepted row j of request b goes to position prefix_len[b] + j, i.e. row
+ * (prefix_len[b] + j) % page_size of page block_table[b][(prefix_len[b] + j) / page_size]
+ * of k_pages / v_pages [L][num_pages][Hkv][page_size][d].  Capacity is max_pages *
+ * page_size; a block-table entry outside [0, num_pages) for a position being written
+ * makes the request's status DDT_ERR_INVALID_ARG and nothing of it is committed.  The
+ * GDN and conv-state part, the outputs and the other statuses are those of ddt_commit. */
+ddt_status ddt_commit_paged(int B, int N, int A, int n_attn_layers, int Hkv, int d, int page_size,
+                            int num_pages, int max_pages, const int32_t* block_table,
+                            ddt_dtype kv_dtype, const void* k_tree, const void* v_tree,
+                            void* k_pages, void* v_pages, int n_gdn_layers, int Hk, int Hv, int dk,
+                            int dv, int conv_k, ddt_dtype x_dtype, const void* x, const void* conv_w,
+                            const float* beta, const float* decay, float* S, void* conv_state,
+                            const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len,
+                            int32_t* src_row, int32_t* dst_pos, int32_t* status, ddt_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -46,7 +46,8 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             for name in ("ddto_build_tree", "ddto_attn_row", "ddto_tree_attn", "ddto_gdn_unit",
-                         "ddto_tree_gdn", "ddto_walk", "ddto_commit"):
+                         "ddto_tree_gdn", "ddto_walk", "ddto_commit", "ddto_gather_pages",
+                         "ddto_scatter_pages"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -120,6 +121,37 @@ def attn_row(q, k_prefix, v_prefix, k_tree, v_tree, anc_row, n_nodes: int, scale
     rc = lib.ddto_attn_row(P, int(n_nodes), d, _p(q), _p(kp), _p(vp), ctypes.c_long(d), _p(kt), _p(vt),
                            ctypes.c_long(d), _p(_u32(anc_row)), ctypes.c_double(scale), _p(out))
     _check(rc, "attn_row")
+    return out
+
+
+def gather_pages(pages, block_table, prefix_len, Pcap: int):
+    """pages [L][num_pages][Hkv][page][d], block_table [B][max_pages] -> the contiguous
+    cache [L][B][Hkv][Pcap][d] (rows >= prefix_len zero)."""
+    lib = _load()
+    pages = _f64(pages)
+    L, num_pages, Hkv, page, d = pages.shape
+    bt = _i32(block_table)
+    B, max_pages = bt.shape
+    cache = np.zeros((L, B, Hkv, Pcap, d))
+    rc = lib.ddto_gather_pages(L, B, Hkv, d, page, num_pages, max_pages, _p(pages), _p(bt), _p(_i32(prefix_len)),
+                               Pcap, _p(cache))
+    _check(rc, "gather_pages")
+    return cache
+
+
+def scatter_pages(cache, block_table, n_rows, pages):
+    """Rows [0, n_rows[b]) of the contiguous cache [L][B][Hkv][Pcap][d] into (a copy of)
+    pages [L][num_pages][Hkv][page][d]."""
+    lib = _load()
+    cache = _f64(cache)
+    L, B, Hkv, Pcap, d = cache.shape
+    out = _f64(pages).copy()
+    num_pages, page = out.shape[1], out.shape[3]
+    bt = _i32(block_table)
+    max_pages = bt.shape[1]
+    rc = lib.ddto_scatter_pages(L, B, Hkv, d, page, num_pages, max_pages, _p(cache), Pcap, _p(bt), _p(_i32(n_rows)),
+                                _p(out))
+    _check(rc, "scatter_pages")
     return out
 
 

@@ -645,3 +645,62 @@ int ddto_commit(int La, int B, int N, int Hkv, int d, int Pcap,
     }
     return DDTO_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Paged KV caches                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* [NOTES] "Where the next step is": the verifier must read the prefix from paged KV
+ * blocks.  Row p of a request's prefix lives at row p % page of page block_table[b][p/page]. */
+int ddto_gather_pages(int L, int B, int Hkv, int d, int page, int num_pages, int max_pages,
+                      const double* pages, const int32_t* block_table, const int32_t* prefix_len,
+                      int Pcap, double* cache) {
+    if (L < 1 || B < 1 || Hkv < 1 || d < 1 || page < 1 || num_pages < 1 || max_pages < 1 || Pcap < 0)
+        return DDTO_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int P = prefix_len[b];
+        if (P < 0 || P > Pcap || P > (long)max_pages * page) return DDTO_ERR_ARG;
+        for (int p = 0; p < P; ++p) {
+            const int pg = block_table[(long)b * max_pages + p / page];
+            if (pg < 0 || pg >= num_pages) return DDTO_ERR_ARG;
+        }
+    }
+    for (int l = 0; l < L; ++l)
+        for (int b = 0; b < B; ++b)
+            for (int g = 0; g < Hkv; ++g)
+                for (int p = 0; p < Pcap; ++p) {
+                    double* dst = cache + ((((long)l * B + b) * Hkv + g) * Pcap + p) * d;
+                    if (p >= prefix_len[b]) {
+                        for (int i = 0; i < d; ++i) dst[i] = 0.0;
+                        continue;
+                    }
+                    const int pg = block_table[(long)b * max_pages + p / page];
+                    const double* src = pages + ((((long)l * num_pages + pg) * Hkv + g) * page + p % page) * d;
+                    for (int i = 0; i < d; ++i) dst[i] = src[i];
+                }
+    return DDTO_OK;
+}
+
+int ddto_scatter_pages(int L, int B, int Hkv, int d, int page, int num_pages, int max_pages,
+                       const double* cache, int Pcap, const int32_t* block_table,
+                       const int32_t* n_rows, double* pages) {
+    if (L < 1 || B < 1 || Hkv < 1 || d < 1 || page < 1 || num_pages < 1 || max_pages < 1 || Pcap < 0)
+        return DDTO_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        if (n_rows[b] < 0 || n_rows[b] > Pcap || n_rows[b] > (long)max_pages * page) return DDTO_ERR_ARG;
+        for (int p = 0; p < n_rows[b]; ++p) {
+            const int pg = block_table[(long)b * max_pages + p / page];
+            if (pg < 0 || pg >= num_pages) return DDTO_ERR_ARG;
+        }
+    }
+    for (int l = 0; l < L; ++l)
+        for (int b = 0; b < B; ++b)
+            for (int g = 0; g < Hkv; ++g)
+                for (int p = 0; p < n_rows[b]; ++p) {
+                    const int pg = block_table[(long)b * max_pages + p / page];
+                    const double* src = cache + ((((long)l * B + b) * Hkv + g) * Pcap + p) * d;
+                    double* dst = pages + ((((long)l * num_pages + pg) * Hkv + g) * page + p % page) * d;
+                    for (int i = 0; i < d; ++i) dst[i] = src[i];
+                }
+    return DDTO_OK;
+}

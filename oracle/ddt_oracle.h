@@ -144,6 +144,21 @@ int ddto_commit(int La, int B, int N, int Hkv, int d, int Pcap,
                 const int32_t* acc_nodes, const int32_t* acc_len, int A,
                 int32_t* prefix_len, int32_t* src_row, int32_t* dst_pos, int32_t* status);
 
+/* Paged KV caches ([NOTES] "Where the next step is": attention over paged KV blocks).
+ * READING: the pages print no layout; a paged cache here is [L][num_pages][Hkv][page][d]
+ * and row p of request b's prefix is row p % page of physical page
+ * block_table[b][p / page].  ddto_gather_pages writes the contiguous cache
+ * [L][B][Hkv][Pcap][d] that ddto_tree_attn / ddto_commit take (rows >= prefix_len[b]
+ * zero); ddto_scatter_pages writes rows [0, n_rows[b]) of a contiguous cache back into
+ * the pages.  Both return DDTO_ERR_ARG for a block-table entry outside [0, num_pages)
+ * or a row past the capacity. */
+int ddto_gather_pages(int L, int B, int Hkv, int d, int page, int num_pages, int max_pages,
+                      const double* pages, const int32_t* block_table, const int32_t* prefix_len,
+                      int Pcap, double* cache);
+int ddto_scatter_pages(int L, int B, int Hkv, int d, int page, int num_pages, int max_pages,
+                       const double* cache, int Pcap, const int32_t* block_table,
+                       const int32_t* n_rows, double* pages);
+
 #ifdef __cplusplus
 }
 #endif

@@ -460,3 +460,59 @@ def test_commit_capacity_refused():
     out = oracle.commit(np.array([[0, 1, 2]]), [2], [3], k_tree=kt, v_tree=kt, k_cache=kc, v_cache=kc)
     assert out["status"][0] == 3 and out["prefix_len"][0] == 3
     np.testing.assert_array_equal(out["k_cache"], kc)
+
+
+# ------------------------------------------------------------------ paged KV layout
+def _pages_from_cache(cache, page, perm=None):
+    """Independent construction: cut each (layer, request, head) slab into pages of `page`
+    rows with numpy reshapes; page index of (b, i) is b * max_pages + i, optionally
+    relabelled by `perm`."""
+    L, B, Hkv, Pcap, d = cache.shape
+    mp = Pcap // page
+    pages = cache.reshape(L, B, Hkv, mp, page, d).transpose(0, 1, 3, 2, 4, 5).reshape(L, B * mp, Hkv, page, d)
+    table = np.arange(B * mp, dtype=np.int32).reshape(B, mp)
+    if perm is not None:
+        out = np.empty_like(pages)
+        out[:, perm] = pages          # logical page j is stored at physical page perm[j]
+        return out, perm[table].astype(np.int32)
+    return pages, table
+
+
+@pytest.mark.parametrize("page", [1, 4, 16])
+def test_gather_pages_identity_and_permuted(page):
+    rng = np.random.default_rng(11)
+    L, B, Hkv, Pcap, d = 2, 3, 2, 32, 5
+    cache = rng.standard_normal((L, B, Hkv, Pcap, d))
+    P = np.array([0, 17, 32], np.int32)
+    want = cache.copy()
+    for b in range(B):
+        want[:, b, :, P[b]:] = 0.0
+    pages, table = _pages_from_cache(cache, page)
+    assert np.array_equal(oracle.gather_pages(pages, table, P, Pcap), want)
+    perm = rng.permutation(pages.shape[1])
+    pages2, table2 = _pages_from_cache(cache, page, perm)
+    assert np.array_equal(oracle.gather_pages(pages2, table2, P, Pcap), want)
+
+
+def test_scatter_pages_inverts_gather_on_the_rows_written():
+    rng = np.random.default_rng(12)
+    L, B, Hkv, Pcap, d, page = 1, 2, 3, 24, 4, 8
+    cache = rng.standard_normal((L, B, Hkv, Pcap, d))
+    pages, table = _pages_from_cache(cache, page, rng.permutation(B * Pcap // page))
+    blank = np.full_like(pages, np.nan)
+    n = np.array([24, 9], np.int32)
+    back = oracle.scatter_pages(cache, table, n, blank)
+    got = oracle.gather_pages(np.nan_to_num(back, nan=0.0), table, n, Pcap)
+    want = cache.copy()
+    want[:, 1, :, 9:] = 0.0
+    assert np.array_equal(got, want)
+    # pages no row was written to stay untouched
+    assert np.isnan(back[:, table[1, 2]]).all()
+
+
+def test_gather_pages_rejects_bad_tables():
+    pages = np.zeros((1, 4, 1, 8, 2))
+    with pytest.raises(RuntimeError):
+        oracle.gather_pages(pages, np.array([[0, 9]], np.int32), [12], 16)   # page 9 does not exist
+    with pytest.raises(RuntimeError):
+        oracle.gather_pages(pages, np.array([[0, 1]], np.int32), [17], 17)   # past max_pages * page

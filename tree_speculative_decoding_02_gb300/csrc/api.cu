@@ -104,6 +104,40 @@ ddt_status ddt_tree_attn(int n_layers, int B, int N, int Hq, int Hkv, int d, int
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static bool page_rows_ok(int r) { return r >= 8 && r <= 4096 && (r >= 64 ? r % 64 == 0 : 64 % r == 0); }
+
+size_t ddt_tree_attn_paged_workspace(int n_layers, int B, int N, int Hq, int Hkv, int d, int page_size,
+                                     int max_pages) {
+    if (!page_rows_ok(page_size) || max_pages < 1) return 0;
+    return ddt_tree_attn_workspace(n_layers, B, N, Hq, Hkv, d, page_size * max_pages);
+}
+
+ddt_status ddt_tree_attn_paged(int n_layers, int B, int N, int Hq, int Hkv, int d, int page_size, int num_pages,
+                               int max_pages, ddt_dtype in_dtype, ddt_dtype out_dtype, const void* q,
+                               const void* k_tree, const void* v_tree, const void* k_pages, const void* v_pages,
+                               const int32_t* block_table, const int32_t* prefix_len, const int32_t* n_nodes,
+                               const uint32_t* anc, float scale, void* o, int32_t* status, void* workspace,
+                               size_t ws_bytes, ddt_stream_t stream) {
+    if (n_layers < 1 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || num_pages < 1 || max_pages < 1 ||
+        !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+        return DDT_ERR_INVALID_ARG;
+    if (!page_rows_ok(page_size) || (long)page_size * max_pages > (1L << 30)) return DDT_ERR_UNSUPPORTED;
+    if (N > kMaxRows || !attn_tc_supported(d, in_dtype)) return DDT_ERR_UNSUPPORTED;
+    if (!q || !k_tree || !v_tree || !k_pages || !v_pages || !block_table || !prefix_len || !n_nodes || !anc || !o ||
+        !status)
+        return DDT_ERR_INVALID_ARG;
+    const AttnPaging pg{page_size, num_pages, max_pages, block_table};
+    if (!workspace || ws_bytes < attn_tc_ws_bytes(n_layers, B, N, Hq, Hkv, d, page_size * max_pages) ||
+        !aligned16(workspace))
+        return DDT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(o) || !aligned16(k_pages) ||
+        !aligned16(v_pages))
+        return DDT_ERR_INVALID_ARG;
+    return from_cuda(launch_attn_tc_paged(n_layers, B, N, Hq, Hkv, d, pg, out_dtype, q, k_tree, v_tree, k_pages,
+                                          v_pages, prefix_len, n_nodes, anc, scale, o, status, workspace, ws_bytes,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------------------ GDN
 size_t ddt_tree_gdn_workspace(int n_layers, int B, int N, int Hk, int Hv, int dk, int dv) {
     (void)n_layers; (void)B; (void)N; (void)Hk; (void)Hv; (void)dk; (void)dv;
@@ -182,7 +216,35 @@ ddt_status ddt_commit(int B, int N, int A, int n_attn_layers, int Hkv, int d, in
     }
     return from_cuda(launch_commit(B, N, A, n_attn_layers, Hkv, d, Pcap, kv_dtype, k_tree, v_tree, k_cache, v_cache,
                                    n_gdn_layers, Hk, Hv, dk, dv, conv_k, x_dtype, x, conv_w, beta, decay, S,
-                                   conv_state, acc_nodes, acc_len, prefix_len, src_row, dst_pos, status,
+                                   conv_state, acc_nodes, acc_len, prefix_len, src_row, dst_pos, status, nullptr,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ddt_status ddt_commit_paged(int B, int N, int A, int n_attn_layers, int Hkv, int d, int page_size, int num_pages,
+                            int max_pages, const int32_t* block_table, ddt_dtype kv_dtype, const void* k_tree,
+                            const void* v_tree, void* k_pages, void* v_pages, int n_gdn_layers, int Hk, int Hv, int dk,
+                            int dv, int conv_k, ddt_dtype x_dtype, const void* x, const void* conv_w,
+                            const float* beta, const float* decay, float* S, void* conv_state,
+                            const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len, int32_t* src_row,
+                            int32_t* dst_pos, int32_t* status, ddt_stream_t stream) {
+    if (n_attn_layers < 1 || !block_table || num_pages < 1 || max_pages < 1) return DDT_ERR_INVALID_ARG;
+    if (!page_rows_ok(page_size) || (long)page_size * max_pages > (1L << 30)) return DDT_ERR_UNSUPPORTED;
+    if (B < 1 || N < 1 || A < 1 || n_gdn_layers < 0) return DDT_ERR_INVALID_ARG;
+    if (!acc_nodes || !acc_len || !prefix_len || !src_row || !dst_pos || !status) return DDT_ERR_INVALID_ARG;
+    if (Hkv < 1 || d < 1 || !dtype_ok(kv_dtype) || !k_tree || !v_tree || !k_pages || !v_pages)
+        return DDT_ERR_INVALID_ARG;
+    if (n_gdn_layers > 0) {
+        if (Hk < 1 || Hv < 1 || Hv % Hk != 0 || conv_k < 1 || conv_k > 8 || !dtype_ok(x_dtype) || !x || !conv_w ||
+            !beta || !decay || !S || (conv_k > 1 && !conv_state) || !aligned16(S))
+            return DDT_ERR_INVALID_ARG;
+        const bool dims = (dk == 32 && dv == 32) || (dk == 64 && dv == 64) || (dk == 128 && dv == 128) ||
+                          (dk == 64 && dv == 128) || (dk == 128 && dv == 64);
+        if (!dims) return DDT_ERR_UNSUPPORTED;
+    }
+    const AttnPaging pg{page_size, num_pages, max_pages, block_table};
+    return from_cuda(launch_commit(B, N, A, n_attn_layers, Hkv, d, page_size * max_pages, kv_dtype, k_tree, v_tree,
+                                   k_pages, v_pages, n_gdn_layers, Hk, Hv, dk, dv, conv_k, x_dtype, x, conv_w, beta,
+                                   decay, S, conv_state, acc_nodes, acc_len, prefix_len, src_row, dst_pos, status, &pg,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 

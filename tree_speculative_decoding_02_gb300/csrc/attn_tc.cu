@@ -47,6 +47,10 @@ constexpr float kTau = 8.f;  // rescale O only when the row max grows by more th
 
 struct TcParams {
     int L, B, N, Hq, Hkv, G, MT, S, chunk, Pcap, W;
+    // paged prefix caches: page_rows positions a page, block_table [B][max_pages] of
+    // physical pages out of num_pages (paged == 0: one contiguous slab per request)
+    int paged, page_rows, num_pages, max_pages;
+    const int32_t* block_table;
     const __nv_bfloat16* q;
     const int32_t* prefix_len;
     const int32_t* n_nodes;
@@ -84,6 +88,9 @@ struct Tile {
     int lo;    // prefix tiles: keys below lo were handled by the previous tile
 };
 
+// ragged: the chunk's last prefix tile is partial.  Contiguous caches shift it to end at
+// the chunk's end (no row past the prefix is read); paged caches keep it aligned (a
+// shifted tile could straddle pages) and mask the rows past the end instead.
 __device__ __forceinline__ Tile tile_of(int j, int n_pre, int c0, int c1, bool ragged) {
     Tile t;
     if (j < n_pre) {
@@ -167,12 +174,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = p.perm[blockIdx.y];
     const long lb = (long)l * p.B + b;
     const int P = p.prefix_len[b], nn = p.n_nodes[b];
-    const bool bad = P < 0 || P > p.Pcap || nn < 1 || nn > p.N;
+    bool bad = P < 0 || P > p.Pcap || nn < 1 || nn > p.N;
+    int bad_table = 0;
+    if (p.paged && !bad) {  // every page the prefix uses must exist
+        const int np = (P + p.page_rows - 1) / p.page_rows;
+        for (int i = tid; i < np; i += kThreads) {
+            const int pg = p.block_table[(long)b * p.max_pages + i];
+            bad_table |= (pg < 0 || pg >= p.num_pages);
+        }
+    }
+    bad_table = __syncthreads_or(bad_table);
+    bad = bad || bad_table;
     const long prow0 = ((((long)s * p.L + l) * p.B + b) * p.Hkv + g) * (long)(p.MT * kBM) + mt * kBM;
 
     if (bad) {
         if (tid == 0 && s == 0 && mt == 0 && g == 0 && l == 0)
-            p.status[b] = (P < 0 || P > p.Pcap) ? DDT_ERR_CAPACITY : DDT_ERR_TREE;
+            p.status[b] = (P < 0 || P > p.Pcap) ? DDT_ERR_CAPACITY : (bad_table ? DDT_ERR_INVALID_ARG : DDT_ERR_TREE);
         if (p.S == 1) {
             for (int e = tid; e < kBM * D; e += kThreads) {
                 const int R = mt * kBM + e / D;
@@ -195,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n_tree = (s == s_last) ? (nn + kBN - 1) / kBN : 0;
     const int T = n_pre + n_tree;
-    const bool ragged = ((c1 - c0) % kBN) != 0;
+    const bool ragged = !p.paged && ((c1 - c0) % kBN) != 0;
     if (T == 0) {  // an empty split (only when S > 1)
         if (tid < kBM) p.part_ml[prow0 + tid] = make_float2(-INFINITY, 0.f);
         return;
@@ -279,13 +296,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::mbar_expect_tx(full + st, Cfg::kStageBytes);
                     unsigned char* dst = sRing + st * Cfg::kStageBytes;
+                    if (!t.tree && p.paged) {
+                        // one box per page slice of the tile (pages of fewer than 64 rows);
+                        // rows past the prefix come from its last page and are masked
+                        const int sub = min(kBN, p.page_rows), last = (P - 1) / p.page_rows;
+                        for (int r0 = 0; r0 < kBN; r0 += sub) {
+                            const int pos = t.y + r0;
+                            const int lp = min(pos / p.page_rows, last);
+                            const int phys = p.block_table[(long)b * p.max_pages + lp];
+                            const int plane = (int)(((long)l * p.num_pages + phys) * p.Hkv + g);
 #pragma unroll
-                    for (int blk = 0; blk < Cfg::kBlocks; ++blk) {
-                        if (!t.tree)
-                            tc::tma_load_3d(dst + blk * (kBN * 128), kv ? &tm_vc : &tm_kc, full + st, blk * 64, t.y, grp);
-                        else
-                            tc::tma_load_4d(dst + blk * (kBN * 128), kv ? &tm_vt : &tm_kt, full + st, blk * 64, g, t.y,
-                                            (int)lb);
+                            for (int blk = 0; blk < Cfg::kBlocks; ++blk)
+                                tc::tma_load_3d(dst + blk * (kBN * 128) + r0 * 128, kv ? &tm_vc : &tm_kc, full + st,
+                                                blk * 64, pos % p.page_rows, plane);
+                        }
+                    } else {
+#pragma unroll
+                        for (int blk = 0; blk < Cfg::kBlocks; ++blk) {
+                            if (!t.tree)
+                                tc::tma_load_3d(dst + blk * (kBN * 128), kv ? &tm_vc : &tm_kc, full + st, blk * 64, t.y,
+                                                grp);
+                            else
+                                tc::tma_load_4d(dst + blk * (kBN * 128), kv ? &tm_vt : &tm_kt, full + st, blk * 64, g,
+                                                t.y, (int)lb);
+                        }
                     }
                     issued = u + 1;
                 }
@@ -379,7 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t vis;
                 if (!t.tree) {
                     const int skip = t.lo - t.y - 32 * hf;  // keys of this half already seen
+                    const int lim = c1 - t.y - 32 * hf;     // keys of this half before the chunk's end
                     vis = skip <= 0 ? ~0u : (skip >= 32 ? 0u : (~0u << skip));
+                    vis &= lim >= 32 ? ~0u : (lim <= 0 ? 0u : ((1u << lim) - 1u));
                 } else {
                     const int w = (t.y >> 5) + hf;
                     vis = (live && w < p.W) ? anc_row[w] : 0u;
@@ -429,11 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 plo[c >> 1] = pack_bf16(a - __low2float(hi), bb - __high2float(hi));
             }
             l_run += sum;
-            if (t.tree) {
-                // V rows of padding nodes may hold anything: zero them before the MMA reads
+            if (t.tree || t.y + kBN > c1) {
+                // V rows of padding nodes (or, paged, rows past the prefix) may hold anything,
+                // even NaN: zero them before the MMA reads them (a zero P does not cancel NaN)
                 const int u = 2 * j + 1, st = u % kStages;
                 ok = __all_sync(kFull, tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag));
-                const int first = max(0, nn - t.y);
+                const int first = t.tree ? max(0, nn - t.y) : c1 - t.y;
                 if (ok && first < kBN) {
                     unsigned char* vst = sRing + st * Cfg::kStageBytes;
                     const int per_blk = (kBN - first) * 8;
@@ -613,10 +650,13 @@ static cudaError_t attn_tc_go(const TcParams& prm, const CUtensorMap* maps, cuda
     return e;
 }
 
-cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out, const void* q,
-                           const void* k_tree, const void* v_tree, const void* k_cache, const void* v_cache,
-                           const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
-                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st) {
+// pg == nullptr: contiguous caches [L][B][Hkv][Pcap][d]; else paged caches
+// [L][num_pages][Hkv][page_rows][d] with Pcap = max_pages * page_rows.
+static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out,
+                                  const void* q, const void* k_tree, const void* v_tree, const void* k_cache,
+                                  const void* v_cache, const AttnPaging* pg, const int32_t* prefix_len,
+                                  const int32_t* n_nodes, const uint32_t* anc, float scale, void* o, int32_t* status,
+                                  void* ws, size_t ws_bytes, cudaStream_t st) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     TcParams prm;
@@ -645,13 +685,21 @@ cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap
     prm.o = o;
     prm.status = status;
     prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.paged = pg != nullptr;
+    prm.page_rows = pg ? pg->page_rows : 0;
+    prm.num_pages = pg ? pg->num_pages : 0;
+    prm.max_pages = pg ? pg->max_pages : 0;
+    prm.block_table = pg ? pg->block_table : nullptr;
 
     // tensor maps: caches (d, position, layer*B*Hkv), tree rows (d, kv head, node, layer*B)
     CUtensorMap maps[4];
-    const cuuint32_t box3[3] = {64, (cuuint32_t)kBN, 1};
+    // (paged: the plane is (layer, physical page, kv head) and a box spans at most a page)
+    const int rows3 = pg ? pg->page_rows : (Pcap > 0 ? Pcap : 1);
+    const cuuint32_t box3[3] = {64, (cuuint32_t)(pg ? (pg->page_rows < kBN ? pg->page_rows : kBN) : kBN), 1};
     const cuuint32_t es3[3] = {1, 1, 1};
-    const cuuint64_t dims3[3] = {(cuuint64_t)d, (cuuint64_t)(Pcap > 0 ? Pcap : 1), (cuuint64_t)L * B * Hkv};
-    const cuuint64_t str3[2] = {(cuuint64_t)d * 2, (cuuint64_t)(Pcap > 0 ? Pcap : 1) * d * 2};
+    const cuuint64_t dims3[3] = {(cuuint64_t)d, (cuuint64_t)rows3,
+                                 (cuuint64_t)L * (pg ? (long)pg->num_pages : (long)B) * Hkv};
+    const cuuint64_t str3[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows3 * d * 2};
     const cuuint32_t box4[4] = {64, 1, (cuuint32_t)kBN, 1};
     const cuuint32_t es4[4] = {1, 1, 1, 1};
     const cuuint64_t dims4[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)N, (cuuint64_t)L * B};
@@ -687,6 +735,23 @@ cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap
         case 256: return bf ? attn_tc_go<256, __nv_bfloat16>(prm, maps, st) : attn_tc_go<256, float>(prm, maps, st);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out, const void* q,
+                           const void* k_tree, const void* v_tree, const void* k_cache, const void* v_cache,
+                           const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
+                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st) {
+    return attn_tc_launch(L, B, N, Hq, Hkv, d, Pcap, out, q, k_tree, v_tree, k_cache, v_cache, nullptr, prefix_len,
+                          n_nodes, anc, scale, o, status, ws, ws_bytes, st);
+}
+
+cudaError_t launch_attn_tc_paged(int L, int B, int N, int Hq, int Hkv, int d, const AttnPaging& pg, ddt_dtype out,
+                                 const void* q, const void* k_tree, const void* v_tree, const void* k_pages,
+                                 const void* v_pages, const int32_t* prefix_len, const int32_t* n_nodes,
+                                 const uint32_t* anc, float scale, void* o, int32_t* status, void* ws,
+                                 size_t ws_bytes, cudaStream_t st) {
+    return attn_tc_launch(L, B, N, Hq, Hkv, d, pg.max_pages * pg.page_rows, out, q, k_tree, v_tree, k_pages, v_pages,
+                          &pg, prefix_len, n_nodes, anc, scale, o, status, ws, ws_bytes, st);
 }
 
 }  // namespace ddt

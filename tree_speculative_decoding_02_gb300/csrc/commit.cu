@@ -23,10 +23,18 @@
 
 namespace ddt {
 
-// A request's commit is valid when its accepted path is well formed and fits.
+// Paged caches: position p of request b is row p % page_rows of physical page
+// bt[b][p / page_rows] (bt == nullptr: contiguous caches).
+struct KvPages {
+    const int32_t* bt;
+    int page_rows, num_pages, max_pages;
+};
+
+// A request's commit is valid when its accepted path is well formed and fits (and, paged,
+// every page it writes exists).  Every commit kernel evaluates the same check.
 __device__ __forceinline__ int commit_check(int b, int N, int A, int cap_check, int Pcap,
                                             const int32_t* acc_nodes, const int32_t* acc_len,
-                                            const int32_t* prefix_len) {
+                                            const int32_t* prefix_len, const KvPages& pg) {
     const int a = acc_len[b];
     if (a < 0 || a + 1 > A) return DDT_ERR_INVALID_ARG;
     for (int j = 0; j <= a; ++j) {
@@ -34,6 +42,11 @@ __device__ __forceinline__ int commit_check(int b, int N, int A, int cap_check, 
         if (r < 0 || r >= N) return DDT_ERR_TREE;
     }
     if (cap_check && (prefix_len[b] < 0 || prefix_len[b] + a + 1 > Pcap)) return DDT_ERR_CAPACITY;
+    if (cap_check && pg.bt)
+        for (int j = 0; j <= a; ++j) {
+            const int phys = pg.bt[(long)b * pg.max_pages + (prefix_len[b] + j) / pg.page_rows];
+            if (phys < 0 || phys >= pg.num_pages) return DDT_ERR_INVALID_ARG;
+        }
     return DDT_OK;
 }
 
@@ -41,17 +54,24 @@ template <typename T>
 __global__ void k_commit_kv(int B, int N, int A, int Hkv, int d, int Pcap, int vec, const T* __restrict__ k_tree,
                             const T* __restrict__ v_tree, T* __restrict__ k_cache, T* __restrict__ v_cache,
                             const int32_t* __restrict__ acc_nodes, const int32_t* __restrict__ acc_len,
-                            const int32_t* __restrict__ prefix_len) {
+                            const int32_t* __restrict__ prefix_len, const KvPages pg) {
     const int j = blockIdx.x, lg = blockIdx.y, b = blockIdx.z;
     const int l = lg / Hkv, g = lg % Hkv;
     __shared__ int s_ok;
-    if (threadIdx.x == 0) s_ok = commit_check(b, N, A, 1, Pcap, acc_nodes, acc_len, prefix_len) == DDT_OK;
+    if (threadIdx.x == 0) s_ok = commit_check(b, N, A, 1, Pcap, acc_nodes, acc_len, prefix_len, pg) == DDT_OK;
     __syncthreads();
     if (!s_ok || j > acc_len[b]) return;
     const int src = acc_nodes[(long)b * A + j];
     const long lb = (long)l * B + b;
     const long so = ((lb * N + src) * Hkv + g) * (long)d;
-    const long dof = ((lb * Hkv + g) * (long)Pcap + prefix_len[b] + j) * d;
+    const int pos = prefix_len[b] + j;
+    long dof;
+    if (pg.bt) {
+        const long phys = pg.bt[(long)b * pg.max_pages + pos / pg.page_rows];
+        dof = ((((long)l * pg.num_pages + phys) * Hkv + g) * pg.page_rows + pos % pg.page_rows) * d;
+    } else {
+        dof = ((lb * Hkv + g) * (long)Pcap + pos) * d;
+    }
     if (vec) {
         const int nv = d * (int)sizeof(T) / 16;
         for (int e = threadIdx.x; e < nv; e += blockDim.x) {
@@ -82,7 +102,7 @@ __global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, i
                                                        const float* __restrict__ decay, float* __restrict__ S,
                                                        const int32_t* __restrict__ acc_nodes,
                                                        const int32_t* __restrict__ acc_len,
-                                                       const int32_t* __restrict__ prefix_len) {
+                                                       const int32_t* __restrict__ prefix_len, const KvPages pg) {
     constexpr int kT = 2 * DV, kH = DK / 2;
     extern __shared__ __align__(16) float sm[];
     float* s_k = sm;                 // [A][DK]  normalised k of each accepted node
@@ -91,7 +111,7 @@ __global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, i
     __shared__ int s_ok;
     const int h = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) s_ok = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len) == DDT_OK;
+    if (tid == 0) s_ok = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len, pg) == DDT_OK;
     __syncthreads();
     if (!s_ok) return;
     const int a = acc_len[b];
@@ -188,10 +208,11 @@ __global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, i
 template <typename Tx>
 __global__ void k_commit_conv(int B, int N, int A, int C, int K, int cap_check, int Pcap, const Tx* __restrict__ x,
                               Tx* __restrict__ conv_state, const int32_t* __restrict__ acc_nodes,
-                              const int32_t* __restrict__ acc_len, const int32_t* __restrict__ prefix_len) {
+                              const int32_t* __restrict__ acc_len, const int32_t* __restrict__ prefix_len,
+                              const KvPages pg) {
     const int l = blockIdx.x, b = blockIdx.y;
     __shared__ int s_ok;
-    if (threadIdx.x == 0) s_ok = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len) == DDT_OK;
+    if (threadIdx.x == 0) s_ok = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len, pg) == DDT_OK;
     __syncthreads();
     if (!s_ok) return;
     const int n = acc_len[b] + 1;
@@ -211,10 +232,10 @@ __global__ void k_commit_conv(int B, int N, int A, int C, int K, int cap_check, 
 __global__ void k_commit_final(int B, int N, int A, int cap_check, int Pcap, const int32_t* __restrict__ acc_nodes,
                                const int32_t* __restrict__ acc_len, int32_t* __restrict__ prefix_len,
                                int32_t* __restrict__ src_row, int32_t* __restrict__ dst_pos,
-                               int32_t* __restrict__ status) {
+                               int32_t* __restrict__ status, const KvPages pg) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
-    const int st = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len);
+    const int st = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len, pg);
     const int P = prefix_len[b];
     const int a = acc_len[b];
     for (int j = 0; j < A; ++j) {
@@ -230,14 +251,14 @@ template <typename Tx, int DK, int DV>
 static cudaError_t commit_gdn_go(int B, int N, int A, int Lg, int Hk, int Hv, int K, int cap, int Pcap,
                                  const void* x, const void* w, const void* cs, const float* beta,
                                  const float* decay, float* S, const int32_t* an, const int32_t* al,
-                                 const int32_t* pl, cudaStream_t st) {
+                                 const int32_t* pl, const KvPages& pg, cudaStream_t st) {
     const size_t smem = sizeof(float) * (size_t)A * (DK + DV + 2);
     cudaError_t e = cudaFuncSetAttribute(k_commit_gdn<Tx, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     k_commit_gdn<Tx, DK, DV><<<counted(dim3(Hv, B, Lg)), 2 * DV, smem, st>>>(
         B, N, A, Hk, Hv, K, cap, Pcap, static_cast<const Tx*>(x), static_cast<const Tx*>(w),
-        static_cast<const Tx*>(cs), beta, decay, S, an, al, pl);
+        static_cast<const Tx*>(cs), beta, decay, S, an, al, pl, pg);
     return cudaGetLastError();
 }
 
@@ -245,10 +266,11 @@ template <typename Tx>
 static cudaError_t commit_gdn_dims(int dk, int dv, int B, int N, int A, int Lg, int Hk, int Hv, int K, int cap,
                                    int Pcap, const void* x, const void* w, const void* cs, const float* beta,
                                    const float* decay, float* S, const int32_t* an, const int32_t* al,
-                                   const int32_t* pl, cudaStream_t st) {
+                                   const int32_t* pl, const KvPages& pg, cudaStream_t st) {
 #define DDT_CG_CASE(P, Q)                                                                                        \
     if (dk == P && dv == Q)                                                                                      \
-        return commit_gdn_go<Tx, P, Q>(B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, w, cs, beta, decay, S, an, al, pl, st);
+        return commit_gdn_go<Tx, P, Q>(B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, w, cs, beta, decay, S, an, al, pl, pg, \
+                                       st);
     DDT_CG_CASE(32, 32)
     DDT_CG_CASE(64, 64)
     DDT_CG_CASE(128, 128)
@@ -263,9 +285,11 @@ cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap,
                           int Hv, int dk, int dv, int K, ddt_dtype x_dtype, const void* x, const void* conv_w,
                           const float* beta, const float* decay, float* S, void* conv_state,
                           const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len, int32_t* src_row,
-                          int32_t* dst_pos, int32_t* status, cudaStream_t st) {
+                          int32_t* dst_pos, int32_t* status, const AttnPaging* paging, cudaStream_t st) {
     cudaError_t e;
     const int cap = La > 0;
+    const KvPages pg = paging ? KvPages{paging->block_table, paging->page_rows, paging->num_pages, paging->max_pages}
+                              : KvPages{nullptr, 0, 0, 0};
     if (La > 0) {
         const size_t es = kv_dtype == DDT_BF16 ? 2 : 4;
         const int vec = ((d * es) % 16 == 0) && (reinterpret_cast<uintptr_t>(k_tree) % 16 == 0) &&
@@ -277,36 +301,36 @@ cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap,
             k_commit_kv<__nv_bfloat16><<<counted(grid), 64, 0, st>>>(
                 B, N, A, Hkv, d, Pcap, vec, static_cast<const __nv_bfloat16*>(k_tree),
                 static_cast<const __nv_bfloat16*>(v_tree), static_cast<__nv_bfloat16*>(k_cache),
-                static_cast<__nv_bfloat16*>(v_cache), acc_nodes, acc_len, prefix_len);
+                static_cast<__nv_bfloat16*>(v_cache), acc_nodes, acc_len, prefix_len, pg);
         else
             k_commit_kv<float><<<counted(grid), 64, 0, st>>>(B, N, A, Hkv, d, Pcap, vec, static_cast<const float*>(k_tree),
                                                     static_cast<const float*>(v_tree), static_cast<float*>(k_cache),
-                                                    static_cast<float*>(v_cache), acc_nodes, acc_len, prefix_len);
+                                                    static_cast<float*>(v_cache), acc_nodes, acc_len, prefix_len, pg);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (Lg > 0) {
         const int C = 2 * Hk * dk + Hv * dv;
         if (x_dtype == DDT_BF16) {
             e = commit_gdn_dims<__nv_bfloat16>(dk, dv, B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, conv_w, conv_state, beta,
-                                               decay, S, acc_nodes, acc_len, prefix_len, st);
+                                               decay, S, acc_nodes, acc_len, prefix_len, pg, st);
             if (e != cudaSuccess) return e;
             if (K > 1)
                 k_commit_conv<__nv_bfloat16><<<counted(dim3(Lg, B)), 256, 0, st>>>(
                     B, N, A, C, K, cap, Pcap, static_cast<const __nv_bfloat16*>(x),
-                    static_cast<__nv_bfloat16*>(conv_state), acc_nodes, acc_len, prefix_len);
+                    static_cast<__nv_bfloat16*>(conv_state), acc_nodes, acc_len, prefix_len, pg);
         } else {
             e = commit_gdn_dims<float>(dk, dv, B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, conv_w, conv_state, beta, decay,
-                                       S, acc_nodes, acc_len, prefix_len, st);
+                                       S, acc_nodes, acc_len, prefix_len, pg, st);
             if (e != cudaSuccess) return e;
             if (K > 1)
                 k_commit_conv<float><<<counted(dim3(Lg, B)), 256, 0, st>>>(B, N, A, C, K, cap, Pcap, static_cast<const float*>(x),
                                                                   static_cast<float*>(conv_state), acc_nodes, acc_len,
-                                                                  prefix_len);
+                                                                  prefix_len, pg);
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     k_commit_final<<<counted((B + 127) / 128), 128, 0, st>>>(B, N, A, cap, Pcap, acc_nodes, acc_len, prefix_len, src_row,
-                                                    dst_pos, status);
+                                                    dst_pos, status, pg);
     return cudaGetLastError();
 }
 

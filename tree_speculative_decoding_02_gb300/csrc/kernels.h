@@ -44,6 +44,16 @@ cudaError_t launch_attn_simt(int L, int B, int N, int Hq, int Hkv, int d, int Pc
                              const void* v_cache, const int32_t* prefix_len, const int32_t* n_nodes,
                              const uint32_t* anc, float scale, void* o, int32_t* status, cudaStream_t st);
 
+// paged prefix caches: positions p of request b live in page block_table[b][p / page_rows]
+struct AttnPaging {
+    int page_rows, num_pages, max_pages;
+    const int32_t* block_table;  // [B][max_pages]
+};
+cudaError_t launch_attn_tc_paged(int L, int B, int N, int Hq, int Hkv, int d, const AttnPaging& pg, ddt_dtype out,
+                                 const void* q, const void* k_tree, const void* v_tree, const void* k_pages,
+                                 const void* v_pages, const int32_t* prefix_len, const int32_t* n_nodes,
+                                 const uint32_t* anc, float scale, void* o, int32_t* status, void* ws,
+                                 size_t ws_bytes, cudaStream_t st);
 size_t attn_tc_ws_bytes(int L, int B, int N, int Hq, int Hkv, int d, int Pcap);
 bool attn_tc_supported(int d, ddt_dtype in);
 cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out, const void* q,
@@ -67,6 +77,6 @@ cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap,
                           int Hv, int dk, int dv, int K, ddt_dtype x_dtype, const void* x, const void* conv_w,
                           const float* beta, const float* decay, float* S, void* conv_state,
                           const int32_t* acc_nodes, const int32_t* acc_len, int32_t* prefix_len, int32_t* src_row,
-                          int32_t* dst_pos, int32_t* status, cudaStream_t st);
+                          int32_t* dst_pos, int32_t* status, const AttnPaging* paging, cudaStream_t st);
 
 }  // namespace ddt

@@ -42,6 +42,10 @@ _SIGS = {
     "ddt_tree_gdn": ([_c_int] * 10 + [_c_p] * 10 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_walk_accept_workspace": ([_c_int] * 3, _c_size),
     "ddt_walk_accept": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_tree_attn_paged_workspace": ([_c_int] * 8, _c_size),
+    "ddt_tree_attn_paged": ([_c_int] * 11 + [_c_p] * 9 + [_c_float, _c_p, _c_p, _c_p, _c_size, _c_p], _c_int),
+    "ddt_commit_paged": ([_c_int] * 9 + [_c_p] + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13,
+                         _c_int),
     "ddt_commit": ([_c_int] * 7 + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13, _c_int),
 }
 EXPORTS = tuple(_SIGS)
@@ -204,6 +208,40 @@ def ddt_tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc,
     return {"o": o, "status": st}
 
 
+def ddt_tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, prefix_len, n_nodes, anc, *,
+                        scale=None, out_dtype=None, out=None, status=None, workspace=None):
+    """q [L][B][N][Hq][d]; k/v_tree [L][B][N][Hkv][d]; k/v_pages [L][num_pages][Hkv][page_size][d] (bf16);
+    block_table [B][max_pages] int32."""
+    lib = _gpu()
+    L, B, N, Hq, d = q.shape
+    Hkv = k_tree.shape[3]
+    num_pages, page = k_pages.shape[1], k_pages.shape[3]
+    max_pages = block_table.shape[1]
+    dt = q.dtype
+    _need(q, (L, B, N, Hq, d), dt, "q")
+    _need(k_tree, (L, B, N, Hkv, d), dt, "k_tree")
+    _need(v_tree, (L, B, N, Hkv, d), dt, "v_tree")
+    _need(k_pages, (L, num_pages, Hkv, page, d), dt, "k_pages")
+    _need(v_pages, (L, num_pages, Hkv, page, d), dt, "v_pages")
+    _need(block_table, (B, max_pages), torch.int32, "block_table")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    _need(anc, (B, N, (N + 31) // 32), None, "anc")
+    out_dtype = out_dtype or dt
+    o = out if out is not None else torch.empty((L, B, N, Hq, d), dtype=out_dtype, device=q.device)
+    _need(o, (L, B, N, Hq, d), out_dtype, "o")
+    st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=q.device)
+    scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    need = lib.ddt_tree_attn_paged_workspace(L, B, N, Hq, Hkv, d, page, max_pages)
+    ws = workspace if workspace is not None else _ws(need, q.device)
+    rc = lib.ddt_tree_attn_paged(L, B, N, Hq, Hkv, d, page, num_pages, max_pages, _DT[dt], _DT[out_dtype], _ptr(q),
+                                 _ptr(k_tree), _ptr(v_tree), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                 _ptr(prefix_len), _ptr(n_nodes), _ptr(anc), scale, _ptr(o), _ptr(st), _ptr(ws),
+                                 ws.numel(), _stream())
+    _check(rc, "ddt_tree_attn_paged")
+    return {"o": o, "status": st}
+
+
 # ----------------------------------------------------------------------------- GDN
 def ddt_tree_gdn(x, conv_w, conv_state, beta, decay, S, parent, n_nodes, *, Hk: int, out_dtype=None, out=None,
                  status=None, workspace=None):
@@ -326,4 +364,52 @@ def ddt_commit(acc_nodes, acc_len, prefix_len, *, k_tree=None, v_tree=None, k_ca
                         _ptr(conv_state), _ptr(acc_nodes), _ptr(acc_len), _ptr(prefix_len), _ptr(res["src_row"]),
                         _ptr(res["dst_pos"]), _ptr(res["status"]), _stream())
     _check(rc, "ddt_commit")
+    return res
+
+
+def ddt_commit_paged(acc_nodes, acc_len, prefix_len, block_table, *, k_tree, v_tree, k_pages, v_pages, x=None,
+                     conv_w=None, beta=None, decay=None, S=None, conv_state=None, Hk: int = 1, out=None):
+    """ddt_commit with the KV part written through a block table into k/v_pages
+    [L][num_pages][Hkv][page_size][d]."""
+    lib = _gpu()
+    B, A = acc_nodes.shape
+    dev = acc_nodes.device
+    _need(acc_nodes, (B, A), torch.int32, "acc_nodes")
+    _need(acc_len, (B,), torch.int32, "acc_len")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    La, _, N, Hkv, d = k_tree.shape
+    num_pages, page = k_pages.shape[1], k_pages.shape[3]
+    max_pages = block_table.shape[1]
+    kdt = k_tree.dtype
+    _need(k_tree, (La, B, N, Hkv, d), kdt, "k_tree")
+    _need(v_tree, (La, B, N, Hkv, d), kdt, "v_tree")
+    _need(k_pages, (La, num_pages, Hkv, page, d), kdt, "k_pages")
+    _need(v_pages, (La, num_pages, Hkv, page, d), kdt, "v_pages")
+    _need(block_table, (B, max_pages), torch.int32, "block_table")
+    if S is not None:
+        Lg, _, N2, C = x.shape
+        if N2 != N:
+            raise DDTError("tree rows differ between the attention and GDN parts")
+        Hv, dv, dk = S.shape[2], S.shape[3], S.shape[4]
+        K = conv_w.shape[2]
+        _need(x, (Lg, B, N, C), x.dtype, "x")
+        _need(conv_w, (Lg, C, K), x.dtype, "conv_w")
+        _need(conv_state, (Lg, B, K - 1, C), x.dtype, "conv_state")
+        _need(beta, (Lg, B, N, Hv), torch.float32, "beta")
+        _need(decay, (Lg, B, N, Hv), torch.float32, "decay")
+        _need(S, (Lg, B, Hv, dv, dk), torch.float32, "S")
+        xd = _DT[x.dtype]
+    else:
+        Lg, Hv, dk, dv, K, xd = 0, 1, 1, 1, 1, F32
+    o = out or {}
+    i32 = dict(dtype=torch.int32, device=dev)
+    res = {"src_row": o.get("src_row", torch.empty((B, A), **i32)),
+           "dst_pos": o.get("dst_pos", torch.empty((B, A), **i32)),
+           "status": o.get("status", torch.empty((B,), **i32))}
+    rc = lib.ddt_commit_paged(B, N, A, La, Hkv, d, page, num_pages, max_pages, _ptr(block_table), _DT[kdt],
+                              _ptr(k_tree), _ptr(v_tree), _ptr(k_pages), _ptr(v_pages), Lg, Hk, Hv, dk, dv, K, xd,
+                              _ptr(x), _ptr(conv_w), _ptr(beta), _ptr(decay), _ptr(S), _ptr(conv_state),
+                              _ptr(acc_nodes), _ptr(acc_len), _ptr(prefix_len), _ptr(res["src_row"]),
+                              _ptr(res["dst_pos"]), _ptr(res["status"]), _stream())
+    _check(rc, "ddt_commit_paged")
     return res
