@@ -220,6 +220,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     ddt.load()
     cfg = dict(synth.WORKLOADS[args.workload])
+    if args.kv_page:
+        cfg["page"] = args.kv_page
     r = Round(cfg, device=dev, workload=args.workload)
     st = torch.cuda.current_stream()
     ev = {k: [] for k in KERNELS}
@@ -237,7 +239,12 @@ def run_ours(args, rank, world, local):
         if timed:
             marks[1].record(st)
         kw = {}
-        if r.Lf:
+        if r.Lf and r.page:
+            a = r.attn
+            ddt.ddt_tree_attn_paged(a.q, a.k_tree, a.v_tree, r.k_pages, r.v_pages, r.block_table, r.prefix_len,
+                                    r.tree["n_nodes"], r.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out=r.attn_o,
+                                    status=r.attn_status, workspace=r.attn_ws)
+        elif r.Lf:
             a = r.attn
             ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, r.prefix_len, r.tree["n_nodes"],
                               r.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out=r.attn_o, status=r.attn_status,
@@ -257,7 +264,12 @@ def run_ours(args, rank, world, local):
                             target_logits=r.target_logits, out=r.walk, workspace=r.walk_ws)
         if timed:
             marks[4].record(st)
-        ddt.ddt_commit(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, out=r.commit, **kw)
+        if r.Lf and r.page:
+            ddt.ddt_commit_paged(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, r.block_table,
+                                 k_tree=r.attn.k_tree, v_tree=r.attn.v_tree, k_pages=r.k_pages, v_pages=r.v_pages,
+                                 out=r.commit, **kw)
+        else:
+            ddt.ddt_commit(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, out=r.commit, **kw)
         if timed:
             marks[5].record(st)
             for i, k in enumerate(KERNELS):
@@ -378,7 +390,10 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg:
+    if args.kv_page:
+        out["config"]["kv"] = f"paged: {args.kv_page} rows a page, shuffled block table"
+        out["roofline"]["traffic"] = None   # the recorded capture is of the contiguous layout
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg and not args.kv_page:
         out["cpu_baseline"] = cpu_baseline(r, seconds=args.cpu_seconds)
     return out
 
@@ -531,6 +546,8 @@ def main():
     ap.add_argument("--workload", type=int, default=WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-page", type=int, default=0,
+                    help="paged prefix caches with this many rows a page (0: contiguous)")
     args = ap.parse_args()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

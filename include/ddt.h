@@ -188,6 +188,25 @@ ddt_status ddt_tree_attn_paged(int n_layers, int B, int N, int Hq, int Hkv, int 
                                void* workspace, size_t ws_bytes, ddt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * ddt_rope_tree -- [NOTES] "Where the next step is": position and RoPE correctness by
+ * branch depth.  Rotary embedding of the tree rows, in place, at each node's own position
+ * (position[b][n] from ddt_build_tree: prefix_len + depth, shared by siblings).
+ *
+ * For every layer, request b, node n < n_nodes[b], and every head row x of q
+ * [L][B][N][Hq][d] and of k_tree [L][B][N][Hkv][d] (dtype):
+ *   for i < rot_dim/2, with a = position[b][n] * theta^(-2i/rot_dim):
+ *     x[i] <- x[i] cos a - x[i + rot_dim/2] sin a,
+ *     x[i + rot_dim/2] <- x[i + rot_dim/2] cos a + x[i] sin a;   channels >= rot_dim kept.
+ * READING: the pages give no rotary formula; this is the half-split convention of
+ * Qwen-style models, with partial rotation (rot_dim < d) allowed.  Rows of padding
+ * nodes are left unchanged.  Call it before ddt_tree_attn / ddt_commit so that the
+ * committed keys are the rotated ones.  rot_dim even, 2 <= rot_dim <= d; theta > 1.
+ * ------------------------------------------------------------------------------- */
+ddt_status ddt_rope_tree(int n_layers, int B, int N, int Hq, int Hkv, int d, int rot_dim,
+                         double theta, ddt_dtype dtype, const int32_t* position,
+                         const int32_t* n_nodes, void* q, void* k_tree, ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * ddt_tree_gdn -- [NOTES] "Why hybrid attention makes it hard" / "Where the next step
  * is": each node reads the GDN and conv state of its parent and writes scratch, never
  * the committed state; [GDN] the gated delta rule.

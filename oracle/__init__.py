@@ -47,7 +47,7 @@ def _load():
             lib = ctypes.CDLL(build())
             for name in ("ddto_build_tree", "ddto_attn_row", "ddto_tree_attn", "ddto_gdn_unit",
                          "ddto_tree_gdn", "ddto_walk", "ddto_commit", "ddto_gather_pages",
-                         "ddto_scatter_pages"):
+                         "ddto_scatter_pages", "ddto_rope_tree"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -153,6 +153,17 @@ def scatter_pages(cache, block_table, n_rows, pages):
                                 _p(out))
     _check(rc, "scatter_pages")
     return out
+
+
+def rope_tree(x, position, n_nodes, rot: int, theta: float = 10000.0):
+    """Rotary embedding of x [L][B][N][H][d] at position [B][N] (a copy is returned)."""
+    lib = _load()
+    x = _f64(x).copy()
+    L, B, N, H, d = x.shape
+    rc = lib.ddto_rope_tree(L, B, N, H, d, int(rot), ctypes.c_double(theta), _p(_i32(position)),
+                            _p(_i32(n_nodes)), _p(x))
+    _check(rc, "rope_tree")
+    return x
 
 
 def tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc, scale: float):

@@ -704,3 +704,28 @@ int ddto_scatter_pages(int L, int B, int Hkv, int d, int page, int num_pages, in
                 }
     return DDTO_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Rotary embedding by depth                                                  */
+/* ------------------------------------------------------------------------- */
+
+/* [NOTES] "Where the next step is" / [ARCH] positions shared per depth: every row of a
+ * node is rotated by its node's position, pairs (i, i + rot/2). */
+int ddto_rope_tree(int L, int B, int N, int H, int d, int rot, double theta,
+                   const int32_t* position, const int32_t* n_nodes, double* x) {
+    if (L < 1 || B < 1 || N < 1 || H < 1 || rot < 2 || rot > d || rot % 2 || !(theta > 1.0)) return DDTO_ERR_ARG;
+    const int half = rot / 2;
+    for (int l = 0; l < L; ++l)
+        for (int b = 0; b < B; ++b)
+            for (int n = 0; n < n_nodes[b] && n < N; ++n)
+                for (int h = 0; h < H; ++h) {
+                    double* row = x + ((((long)l * B + b) * N + n) * H + h) * d;
+                    for (int i = 0; i < half; ++i) {
+                        const double a = (double)position[(long)b * N + n] * pow(theta, -2.0 * i / rot);
+                        const double x0 = row[i], x1 = row[i + half];
+                        row[i] = x0 * cos(a) - x1 * sin(a);
+                        row[i + half] = x1 * cos(a) + x0 * sin(a);
+                    }
+                }
+    return DDTO_OK;
+}

@@ -159,6 +159,14 @@ int ddto_scatter_pages(int L, int B, int Hkv, int d, int page, int num_pages, in
                        const double* cache, int Pcap, const int32_t* block_table,
                        const int32_t* n_rows, double* pages);
 
+/* Rotary embedding of tree rows by depth ([NOTES] "Where the next step is": position and
+ * RoPE correctness by branch depth).  READING: the half-split convention of Qwen-style
+ * models.  In place on x [L][B][N][H][d]: for node n < n_nodes[b], i < rot/2,
+ * a = position[b][n] * theta^(-2i/rot): (x[i], x[i+rot/2]) <- (x[i] cos a - x[i+rot/2] sin a,
+ * x[i+rot/2] cos a + x[i] sin a); other channels and padding rows unchanged. */
+int ddto_rope_tree(int L, int B, int N, int H, int d, int rot, double theta,
+                   const int32_t* position, const int32_t* n_nodes, double* x);
+
 #ifdef __cplusplus
 }
 #endif

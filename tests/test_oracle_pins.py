@@ -516,3 +516,41 @@ def test_gather_pages_rejects_bad_tables():
         oracle.gather_pages(pages, np.array([[0, 9]], np.int32), [12], 16)   # page 9 does not exist
     with pytest.raises(RuntimeError):
         oracle.gather_pages(pages, np.array([[0, 1]], np.int32), [17], 17)   # past max_pages * page
+
+
+# ------------------------------------------------------------------ rotary by depth
+def test_rope_closed_forms():
+    """Position 0 is the identity; pair 0 (frequency 1) turns by exactly `position`
+    radians; pair i turns by position * theta^(-2i/rot); channels past rot are kept."""
+    d, rot = 8, 6
+    x = np.zeros((1, 1, 3, 1, d))
+    x[..., 0] = 1.0          # pair 0 -> (cos p, sin p) at channels (0, 3)
+    x[..., 1] = 2.0          # pair 1: x1 = 2 at channel 1, 0 at channel 4
+    x[..., 6:] = 5.0         # outside the rotated part
+    pos = np.array([[0, 3, 7]], np.int32)
+    y = oracle.rope_tree(x, pos, [3], rot, theta=100.0)
+    assert np.allclose(y[0, 0, 0, 0], x[0, 0, 0, 0])
+    for n, p in ((1, 3), (2, 7)):
+        assert np.isclose(y[0, 0, n, 0, 0], np.cos(p)) and np.isclose(y[0, 0, n, 0, 3], np.sin(p))
+        a1 = p * 100.0 ** (-2.0 / rot)
+        assert np.isclose(y[0, 0, n, 0, 1], 2 * np.cos(a1)) and np.isclose(y[0, 0, n, 0, 4], 2 * np.sin(a1))
+        assert (y[0, 0, n, 0, 6:] == 5.0).all()
+
+
+def test_rope_dot_products_depend_on_position_difference_only():
+    """<R(m) q, R(n) k> = <R(m - n) q, k>: the defining property of rotary embedding; also
+    norms are kept and padding rows are untouched."""
+    rng = np.random.default_rng(21)
+    d = 16
+    q = rng.standard_normal((1, 1, 4, 1, d))
+    k = rng.standard_normal((1, 1, 4, 1, d))
+    pos = np.array([[5, 12, 40, 40]], np.int32)
+    qr = oracle.rope_tree(q, pos, [3], d, theta=500.0)
+    kr = oracle.rope_tree(k, pos, [3], d, theta=500.0)
+    for m in range(3):
+        for n in range(3):
+            rel = oracle.rope_tree(q[:, :, m:m + 1], np.array([[pos[0, m] - pos[0, n]]], np.int32), [1], d,
+                                   theta=500.0)
+            assert np.isclose(np.dot(qr[0, 0, m, 0], kr[0, 0, n, 0]), np.dot(rel[0, 0, 0, 0], k[0, 0, n, 0]))
+        assert np.isclose(np.linalg.norm(qr[0, 0, m, 0]), np.linalg.norm(q[0, 0, m, 0]))
+    assert np.array_equal(qr[0, 0, 3], q[0, 0, 3])   # row 3 is padding (n_nodes = 3)

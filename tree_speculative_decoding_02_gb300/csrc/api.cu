@@ -138,6 +138,17 @@ ddt_status ddt_tree_attn_paged(int n_layers, int B, int N, int Hq, int Hkv, int 
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ddt_status ddt_rope_tree(int n_layers, int B, int N, int Hq, int Hkv, int d, int rot_dim, double theta,
+                         ddt_dtype dtype, const int32_t* position, const int32_t* n_nodes, void* q, void* k_tree,
+                         ddt_stream_t stream) {
+    if (n_layers < 1 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || d < 2 || !dtype_ok(dtype)) return DDT_ERR_INVALID_ARG;
+    if (rot_dim < 2 || rot_dim > d || rot_dim % 2 != 0 || !(theta > 1.0)) return DDT_ERR_INVALID_ARG;
+    if (!position || !n_nodes || !q || !k_tree) return DDT_ERR_INVALID_ARG;
+    if (B > 65535) return DDT_ERR_UNSUPPORTED;
+    return from_cuda(launch_rope_tree(n_layers, B, N, Hq, Hkv, d, rot_dim, theta, dtype, position, n_nodes, q, k_tree,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------------------ GDN
 size_t ddt_tree_gdn_workspace(int n_layers, int B, int N, int Hk, int Hv, int dk, int dv) {
     (void)n_layers; (void)B; (void)N; (void)Hk; (void)Hv; (void)dk; (void)dv;

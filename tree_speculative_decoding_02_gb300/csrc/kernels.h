@@ -61,6 +61,8 @@ cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap
                            const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
                            void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st);
 
+cudaError_t launch_rope_tree(int L, int B, int N, int Hq, int Hkv, int d, int rot, double theta, ddt_dtype dtype,
+                             const int32_t* position, const int32_t* n_nodes, void* q, void* k, cudaStream_t st);
 bool gdn_tc_supported(int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in);
 cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype in, ddt_dtype out, const void* x,
                           const void* conv_w, const void* conv_state, const float* beta, const float* decay,

@@ -46,6 +46,7 @@ _SIGS = {
     "ddt_tree_attn_paged": ([_c_int] * 11 + [_c_p] * 9 + [_c_float, _c_p, _c_p, _c_p, _c_size, _c_p], _c_int),
     "ddt_commit_paged": ([_c_int] * 9 + [_c_p] + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13,
                          _c_int),
+    "ddt_rope_tree": ([_c_int] * 7 + [ctypes.c_double, _c_int] + [_c_p] * 5, _c_int),
     "ddt_commit": ([_c_int] * 7 + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13, _c_int),
 }
 EXPORTS = tuple(_SIGS)
@@ -240,6 +241,22 @@ def ddt_tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, prefix
                                  ws.numel(), _stream())
     _check(rc, "ddt_tree_attn_paged")
     return {"o": o, "status": st}
+
+
+def ddt_rope_tree(q, k_tree, position, n_nodes, *, rot_dim=None, theta=10000.0):
+    """In place: q [L][B][N][Hq][d], k_tree [L][B][N][Hkv][d] rotated at position [B][N]."""
+    lib = _gpu()
+    L, B, N, Hq, d = q.shape
+    Hkv = k_tree.shape[3]
+    _need(q, (L, B, N, Hq, d), q.dtype, "q")
+    _need(k_tree, (L, B, N, Hkv, d), q.dtype, "k_tree")
+    _need(position, (B, N), torch.int32, "position")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    rot = int(rot_dim or d)
+    rc = lib.ddt_rope_tree(L, B, N, Hq, Hkv, d, rot, float(theta), _DT[q.dtype], _ptr(position), _ptr(n_nodes),
+                           _ptr(q), _ptr(k_tree), _stream())
+    _check(rc, "ddt_rope_tree")
+    return q, k_tree
 
 
 # ----------------------------------------------------------------------------- GDN

@@ -36,6 +36,9 @@ class Round:
         self.prefix0 = torch.as_tensor(prefix).to(dev)
         self.prefix_len = self.prefix0.clone()
         self.Pcap = int(c.get("Pcap", int(prefix.max()) + self.A))
+        self.page = int(c.get("page", 0))   # > 0: paged prefix caches of this many rows a page
+        if self.page:
+            self.Pcap = -(-self.Pcap // self.page) * self.page
         i32 = dict(dtype=torch.int32, device=dev)
         # drafter output and round roots
         self.draft_logits = synth.draft_logits(B, D, V, std=c.get("logit_std", 3.0), boost=c.get("boost", 6.0),
@@ -53,6 +56,8 @@ class Round:
             self.attn_status = torch.empty((B,), **i32)
             self.attn_ws = torch.empty(max(16, ddt.load().ddt_tree_attn_workspace(
                 self.Lf, B, N, c["Hq"], c["Hkv"], c["d"], self.Pcap)), dtype=torch.uint8, device=dev)
+            if self.page:
+                self._to_pages(workload)
         # GDN layers (state stored [dv][dk])
         self.Lg = c.get("Lg", 0)
         if self.Lg:
@@ -79,12 +84,35 @@ class Round:
         self.commit = {"src_row": torch.empty((B, self.A), **i32), "dst_pos": torch.empty((B, self.A), **i32),
                        "status": torch.empty((B,), **i32)}
 
+    def _to_pages(self, workload):
+        """Move the contiguous caches into head-major pages [L][num_pages][Hkv][page][d]
+        behind a shuffled block table (two spare pages), one layer at a time."""
+        a, pg = self.attn, self.page
+        L, B, Hkv, Pcap, d = a.k_cache.shape
+        mp = Pcap // pg
+        num = B * mp + 2
+        g = synth.gen(workload, 60)
+        self.block_table = torch.randperm(num, generator=g)[:B * mp].reshape(B, mp).to(torch.int32).to(self.device)
+        phys = self.block_table.flatten().long()
+        self.k_pages = torch.empty((L, num, Hkv, pg, d), dtype=a.k_cache.dtype, device=self.device)
+        self.v_pages = torch.empty_like(self.k_pages)
+        for src, dst in ((a.k_cache, self.k_pages), (a.v_cache, self.v_pages)):
+            for l in range(L):
+                dst[l, phys] = src[l].reshape(B, Hkv, mp, pg, d).transpose(1, 2).reshape(B * mp, Hkv, pg, d)
+        a.k_cache = a.v_cache = None
+
     # ------------------------------------------------------------------ the round
     def step(self):
         c = self.cfg
         ddt.ddt_build_tree(self.draft_logits, self.root_token, self.prefix_len, c["top_k"], c["budget"],
                            out=self.tree, workspace=self.build_ws)
-        if self.Lf:
+        if self.Lf and self.page:
+            a = self.attn
+            ddt.ddt_tree_attn_paged(a.q, a.k_tree, a.v_tree, self.k_pages, self.v_pages, self.block_table,
+                                    self.prefix_len, self.tree["n_nodes"], self.tree["anc"],
+                                    scale=1.0 / math.sqrt(c["d"]), out_dtype=self.attn_o.dtype, out=self.attn_o,
+                                    status=self.attn_status, workspace=self.attn_ws)
+        elif self.Lf:
             a = self.attn
             ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, self.prefix_len, self.tree["n_nodes"],
                               self.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out_dtype=self.attn_o.dtype,
@@ -97,14 +125,19 @@ class Round:
         ddt.ddt_walk_accept(self.tree["token"], self.tree["parent"], self.tree["n_nodes"], self.A - 1,
                             target_logits=self.target_logits, out=self.walk, workspace=self.walk_ws)
         kw = {}
-        if self.Lf:
+        if self.Lf and not self.page:
             kw.update(k_tree=self.attn.k_tree, v_tree=self.attn.v_tree, k_cache=self.attn.k_cache,
                       v_cache=self.attn.v_cache)
         if self.Lg:
             g = self.gdn
             kw.update(x=g.x, conv_w=g.conv_w, beta=g.beta, decay=g.decay, S=g.S, conv_state=g.conv_state,
                       Hk=c["Hk"])
-        ddt.ddt_commit(self.walk["acc_nodes"], self.walk["acc_len"], self.prefix_len, out=self.commit, **kw)
+        if self.Lf and self.page:
+            ddt.ddt_commit_paged(self.walk["acc_nodes"], self.walk["acc_len"], self.prefix_len, self.block_table,
+                                 k_tree=self.attn.k_tree, v_tree=self.attn.v_tree, k_pages=self.k_pages,
+                                 v_pages=self.v_pages, out=self.commit, **kw)
+        else:
+            ddt.ddt_commit(self.walk["acc_nodes"], self.walk["acc_len"], self.prefix_len, out=self.commit, **kw)
 
     def restore_prefix(self):
         """Reset the committed prefix lengths (the commit advanced them)."""
