@@ -222,6 +222,7 @@ def run_ours(args, rank, world, local):
     cfg = dict(synth.WORKLOADS[args.workload])
     if args.kv_page:
         cfg["page"] = args.kv_page
+    cfg["flat"] = args.flat
     r = Round(cfg, device=dev, workload=args.workload)
     st = torch.cuda.current_stream()
     ev = {k: [] for k in KERNELS}
@@ -261,7 +262,7 @@ def run_ours(args, rank, world, local):
         if timed:
             marks[3].record(st)
         ddt.ddt_walk_accept(r.tree["token"], r.tree["parent"], r.tree["n_nodes"], r.A - 1,
-                            target_logits=r.target_logits, out=r.walk, workspace=r.walk_ws)
+                            target_logits=r.target_logits, out=r.walk, workspace=r.walk_ws, flat=args.flat)
         if timed:
             marks[4].record(st)
         if r.Lf and r.page:
@@ -390,6 +391,8 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if args.flat:
+        out["config"]["walk"] = "flat-commit safe mode (first children only)"
     if args.kv_page:
         out["config"]["kv"] = f"paged: {args.kv_page} rows a page, shuffled block table"
         out["roofline"]["traffic"] = None   # the recorded capture is of the contiguous layout
@@ -546,6 +549,7 @@ def main():
     ap.add_argument("--workload", type=int, default=WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flat", action="store_true", help="flat-commit safe mode: walk first children only")
     ap.add_argument("--kv-page", type=int, default=0,
                     help="paged prefix caches with this many rows a page (0: contiguous)")
     args = ap.parse_args()

@@ -263,6 +263,20 @@ ddt_status ddt_walk_accept(int B, int N, int V, int max_accept, ddt_dtype dtype,
                            int32_t* emitted, int32_t* n_emitted, int32_t* status,
                            void* workspace, size_t ws_bytes, ddt_stream_t stream);
 
+/* ddt_walk_accept_flat -- the flat-commit safe mode ([NOTES] "What broke along the way":
+ * full non-flat branch commit through the hybrid state is kept behind a research switch).
+ * Same arguments and outputs as ddt_walk_accept, but the walk only ever descends into a
+ * node's first child (its rank-0 child: children are numbered by rank), so the accepted
+ * path is the longest agreeing prefix of the flat DFlash chain inside the tree, and a
+ * round behaves exactly like flat DFlash verification of that chain. */
+ddt_status ddt_walk_accept_flat(int B, int N, int V, int max_accept, ddt_dtype dtype,
+                                const void* target_logits, int32_t* target_argmax,
+                                const int32_t* token, const int32_t* parent,
+                                const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len,
+                                int32_t* bonus, int32_t* emitted, int32_t* n_emitted,
+                                int32_t* status, void* workspace, size_t ws_bytes,
+                                ddt_stream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * ddt_commit -- [NOTES] "Why hybrid attention makes it hard": once a path is accepted,
  * only that path is copied into the contiguous KV and recurrent buffers; [ARCH] KV

@@ -47,7 +47,7 @@ def _load():
             lib = ctypes.CDLL(build())
             for name in ("ddto_build_tree", "ddto_attn_row", "ddto_tree_attn", "ddto_gdn_unit",
                          "ddto_tree_gdn", "ddto_walk", "ddto_commit", "ddto_gather_pages",
-                         "ddto_scatter_pages", "ddto_rope_tree"):
+                         "ddto_scatter_pages", "ddto_rope_tree", "ddto_walk_flat"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -220,8 +220,9 @@ def tree_gdn(x, conv_w, conv_state, beta, decay, S, parent, n_nodes, Hk: int, wa
     return {"o": o, "S_node": sn}
 
 
-def walk(token, parent, n_nodes, D: int, target_logits=None, target_argmax=None):
-    """Greedy tree walk.  target_logits [B][N][V] or target_argmax [B][N]."""
+def walk(token, parent, n_nodes, D: int, target_logits=None, target_argmax=None, flat: bool = False):
+    """Greedy tree walk.  target_logits [B][N][V] or target_argmax [B][N].  flat: the safe
+    mode that only descends into first (rank-0) children."""
     lib = _load()
     token, parent = _i32(token), _i32(parent)
     B, N = token.shape
@@ -237,9 +238,10 @@ def walk(token, parent, n_nodes, D: int, target_logits=None, target_argmax=None)
     out = {"target_argmax": np.zeros((B, N), np.int32), "acc_nodes": np.zeros((B, A), np.int32),
            "acc_len": np.zeros(B, np.int32), "bonus": np.zeros(B, np.int32),
            "emitted": np.zeros((B, A), np.int32), "n_emitted": np.zeros(B, np.int32)}
-    rc = lib.ddto_walk(B, N, V, D, _p(tl), _p(ta_in), _p(token), _p(parent), _p(_i32(n_nodes)),
-                       _p(out["target_argmax"]), _p(out["acc_nodes"]), _p(out["acc_len"]), _p(out["bonus"]),
-                       _p(out["emitted"]), _p(out["n_emitted"]))
+    fn = lib.ddto_walk_flat if flat else lib.ddto_walk
+    rc = fn(B, N, V, D, _p(tl), _p(ta_in), _p(token), _p(parent), _p(_i32(n_nodes)),
+            _p(out["target_argmax"]), _p(out["acc_nodes"]), _p(out["acc_len"]), _p(out["bonus"]),
+            _p(out["emitted"]), _p(out["n_emitted"]))
     _check(rc, "walk")
     return out
 

@@ -496,10 +496,10 @@ int ddto_tree_gdn(int L, int B, int N, int Hk, int Hv, int dk, int dv, int K,
  * row is its argmax (READING: ties to the lower id).  [NOTES] "What broke along the
  * way": the bonus token (the target's token at the last accepted node) is emitted but
  * is not an accepted draft. */
-int ddto_walk(int B, int N, int V, int D, const double* target_logits,
-              const int32_t* target_argmax_in, const int32_t* token, const int32_t* parent,
-              const int32_t* n_nodes, int32_t* target_argmax_out, int32_t* acc_nodes,
-              int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted) {
+static int walk_impl(int B, int N, int V, int D, const double* target_logits,
+                     const int32_t* target_argmax_in, const int32_t* token, const int32_t* parent,
+                     const int32_t* n_nodes, int32_t* target_argmax_out, int32_t* acc_nodes,
+                     int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted, int flat) {
     if (B < 1 || N < 1 || V < 1 || D < 0) return DDTO_ERR_ARG;
     const int A = D + 1;
     int* t = (int*)malloc(sizeof(int) * (size_t)N);
@@ -527,10 +527,12 @@ int ddto_walk(int B, int N, int V, int D, const double* target_logits,
         for (;;) {
             int next = -1;
             for (int c = 1; c < nn; ++c)
-                if (parent[(long)b * N + c] == cur && token[(long)b * N + c] == t[cur]) {
+                if (parent[(long)b * N + c] == cur && (flat || token[(long)b * N + c] == t[cur])) {
                     next = c;
                     break;
                 }
+            /* flat: only the first child, the rank-0 one, may be taken */
+            if (flat && next >= 0 && token[(long)b * N + next] != t[cur]) next = -1;
             if (next < 0 || a + 1 >= A) break;
             cur = next;
             an[++a] = cur;
@@ -543,6 +545,24 @@ int ddto_walk(int B, int N, int V, int D, const double* target_logits,
     }
     free(t);
     return DDTO_OK;
+}
+
+int ddto_walk(int B, int N, int V, int D, const double* target_logits,
+              const int32_t* target_argmax_in, const int32_t* token, const int32_t* parent,
+              const int32_t* n_nodes, int32_t* target_argmax_out, int32_t* acc_nodes,
+              int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted) {
+    return walk_impl(B, N, V, D, target_logits, target_argmax_in, token, parent, n_nodes, target_argmax_out,
+                     acc_nodes, acc_len, bonus, emitted, n_emitted, 0);
+}
+
+/* [NOTES] "What broke along the way": the safe mode commits only along the flat chain,
+ * i.e. the walk descends only into a node's first (rank-0) child. */
+int ddto_walk_flat(int B, int N, int V, int D, const double* target_logits,
+                   const int32_t* target_argmax_in, const int32_t* token, const int32_t* parent,
+                   const int32_t* n_nodes, int32_t* target_argmax_out, int32_t* acc_nodes,
+                   int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted) {
+    return walk_impl(B, N, V, D, target_logits, target_argmax_in, token, parent, n_nodes, target_argmax_out,
+                     acc_nodes, acc_len, bonus, emitted, n_emitted, 1);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -124,6 +124,12 @@ int ddto_walk(int B, int N, int V, int D, const double* target_logits,
               const int32_t* target_argmax_in, const int32_t* token, const int32_t* parent,
               const int32_t* n_nodes, int32_t* target_argmax_out, int32_t* acc_nodes,
               int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted);
+/* Flat-commit safe mode: as ddto_walk, but only a node's first (rank-0) child is ever
+ * taken, so the accepted path is the agreeing prefix of the tree's flat chain. */
+int ddto_walk_flat(int B, int N, int V, int D, const double* target_logits,
+                   const int32_t* target_argmax_in, const int32_t* token, const int32_t* parent,
+                   const int32_t* n_nodes, int32_t* target_argmax_out, int32_t* acc_nodes,
+                   int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted);
 
 /*
  * Commit of the accepted path ([NOTES] "Why hybrid attention makes it hard",

@@ -63,6 +63,36 @@ def test_walk_argmax_input_and_ties():
         np.testing.assert_array_equal(g2[k], o[k])
 
 
+def test_flat_walk_matches_oracle():
+    """Safe mode: only first (rank-0) children are taken.  Targets agree with a random child
+    (often not the first) at 70 % of the rows, so the flat and the ordinary walks differ."""
+    tree, _ = C.tree_from_logits(2, 4, 8, 3000, 4, 64)
+    rng = np.random.default_rng(9)
+    N = tree["token"].shape[1]
+    targ = np.full((4, N), 5, np.int32)
+    for b in range(4):
+        for i in range(int(tree["n_nodes"][b])):
+            kids = [c for c in range(1, int(tree["n_nodes"][b])) if tree["parent"][b][c] == i]
+            if kids and rng.random() < 0.7:
+                targ[b, i] = tree["token"][b][kids[0] if rng.random() < 0.6 else kids[-1]]
+    t = C.tree_to_dev(tree)
+    r = ddt.ddt_walk_accept(t["token"], t["parent"], t["n_nodes"], 8,
+                            target_argmax=torch.as_tensor(targ).cuda(), flat=True)
+    torch.cuda.synchronize()
+    o = oracle.walk(tree["token"], tree["parent"], tree["n_nodes"], 8, target_argmax=targ, flat=True)
+    for k in _WALK_KEYS:
+        np.testing.assert_array_equal(r[k].cpu().numpy(), o[k], err_msg=k)
+    full = oracle.walk(tree["token"], tree["parent"], tree["n_nodes"], 8, target_argmax=targ)
+    assert (o["acc_len"] <= full["acc_len"]).all() and (o["acc_len"] < full["acc_len"]).any()
+    # with target logits: planted along the first-child spine, flat and ordinary agree
+    tl = _planted_logits(tree, 3000, 2, torch.bfloat16, np.array([8, 3, 0, 5]))
+    g = _walk_gpu(tree, 8, tl=tl)
+    r2 = ddt.ddt_walk_accept(t["token"], t["parent"], t["n_nodes"], 8, target_logits=tl.cuda(), flat=True)
+    torch.cuda.synchronize()
+    for k in _WALK_KEYS:
+        np.testing.assert_array_equal(r2[k].cpu().numpy(), g[k], err_msg=k)
+
+
 def test_walk_nonfinite_flagged():
     tree, _ = C.tree_from_logits(2, 2, 4, 40, 2, 6, std=2.0, boost=0.0)
     tl = torch.randn(2, 7, 40)

@@ -554,3 +554,75 @@ def test_rope_dot_products_depend_on_position_difference_only():
             assert np.isclose(np.dot(qr[0, 0, m, 0], kr[0, 0, n, 0]), np.dot(rel[0, 0, 0, 0], k[0, 0, n, 0]))
         assert np.isclose(np.linalg.norm(qr[0, 0, m, 0]), np.linalg.norm(q[0, 0, m, 0]))
     assert np.array_equal(qr[0, 0, 3], q[0, 0, 3])   # row 3 is padding (n_nodes = 3)
+
+
+# ------------------------------------------------------------------ flat-commit safe mode
+def _paths(tree, b):
+    """Token path (root excluded) of every row of request b."""
+    out = []
+    for i in range(int(tree["n_nodes"][b])):
+        p = R.path_rows(tree["parent"][b], i)
+        out.append(tuple(int(tree["token"][b][r]) for r in p[1:]))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_flat_walk_is_the_dflash_chain_walk(seed):
+    """The safe-mode walk on a k = 4 tree accepts exactly what the ordinary walk accepts on
+    the k = 1 tree (the flat DFlash chain) of the same drafter logits, when the target's
+    token is a function of the token path: the regression invariant against flat DFlash."""
+    rng = np.random.default_rng(100 + seed)
+    D, V = 5, 7
+    logits = rng.integers(-3, 4, size=(1, D, V)).astype(np.float64) + rng.standard_normal((1, D, V)) * 0.1
+    full = oracle.build_tree(logits, [1], [0], 4, 30)
+    chain = oracle.build_tree(logits, [1], [0], 1, 30)
+    spine = _paths(chain, 0)[-1]                  # c_1 .. c_D
+    m = int(rng.integers(0, D + 1))
+    table = {}
+
+    def target(path):
+        if path not in table:
+            j = len(path)
+            if j < m and path == spine[:j]:
+                table[path] = spine[j]            # agree along the chain
+            else:                                 # anything else (often a sibling's token)
+                table[path] = int(rng.integers(0, V)) if j >= D or path != spine[:j] else (spine[j] + 1) % V
+        return table[path]
+
+    def argmax_rows(tree):
+        return np.array([[target(p) for p in _paths(tree, 0)] + [0] * (tree["token"].shape[1] - tree["n_nodes"][0])],
+                        np.int32)
+
+    f = oracle.walk(full["token"], full["parent"], full["n_nodes"], D, target_argmax=argmax_rows(full), flat=True)
+    c = oracle.walk(chain["token"], chain["parent"], chain["n_nodes"], D, target_argmax=argmax_rows(chain))
+    assert int(f["acc_len"][0]) == int(c["acc_len"][0]) == min(m, D)
+    assert f["emitted"].tolist() == c["emitted"].tolist() and int(f["bonus"][0]) == int(c["bonus"][0])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_flat_walk_brute_force_on_the_first_child_spine(seed):
+    """Brute force: follow first children while the edge matches the target argmax; also
+    never longer than the ordinary walk, and equal to it on a chain tree."""
+    rng = np.random.default_rng(200 + seed)
+    tree, _ = C_tree(rng)
+    tok, par, nn = tree["token"][0], tree["parent"][0], int(tree["n_nodes"][0])
+    targ = np.zeros((1, tok.shape[0]), np.int32)
+    for i in range(nn):                          # half the rows agree with some child
+        kids = [c for c in range(1, nn) if par[c] == i]
+        targ[0, i] = int(tok[kids[int(rng.integers(len(kids)))]]) if kids and rng.random() < 0.7 else 10 ** 6
+    f = oracle.walk(tree["token"], tree["parent"], tree["n_nodes"], 8, target_argmax=targ, flat=True)
+    g = oracle.walk(tree["token"], tree["parent"], tree["n_nodes"], 8, target_argmax=targ)
+    cur, want = 0, [0]
+    while True:
+        kids = [c for c in range(1, nn) if par[c] == cur]
+        if not kids or int(tok[kids[0]]) != int(targ[0, cur]) or len(want) > 8:
+            break
+        cur = kids[0]
+        want.append(cur)
+    assert f["acc_nodes"][0][:len(want)].tolist() == want and int(f["acc_len"][0]) == len(want) - 1
+    assert int(f["acc_len"][0]) <= int(g["acc_len"][0])
+
+
+def C_tree(rng):
+    logits = rng.standard_normal((1, 8, 40)) * 2
+    return oracle.build_tree(logits, [3], [0], 3, 40), logits

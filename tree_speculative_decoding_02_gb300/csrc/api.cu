@@ -187,11 +187,11 @@ size_t ddt_walk_accept_workspace(int B, int N, int V) {
     return walk_ws_bytes(B, N, V);
 }
 
-ddt_status ddt_walk_accept(int B, int N, int V, int max_accept, ddt_dtype dtype, const void* target_logits,
-                           int32_t* target_argmax, const int32_t* token, const int32_t* parent,
-                           const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
-                           int32_t* emitted, int32_t* n_emitted, int32_t* status, void* workspace, size_t ws_bytes,
-                           ddt_stream_t stream) {
+static ddt_status walk_accept(int B, int N, int V, int max_accept, ddt_dtype dtype, const void* target_logits,
+                              int32_t* target_argmax, const int32_t* token, const int32_t* parent,
+                              const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
+                              int32_t* emitted, int32_t* n_emitted, int32_t* status, void* workspace, size_t ws_bytes,
+                              int flat, ddt_stream_t stream) {
     if (B < 1 || N < 1 || V < 1 || max_accept < 0 || !dtype_ok(dtype)) return DDT_ERR_INVALID_ARG;
     if (N > kMaxRows) return DDT_ERR_UNSUPPORTED;
     if (!target_argmax || !token || !parent || !n_nodes || !acc_nodes || !acc_len || !bonus || !emitted ||
@@ -200,8 +200,26 @@ ddt_status ddt_walk_accept(int B, int N, int V, int max_accept, ddt_dtype dtype,
     if (target_logits && (!workspace || ws_bytes < walk_ws_bytes(B, N, V) || !aligned16(workspace)))
         return DDT_ERR_INVALID_ARG;
     return from_cuda(launch_walk(B, N, V, max_accept + 1, dtype, target_logits, target_argmax, token, parent, n_nodes,
-                                 acc_nodes, acc_len, bonus, emitted, n_emitted, status, workspace,
+                                 acc_nodes, acc_len, bonus, emitted, n_emitted, status, workspace, flat,
                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ddt_status ddt_walk_accept(int B, int N, int V, int max_accept, ddt_dtype dtype, const void* target_logits,
+                           int32_t* target_argmax, const int32_t* token, const int32_t* parent,
+                           const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
+                           int32_t* emitted, int32_t* n_emitted, int32_t* status, void* workspace, size_t ws_bytes,
+                           ddt_stream_t stream) {
+    return walk_accept(B, N, V, max_accept, dtype, target_logits, target_argmax, token, parent, n_nodes, acc_nodes,
+                       acc_len, bonus, emitted, n_emitted, status, workspace, ws_bytes, 0, stream);
+}
+
+ddt_status ddt_walk_accept_flat(int B, int N, int V, int max_accept, ddt_dtype dtype, const void* target_logits,
+                                int32_t* target_argmax, const int32_t* token, const int32_t* parent,
+                                const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
+                                int32_t* emitted, int32_t* n_emitted, int32_t* status, void* workspace,
+                                size_t ws_bytes, ddt_stream_t stream) {
+    return walk_accept(B, N, V, max_accept, dtype, target_logits, target_argmax, token, parent, n_nodes, acc_nodes,
+                       acc_len, bonus, emitted, n_emitted, status, workspace, ws_bytes, 1, stream);
 }
 
 // ---------------------------------------------------------------------------- commit

@@ -37,7 +37,7 @@ size_t walk_ws_bytes(int B, int N, int V);
 cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void* logits, int32_t* targ,
                         const int32_t* token, const int32_t* parent, const int32_t* n_nodes, int32_t* acc_nodes,
                         int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted, int32_t* status,
-                        void* ws, cudaStream_t st);
+                        void* ws, int flat, cudaStream_t st);
 
 cudaError_t launch_attn_simt(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype in, ddt_dtype out,
                              const void* q, const void* k_tree, const void* v_tree, const void* k_cache,

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) k_walk_argmax(const T* __restrict__ logit
     }
 }
 
-__global__ void __launch_bounds__(256) k_walk_descend(int N, int V, int A, int nch, int have_logits,
+__global__ void __launch_bounds__(256) k_walk_descend(int N, int V, int A, int nch, int have_logits, int flat,
                                                        const ArgPartial* __restrict__ part,
                                                        int32_t* __restrict__ targ, const int32_t* __restrict__ token,
                                                        const int32_t* __restrict__ parent,
@@ -177,10 +177,12 @@ __global__ void __launch_bounds__(256) k_walk_descend(int N, int V, int A, int n
         for (;;) {
             const int want = s_t[cur];
             int found = 0x7fffffff;
+            // flat: only the first child (the rank-0 one: children are numbered by rank)
             for (int c = 1 + lane; c < nn; c += 32)
-                if (s_par[c] == cur && s_tok[c] == want) found = min(found, c);
+                if (s_par[c] == cur && (flat || s_tok[c] == want)) found = min(found, c);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) found = min(found, __shfl_xor_sync(kFull, found, o));
+            if (flat && found != 0x7fffffff && s_tok[found] != want) found = 0x7fffffff;
             if (found == 0x7fffffff || a + 1 >= A) break;
             if (lane == 0) an[a + 1] = found;
             cur = found;
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(256) k_walk_descend(int N, int V, int A, int n
 cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void* logits, int32_t* targ,
                         const int32_t* token, const int32_t* parent, const int32_t* n_nodes, int32_t* acc_nodes,
                         int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted, int32_t* status,
-                        void* ws, cudaStream_t st) {
+                        void* ws, int flat, cudaStream_t st) {
     const int nch = (V + kBuildChunk - 1) / kBuildChunk;
     ArgPartial* part = static_cast<ArgPartial*>(ws);
     if (logits) {
@@ -227,7 +229,7 @@ cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void*
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    k_walk_descend<<<counted(B), 256, 0, st>>>(N, V, A, nch, logits != nullptr, part, targ, token, parent, n_nodes, acc_nodes,
+    k_walk_descend<<<counted(B), 256, 0, st>>>(N, V, A, nch, logits != nullptr, flat, part, targ, token, parent, n_nodes, acc_nodes,
                                       acc_len, bonus, emitted, n_emitted, status);
     return cudaGetLastError();
 }

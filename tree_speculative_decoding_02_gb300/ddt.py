@@ -42,6 +42,7 @@ _SIGS = {
     "ddt_tree_gdn": ([_c_int] * 10 + [_c_p] * 10 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_walk_accept_workspace": ([_c_int] * 3, _c_size),
     "ddt_walk_accept": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_walk_accept_flat": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_tree_attn_paged_workspace": ([_c_int] * 8, _c_size),
     "ddt_tree_attn_paged": ([_c_int] * 11 + [_c_p] * 9 + [_c_float, _c_p, _c_p, _c_p, _c_size, _c_p], _c_int),
     "ddt_commit_paged": ([_c_int] * 9 + [_c_p] + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13,
@@ -294,8 +295,9 @@ def ddt_tree_gdn(x, conv_w, conv_state, beta, decay, S, parent, n_nodes, *, Hk: 
 
 # ---------------------------------------------------------------------------- walk
 def ddt_walk_accept(token, parent, n_nodes, max_accept: int, *, target_logits=None, target_argmax=None, out=None,
-                    workspace=None):
-    """Greedy walk.  target_logits [B][N][V] (or target_argmax [B][N] int32)."""
+                    workspace=None, flat=False):
+    """Greedy walk.  target_logits [B][N][V] (or target_argmax [B][N] int32).  flat: the
+    safe mode that only descends into first (rank-0) children (ddt_walk_accept_flat)."""
     lib = _gpu()
     B, N = token.shape
     dev = token.device
@@ -323,11 +325,12 @@ def ddt_walk_accept(token, parent, n_nodes, max_accept: int, *, target_logits=No
            "status": o.get("status", torch.empty((B,), **i32))}
     need = lib.ddt_walk_accept_workspace(B, N, V)
     ws = workspace if workspace is not None else _ws(need, dev)
-    rc = lib.ddt_walk_accept(B, N, V, int(max_accept), dt, _ptr(target_logits), _ptr(targ), _ptr(token),
-                             _ptr(parent), _ptr(n_nodes), _ptr(res["acc_nodes"]), _ptr(res["acc_len"]),
-                             _ptr(res["bonus"]), _ptr(res["emitted"]), _ptr(res["n_emitted"]), _ptr(res["status"]),
-                             _ptr(ws), ws.numel(), _stream())
-    _check(rc, "ddt_walk_accept")
+    fn = lib.ddt_walk_accept_flat if flat else lib.ddt_walk_accept
+    rc = fn(B, N, V, int(max_accept), dt, _ptr(target_logits), _ptr(targ), _ptr(token),
+            _ptr(parent), _ptr(n_nodes), _ptr(res["acc_nodes"]), _ptr(res["acc_len"]),
+            _ptr(res["bonus"]), _ptr(res["emitted"]), _ptr(res["n_emitted"]), _ptr(res["status"]),
+            _ptr(ws), ws.numel(), _stream())
+    _check(rc, "ddt_walk_accept_flat" if flat else "ddt_walk_accept")
     return res
 
 

@@ -123,7 +123,8 @@ class Round:
                              self.tree["n_nodes"], Hk=c["Hk"], out_dtype=self.gdn_o.dtype, out=self.gdn_o,
                              status=self.gdn_status)
         ddt.ddt_walk_accept(self.tree["token"], self.tree["parent"], self.tree["n_nodes"], self.A - 1,
-                            target_logits=self.target_logits, out=self.walk, workspace=self.walk_ws)
+                            target_logits=self.target_logits, out=self.walk, workspace=self.walk_ws,
+                            flat=bool(c.get("flat", False)))
         kw = {}
         if self.Lf and not self.page:
             kw.update(k_tree=self.attn.k_tree, v_tree=self.attn.v_tree, k_cache=self.attn.k_cache,
