@@ -169,8 +169,8 @@ def round_bytes(r):
 # keyed by the SHA-256 of the kernel's sources: once they change, the figure is stale
 # and the bench reports null until it is captured again.
 ATTN_TRAFFIC = {
-    # ncu: dram__bytes_read.sum 40.35 GB + dram__bytes_write.sum 402.61 MB, batched round
-    "51b97e022bc50a663363ccd404af2087c653ab1306d0c826604471f038c7a718": {"workload": 5, "bytes": 40.75261e9},
+    # ncu: dram__bytes_read.sum 40,354,602,496 B + dram__bytes_write.sum 402,604,288 B, batched round
+    "6dc682ba13aa8af5202906b4e1309c7fd20f878870e5941d616d41acd0d02637": {"workload": 5, "bytes": 40757206784.0},
 }
 ATTN_SOURCES = ("attn_tc.cu", "tc.cuh")
 
