@@ -41,7 +41,7 @@ size_t build_ws_bytes(int B, int D, int V, int k) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) k_build_partial(const T* __restrict__ logits, int D, int V, int k,
+__global__ void __launch_bounds__(256, 4) k_build_partial(const T* __restrict__ logits, int D, int V, int k,
                                                         int nch, int vec, BuildPartial* __restrict__ part,
                                                         float* __restrict__ pv, int* __restrict__ pid) {
     constexpr int kPer = kBuildChunk / 256;  // elements per thread (32)
