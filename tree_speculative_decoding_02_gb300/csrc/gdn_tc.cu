@@ -120,6 +120,22 @@ __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.syn
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
 
+// four consecutive input channels as floats (8-byte bf16 / 16-byte fp32 loads)
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xffff0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = a.x;
+    v[1] = a.y;
+    v[2] = a.z;
+    v[3] = a.w;
+}
+
 // 16-byte global -> shared copy that completes asynchronously (both addresses 16-byte aligned)
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
@@ -191,6 +207,10 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             else off = 2L * p.Hk * kDK + (long)g * p.R * kDV + (sgm - 2 * lq) * step;
             prefetch_l2(row + off);
         }
+        for (int n = tid; n < nr; n += kThr) {  // the gates of the CTA's value heads
+            prefetch_l2(p.beta + (lb * N + n) * p.Hv + (long)g * p.R);
+            prefetch_l2(p.decay + (lb * N + n) * p.Hv + (long)g * p.R);
+        }
     }
     if (tid == 0) {
         *err = (nn < 1 || nn > N) ? DDT_ERR_TREE : DDT_OK;
@@ -257,15 +277,19 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     const int srow0 = (int)((lb * p.Hv + (long)g * p.R) * kDV);
     if (tid == 0) tc::prefetch_tmap(&tm_s);
 
-    // ---- conv + SiLU + L2 norm of q and k: half-warp per (node, q|k), 8 channels a lane
+    // ---- conv + SiLU + L2 norm of q and k: half-warp per (node, q|k); a lane takes channels
+    //      4 sub .. 4 sub + 3 and 64 + 4 sub .. 64 + 4 sub + 3 of its half, so that each
+    //      16-byte store of the swizzled tile is free of bank conflicts
     {
         const int half = lane >> 4, sub = lane & 15;
-        const int c0 = (half == 0 ? g * kDK : p.Hk * kDK + g * kDK) + sub * 8;
+        const int cb = (half == 0 ? g * kDK : p.Hk * kDK + g * kDK);
+        const int cA = cb + 4 * sub, cB = cb + 64 + 4 * sub;
         float w[8][KT];
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
 #pragma unroll
-            for (int q = 0; q < KT; ++q) w[ch][q] = (q < K) ? to_f32(wl[(long)(c0 + ch) * K + q]) : 0.f;
+            for (int q = 0; q < KT; ++q)
+                w[ch][q] = (q < K) ? to_f32(wl[(long)(ch < 4 ? cA + ch : cB + ch - 4) * K + q]) : 0.f;
         // two nodes per pass, so their loads are in flight together
         constexpr int kW = kThr / 32;
         for (int n0 = warp; n0 < N; n0 += 2 * kW) {
@@ -278,10 +302,14 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
 #pragma unroll
                 for (int q = 0; q < KT; ++q) {
                     if (q < K) {
-                        float in[8];
-                        load8(taps[nc * K + q] + c0, in);
+                        float ia[4], ib[4];
+                        load4(taps[nc * K + q] + cA, ia);
+                        load4(taps[nc * K + q] + cB, ib);
 #pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) yy[s2][ch] = fmaf(w[ch][q], in[ch], yy[s2][ch]);
+                        for (int ch = 0; ch < 4; ++ch) {
+                            yy[s2][ch] = fmaf(w[ch][q], ia[ch], yy[s2][ch]);
+                            yy[s2][ch + 4] = fmaf(w[ch + 4][q], ib[ch], yy[s2][ch + 4]);
+                        }
                     }
                 }
             }
@@ -306,7 +334,6 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 for (int ch = 0; ch < 8; ++ch) y[ch] *= sc;
             }
             const int row = half == 0 ? p.QOFF + n : n;
-            const int col = sub * 8;
             // y = hi + lo, hi rounded to tf32: the dense MMAs read hi, the Gram reads both
             float lo[8];
 #pragma unroll
@@ -315,10 +342,10 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 lo[ch] = y[ch] - hv;
                 y[ch] = hv;
             }
-            *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(y[0], y[1], y[2], y[3]);
-            *reinterpret_cast<float4*>(sKQ + sw_off(row, col + 4, p.NPAD)) = make_float4(y[4], y[5], y[6], y[7]);
-            *reinterpret_cast<float4*>(sLO + sw_off(row, col, p.NPAD)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<float4*>(sLO + sw_off(row, col + 4, p.NPAD)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
+            *reinterpret_cast<float4*>(sKQ + sw_off(row, 4 * sub, p.NPAD)) = make_float4(y[0], y[1], y[2], y[3]);
+            *reinterpret_cast<float4*>(sKQ + sw_off(row, 64 + 4 * sub, p.NPAD)) = make_float4(y[4], y[5], y[6], y[7]);
+            *reinterpret_cast<float4*>(sLO + sw_off(row, 4 * sub, p.NPAD)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<float4*>(sLO + sw_off(row, 64 + 4 * sub, p.NPAD)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
             }
         }
         // padding rows of the tile
