@@ -151,13 +151,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sRing = base;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * Cfg::kStageBytes);
     uint64_t* full = bars;                 // [kStages] TMA landed
-    uint64_t* empty = bars + kStages;      // [kStages] MMA done with the stage
+    // [kSlots] tile slot free: the P.V MMAs of the slot's last tile are done, so its K and
+    // V stages may be refilled and O holds that tile.  One commit per tile instead of one
+    // per stage and one more for O: each commit costs the single issuing thread ~100 cycles.
+    constexpr int kSlots = kStages / 2;
+    uint64_t* tfree = bars + kStages;
     uint64_t* s_full = bars + 2 * kStages; // [2] S_j in TMEM
     uint64_t* p_full = s_full + 2;         // [2] P_j in TMEM (128 arrivals)
-    uint64_t* o_done = p_full + 2;         // one completion per PV
-    uint64_t* drain = o_done + 1;
-    // Single-phase barrier for the epilogue: when the softmax reaches it, o_done may
-    // still lack the last two completions, which a parity wait cannot tell apart.
+    uint64_t* drain = p_full + 2;
+    // Single-phase barrier for the epilogue: a tile-slot barrier may be behind by more
+    // than one phase when the softmax finishes, which a parity wait cannot tell apart.
     uint64_t* o_final = drain + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -222,13 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             tc::mbar_init(full + i, 1);
-            tc::mbar_init(empty + i, 1);
+            if (i < kSlots) tc::mbar_init(tfree + i, 1);
         }
         tc::mbar_init(s_full, 1);
         tc::mbar_init(s_full + 1, 1);
         tc::mbar_init(p_full, 256);
         tc::mbar_init(p_full + 1, 256);
-        tc::mbar_init(o_done, 1);
         tc::mbar_init(drain, 1);
         tc::mbar_init(o_final, 1);
         *abort_flag = 0;
@@ -287,13 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             for (int j = 0; j < T && !*abort_flag; ++j) {
                 const Tile t = tile_of(j, n_pre, c0, c1, ragged);
-                bool ok = true;
+                // both stages of tile j sit in slot j % kSlots (stages 2j and 2j + 1 mod kStages)
+                bool ok = tc::mbar_wait(tfree + j % kSlots, ((j / kSlots) & 1) ^ 1, abort_flag);
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                     const int u = 2 * j + kv, st = u % kStages;
-                    if (!tc::mbar_wait(empty + st, ((u / kStages) & 1) ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
                     tc::mbar_expect_tx(full + st, Cfg::kStageBytes);
                     unsigned char* dst = sRing + st * Cfg::kStageBytes;
                     if (!t.tree && p.paged) {
@@ -356,8 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::mma_f16_ts_acc(tmem + Cfg::kOCol, pa + part * (kBN / 2) + kk * 8,
                                        vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv);
                 }
-                tc::mma_commit(empty + st);
-                tc::mma_commit(o_done);
+                tc::mma_commit(tfree + i % kSlots);
                 return true;
             };
             bool ok = true;
@@ -376,7 +374,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t koff = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
                     tc::mma_f16_ts_acc(sd, qa + kk * 8, kd + static_cast<uint64_t>(koff >> 4), idesc_qk);
                 }
-                tc::mma_commit(empty + st);
                 tc::mma_commit(s_full + (j & 1));
                 if (j >= 1) ok = pv(j - 1);
             }
@@ -436,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool grow = mtile > m_used + kTau;
             const bool need = grow && (m_used != -INFINITY);  // O already holds this row's data
             if (__any_sync(kFull, need)) {
-                ok = __all_sync(kFull, tc::mbar_wait(o_done, (j - 1) & 1, abort_flag));
+                ok = __all_sync(kFull, tc::mbar_wait(tfree + (j - 1) % kSlots, ((j - 1) / kSlots) & 1, abort_flag));
                 if (!ok) continue;
                 tc::tc_fence_after();
                 const float f = need ? tc::ex2(m_used - mtile) : 1.f;
