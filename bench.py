@@ -220,6 +220,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     ddt.load()
     cfg = dict(synth.WORKLOADS[args.workload])
+    if "budget" not in cfg:          # the build-and-walk workload lists budgets: time the largest
+        cfg["budget"] = max(cfg["budgets"])
     if args.kv_page:
         cfg["page"] = args.kv_page
     cfg["flat"] = args.flat
@@ -265,7 +267,9 @@ def run_ours(args, rank, world, local):
                             target_logits=r.target_logits, out=r.walk, workspace=r.walk_ws, flat=args.flat)
         if timed:
             marks[4].record(st)
-        if r.Lf and r.page:
+        if not (r.Lf or r.Lg):
+            pass                       # nothing is cached: the round ends with the walk
+        elif r.Lf and r.page:
             ddt.ddt_commit_paged(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, r.block_table,
                                  k_tree=r.attn.k_tree, v_tree=r.attn.v_tree, k_pages=r.k_pages, v_pages=r.v_pages,
                                  out=r.commit, **kw)

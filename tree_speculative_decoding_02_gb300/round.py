@@ -30,8 +30,10 @@ class Round:
         if prefix is None:
             if "P" in c:
                 prefix = np.full(B, c["P"], np.int32)
-            else:
+            elif "P_lo" in c:
                 prefix = synth.prefix_lengths(B, c["P_lo"], c["P_hi"], g=synth.gen(workload, 2)).numpy()
+            else:                      # no attention layers: the prefix only sets positions
+                prefix = np.zeros(B, np.int32)
         prefix = np.asarray(prefix, np.int32)
         self.prefix0 = torch.as_tensor(prefix).to(dev)
         self.prefix_len = self.prefix0.clone()
@@ -133,6 +135,8 @@ class Round:
             g = self.gdn
             kw.update(x=g.x, conv_w=g.conv_w, beta=g.beta, decay=g.decay, S=g.S, conv_state=g.conv_state,
                       Hk=c["Hk"])
+        if not (self.Lf or self.Lg):
+            return                     # nothing is cached: the round ends with the walk
         if self.Lf and self.page:
             ddt.ddt_commit_paged(self.walk["acc_nodes"], self.walk["acc_len"], self.prefix_len, self.block_table,
                                  k_tree=self.attn.k_tree, v_tree=self.attn.v_tree, k_pages=self.k_pages,
