@@ -104,10 +104,16 @@ class Round:
         a.k_cache = a.v_cache = None
 
     # ------------------------------------------------------------------ the round
-    def step(self):
+    def step(self, wait=None):
+        """One round.  wait(name), if given, is called before the call that first reads the
+        inputs of group `name` ("build", "attn", "gdn", "walk"; see input_groups)."""
         c = self.cfg
+        if wait:
+            wait("build")
         ddt.ddt_build_tree(self.draft_logits, self.root_token, self.prefix_len, c["top_k"], c["budget"],
                            out=self.tree, workspace=self.build_ws)
+        if wait and self.Lf:
+            wait("attn")
         if self.Lf and self.page:
             a = self.attn
             ddt.ddt_tree_attn_paged(a.q, a.k_tree, a.v_tree, self.k_pages, self.v_pages, self.block_table,
@@ -120,10 +126,14 @@ class Round:
                               self.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out_dtype=self.attn_o.dtype,
                               out=self.attn_o, status=self.attn_status, workspace=self.attn_ws)
         if self.Lg:
+            if wait:
+                wait("gdn")
             g = self.gdn
             ddt.ddt_tree_gdn(g.x, g.conv_w, g.conv_state, g.beta, g.decay, g.S, self.tree["parent"],
                              self.tree["n_nodes"], Hk=c["Hk"], out_dtype=self.gdn_o.dtype, out=self.gdn_o,
                              status=self.gdn_status)
+        if wait:
+            wait("walk")
         ddt.ddt_walk_accept(self.tree["token"], self.tree["parent"], self.tree["n_nodes"], self.A - 1,
                             target_logits=self.target_logits, out=self.walk, workspace=self.walk_ws,
                             flat=bool(c.get("flat", False)))
@@ -161,6 +171,16 @@ class Round:
         if self.Lg:
             ins.update(x=self.gdn.x, beta=self.gdn.beta, decay=self.gdn.decay)
         return ins
+
+    def input_groups(self):
+        """Names of round_inputs() by the call that first reads them, in call order."""
+        g = {"build": ["draft_logits", "root_token"]}
+        if self.Lf:
+            g["attn"] = ["q", "k_tree", "v_tree"]
+        if self.Lg:
+            g["gdn"] = ["x", "beta", "decay"]
+        g["walk"] = ["target_logits"]
+        return g
 
     def bind_inputs(self, ins: dict):
         """Point the round at another set of per-round input tensors (same keys, shapes and
