@@ -280,9 +280,24 @@ def run_ours(args, rank, world, local):
             for i, k in enumerate(KERNELS):
                 ev[k].append((marks[i], marks[i + 1]))
 
+    accepted = None
+    if args.planted:
+        # the tree is a function of the drafter logits: build it once, then boost the
+        # target logit of the child token along a path of each request, with lengths drawn
+        # from a geometric distribution of mean `planted` (capped at the drafter depth)
+        c = r.cfg
+        ddt.ddt_build_tree(r.draft_logits, r.root_token, r.prefix_len, c["top_k"], c["budget"], out=r.tree,
+                           workspace=r.build_ws)
+        torch.cuda.synchronize()
+        rng = np.random.default_rng(7)
+        lens = np.minimum(rng.geometric(1.0 / (1.0 + args.planted), c["B"]) - 1, c["D"])
+        synth.plant_path(r.target_logits, r.tree["token"].cpu().numpy(), r.tree["parent"].cpu().numpy(),
+                         r.tree["n_nodes"].cpu().numpy(), lens)
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize()
+    if args.planted:
+        accepted = float(r.walk["acc_len"].float().mean())
     nodes_per_step = r.drafted_nodes()
     for k in ("status",):
         bad = int((r.tree[k] != 0).sum())
@@ -401,6 +416,9 @@ def run_ours(args, rank, world, local):
     }
     if args.flat:
         out["config"]["walk"] = "flat-commit safe mode (first children only)"
+    if args.planted:
+        out["config"]["acceptance"] = (f"planted paths, geometric lengths of mean {args.planted}; "
+                                       f"mean accepted drafted nodes {accepted:.2f}")
     if args.kv_page:
         out["config"]["kv"] = f"paged: {args.kv_page} rows a page, shuffled block table"
         out["roofline"]["traffic"] = None   # the recorded capture is of the contiguous layout
@@ -558,6 +576,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flat", action="store_true", help="flat-commit safe mode: walk first children only")
+    ap.add_argument("--planted", type=float, default=0.0,
+                    help="plant accepted paths with this mean length (0: random targets, little accepted)")
     ap.add_argument("--kv-page", type=int, default=0,
                     help="paged prefix caches with this many rows a page (0: contiguous)")
     args = ap.parse_args()
