@@ -304,11 +304,14 @@ def run_ours(args, rank, world, local):
         if bad:
             raise RuntimeError(f"build reported {bad} request errors")
 
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv")) if rank == 0 else None
-    if clocks and os.path.isdir(os.path.join(ROOT, "gpurun_out")):
+    # nvidia-smi samples during the timed region; the raw CSV goes to $DDT_CLOCKS_CSV when
+    # set, else to a temporary file, and its summary into the JSON line
+    clocks = None
+    if rank == 0:
+        import tempfile
+        path = os.environ.get("DDT_CLOCKS_CSV") or os.path.join(tempfile.gettempdir(), f"ddt_clocks_{os.getpid()}.csv")
+        clocks = ClockSampler(path)
         clocks.start()
-    elif clocks:
-        clocks = None
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)

@@ -1,6 +1,6 @@
 """Comparison helpers for the GPU-vs-oracle parity tests.
 
-Tolerance (spec bound of 2e-3 max relative error, read normwise): for every output
+Tolerance (2e-3 max relative error with fp32 accumulation, read normwise): for every output
 vector (one (layer, request, row, head) attention or GDN output, one (layer, request,
 head) GDN state matrix) max|gpu - oracle| / max|oracle| <= 2e-3, with the GPU writing
 fp32 outputs.  Integer outputs (tree arrays, masks, accepted rows, commit indices) must
