@@ -33,8 +33,8 @@ namespace {
 
 constexpr int kDK = 128, kDV = 128;  // head sizes of this path
 constexpr int kMD = 16;              // deepest tree this path takes (drafter depth <= 16)
-constexpr int kThr = 384;   // warps 0 TMA, 1 MMA, 2-3 setup only, 4-11 epilogue
-constexpr int kEpi = 256;   // epilogue threads
+constexpr int kThr = 384;   // 12 warps; lane 0 of warp 0 loads S0, lane 0 of warp 1 issues the MMAs
+constexpr int kEpi = kThr;  // epilogue threads: every warp
 constexpr int kMaxK = 8;    // widest short conv
 
 struct GdnTcParams {
@@ -444,50 +444,44 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     __syncthreads();
     tc::tc_fence_after();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ S0 loads
-        if (lane == 0) {
-            for (int hi = 1; hi < p.R; ++hi) {
-                if (!tc::mbar_wait(s_free, (hi - 1) & 1, abort_flag)) break;
-                tc::mbar_expect_tx(full, kDV * kDK * 4);
-                for (int blk = 0; blk < kDK / 32; ++blk)
-                    tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0 + hi * kDV);
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA
-        if (lane == 0) {
-            const uint32_t idesc = tc::idesc_tf32(128, p.NPAD, false, false);
-            const uint32_t sSa = tc::smem_u32(sS0), sKa = tc::smem_u32(sKQ);
-            for (int hi = 0; hi < p.R; ++hi) {
-                const int db = hi & 1;
-                if (!tc::mbar_wait(full, hi & 1, abort_flag)) break;
-                if (hi >= 2 && !tc::mbar_wait(d_free + db, ((hi - 2) >> 1) & 1, abort_flag)) break;
-                tc::tc_fence_after();
+    // ---- per value head, all 12 warps run the epilogue (each TMEM lane quarter has three
+    //      warps, which take alternate 16-node chunks).  Lane 0 of warp 0 loads the next
+    //      head's S0 once the MMA has read the current one; lane 0 of warp 1 issues the next
+    //      head's S0 . [k | q] MMA after the R pass, while the S0 load has long landed.
+    const uint32_t mma_idesc = tc::idesc_tf32(128, p.NPAD, false, false);
+    const uint32_t sSa = tc::smem_u32(sS0), sKa = tc::smem_u32(sKQ);
+    auto issue_mma = [&](int hi) {  // warp 1 lane 0: D[hi & 1] = S0 . [k | q]^T
+        const int db = hi & 1;
+        if (!tc::mbar_wait(full, hi & 1, abort_flag)) return;
+        if (hi >= 2 && !tc::mbar_wait(d_free + db, ((hi - 2) >> 1) & 1, abort_flag)) return;
+        tc::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kDK / 8; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * (kDV * 128) + (kk & 3) * 32;
-                    const uint32_t boff = (kk >> 2) * (p.NPAD * 128) + (kk & 3) * 32;
-                    tc::mma_tf32_ss(tmem + db * p.NPAD, tc::desc_sw128(sSa + aoff, 16, 1024),
-                                    tc::desc_sw128(sKa + boff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
-                }
-                tc::mma_commit(s_free);
-                tc::mma_commit(d_full + db);
-            }
-            tc::mma_commit(drain);
-            const long long t0 = clock64();
-            while (!tc::mbar_try(drain, 0) && clock64() - t0 < tc::kWaitCycles) {
-            }
+        for (int kk = 0; kk < kDK / 8; ++kk) {
+            const uint32_t aoff = (kk >> 2) * (kDV * 128) + (kk & 3) * 32;
+            const uint32_t boff = (kk >> 2) * (p.NPAD * 128) + (kk & 3) * 32;
+            tc::mma_tf32_ss(tmem + db * p.NPAD, tc::desc_sw128(sSa + aoff, 16, 1024),
+                            tc::desc_sw128(sKa + boff, 16, 1024), mma_idesc, kk > 0 ? 1u : 0u);
         }
-    } else if (warp >= 4) {
-        // --------------------------------------------------------------- epilogue (8 warps)
-        const int e = tid - 128;
+        tc::mma_commit(s_free);
+        tc::mma_commit(d_full + db);
+    };
+    if (warp == 1 && lane == 0) issue_mma(0);
+    __syncwarp();
+    {
+        // --------------------------------------------------------------- epilogue (12 warps)
+        const int e = tid;
         const int j = e & (kDV - 1);  // value channel = TMEM lane
-        const int quad = e >> 7;      // which half of the nodes
+        const int quad = e >> 7;      // which third of the node chunks
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         bool dead = false;
         for (int hi = 0; hi < p.R; ++hi) {
             const int h = g * p.R + hi, db = hi & 1;
+            if (warp == 0 && lane == 0 && hi + 1 < p.R && tc::mbar_wait(s_free, hi & 1, abort_flag)) {
+                tc::mbar_expect_tx(full, kDV * kDK * 4);  // S0 of the next head over the read one
+                for (int blk = 0; blk < kDK / 32; ++blk)
+                    tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0 + (hi + 1) * kDV);
+            }
+            __syncwarp();
             // gates of this head; per-node decay products and chain coefficients
             //   A(t, s_m) = b_t G(t, s_m) (k_s.k_t),  B(t, s_m) = G(t, s_m) (k_s.q_t)
             // stage this head's v channels of the node rows and conv-state rows (16-byte
@@ -564,7 +558,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
             // each thread takes whole 16-node chunks (its half's chunks alternate with the
             // other half's), so all 16 loaded columns are used and 16 nodes are in flight
-            for (int c = quad; c * 16 < nn; c += 2) {
+            for (int c = quad; c * 16 < nn; c += 3) {
                 const int t0 = c * 16;
                 uint32_t ks[16];
                 tmem_ld16(dcol + t0, ks);
@@ -594,9 +588,11 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 }
             }
             named_bar(1, kEpi);
+            if (warp == 1 && lane == 0 && hi + 1 < p.R) issue_mma(hi + 1);
+            __syncwarp();
             // pass C: outputs as independent sums over each node's own path; the 16 nodes of
             // a chunk advance one ancestor level at a time, so their loads overlap
-            for (int c = quad; c * 16 < N; c += 2) {
+            for (int c = quad; c * 16 < N; c += 3) {
                 const int t0 = c * 16;
                 uint32_t qs[16];
                 if (t0 < nn) {
@@ -635,6 +631,13 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             named_bar(1, kEpi);  // ubuf and the per-head arrays are rewritten by the next head
         }
     }
+    if (warp == 1 && lane == 0) {  // every MMA has completed before TMEM is freed
+        tc::mma_commit(drain);
+        const long long t0 = clock64();
+        while (!tc::mbar_try(drain, 0) && clock64() - t0 < tc::kWaitCycles) {
+        }
+    }
+    __syncwarp();
 
     tc::tc_fence_before();
     __syncthreads();
