@@ -108,6 +108,12 @@ __device__ __forceinline__ uint32_t sw_off(int row, int col, int rows) {
     return blk * (rows * 128) + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 3) * 4;
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     tc::tc_fence_after();
 
     // ---- per value head, all 12 warps run the epilogue (each TMEM lane quarter has three
-    //      warps, which take alternate 16-node chunks).  Lane 0 of warp 0 loads the next
+    //      warps, which take every third 8-node chunk).  Lane 0 of warp 0 loads the next
     //      head's S0 once the MMA has read the current one; lane 0 of warp 1 issues the next
     //      head's S0 . [k | q] MMA after the R pass, while the S0 load has long landed.
     const uint32_t mma_idesc = tc::idesc_tf32(128, p.NPAD, false, false);
@@ -556,15 +562,15 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             float wv[KT];
 #pragma unroll
             for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
-            // each thread takes whole 16-node chunks (its half's chunks alternate with the
-            // other half's), so all 16 loaded columns are used and 16 nodes are in flight
-            for (int c = quad; c * 16 < nn; c += 3) {
-                const int t0 = c * 16;
-                uint32_t ks[16];
-                tmem_ld16(dcol + t0, ks);
-                float vin[16][KT];
+            // each thread takes whole 8-node chunks (the three warps of a lane quarter take
+            // every third chunk), so every loaded column is used and 8 nodes are in flight
+            for (int c = quad; c * 8 < nn; c += 3) {
+                const int t0 = c * 8;
+                uint32_t ks[8];
+                tmem_ld8(dcol + t0, ks);
+                float vin[8][KT];
 #pragma unroll
-                for (int uu = 0; uu < 16; ++uu) {
+                for (int uu = 0; uu < 8; ++uu) {
                     const int t = min(t0 + uu, nn - 1);
                     if constexpr (KT == 4) {
                         const int4 r4 = *reinterpret_cast<const int4*>(trow + t * 4);
@@ -579,7 +585,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 }
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int uu = 0; uu < 16; ++uu) {
+                for (int uu = 0; uu < 8; ++uu) {
                     const int t = t0 + uu;
                     float acc = 0.f;
 #pragma unroll
@@ -590,20 +596,20 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             named_bar(1, kEpi);
             if (warp == 1 && lane == 0 && hi + 1 < p.R) issue_mma(hi + 1);
             __syncwarp();
-            // pass C: outputs as independent sums over each node's own path; the 16 nodes of
+            // pass C: outputs as independent sums over each node's own path; the 8 nodes of
             // a chunk advance one ancestor level at a time, so their loads overlap
-            for (int c = quad; c * 16 < N; c += 3) {
-                const int t0 = c * 16;
-                uint32_t qs[16];
+            for (int c = quad; c * 8 < N; c += 3) {
+                const int t0 = c * 8;
+                uint32_t qs[8];
                 if (t0 < nn) {
-                    tmem_ld16(dcol + p.QOFF + t0, qs);
+                    tmem_ld8(dcol + p.QOFF + t0, qs);
                     tc::tmem_wait_ld();
                 }
-                float ot[16];
-                int dp[16];
+                float ot[8];
+                int dp[8];
                 int md = 0;
 #pragma unroll
-                for (int uu = 0; uu < 16; ++uu) {
+                for (int uu = 0; uu < 8; ++uu) {
                     const int t = t0 + uu;
                     dp[uu] = 0;
                     ot[uu] = 0.f;
@@ -615,13 +621,13 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 }
                 for (int a = 0; a < md; ++a) {
 #pragma unroll
-                    for (int uu = 0; uu < 16; ++uu) {
+                    for (int uu = 0; uu < 8; ++uu) {
                         const int t = t0 + uu;
                         if (a < dp[uu]) ot[uu] = fmaf(scb[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot[uu]);
                     }
                 }
 #pragma unroll
-                for (int uu = 0; uu < 16; ++uu) {
+                for (int uu = 0; uu < 8; ++uu) {
                     const int t = t0 + uu;
                     if (t < N) obase[((long)t * p.Hv + h) * kDV + j] = from_f32<Tout>(ot[uu]);
                 }
