@@ -51,7 +51,7 @@ struct GdnTcParams {
 };
 
 struct GdnSmem {
-    size_t s0, kq, u, kk, qk, ca, cb, tt, tr, alist, small, sv, bars, total;
+    size_t s0, kq, u, sk, kk, qk, ca, cb, tr, alist, small, sv, bars, total;
 };
 
 // esz = bytes per input element (the staged v rows keep the input type)
@@ -71,6 +71,11 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     // R (one column per value channel), first used for the Gram rows [N][2N + 1]
     size_t ub = (size_t)N * (kDV > 2 * N + 1 ? kDV : 2 * N + 1) * 4;
     if (L.u + ub < L.s0 + kq_bytes) ub = L.s0 + kq_bytes - L.u;
+    // during the conv stage the k channels' input rows are staged past the low parts
+    L.sk = (L.s0 + kq_bytes > L.u ? L.s0 + kq_bytes - L.u : 0);
+    L.sk = L.u + ((L.sk + 15) & ~(size_t)15);
+    const size_t skb = (size_t)(N + K - 1) * kDK * esz;
+    if (L.u + ub < L.sk + skb) ub = L.sk + skb - L.u;
     off += (ub + 15) & ~(size_t)15;
     L.kk = off;
     off += (size_t)N * kMD * 4;
@@ -80,8 +85,6 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     off += (size_t)N * kMD * 4;
     L.cb = off;
     off += (size_t)N * kMD * 4;
-    L.tt = off;
-    off += (size_t)N * kMaxK * 8;            // conv input row pointers
     off = (off + 15) & ~(size_t)15;
     L.tr = off;                              // 16-byte aligned: four taps load as one int4
     off += (size_t)N * kMaxK * 4;            // conv input rows as staging-row indices
@@ -126,16 +129,16 @@ __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.syn
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
 
-// four consecutive input channels as floats (8-byte bf16 / 16-byte fp32 loads)
+// four consecutive channels of a staged row (shared memory) as floats
 __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
     v[0] = __uint_as_float(u.x << 16);
     v[1] = __uint_as_float(u.x & 0xffff0000u);
     v[2] = __uint_as_float(u.y << 16);
     v[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 __device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 a = *reinterpret_cast<const float4*>(p);
     v[0] = a.x;
     v[1] = a.y;
     v[2] = a.z;
@@ -167,7 +170,6 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     float* sqk = reinterpret_cast<float*>(base + lay.qk);
     float* sca = reinterpret_cast<float*>(base + lay.ca);
     float* scb = reinterpret_cast<float*>(base + lay.cb);
-    const Tin** taps = reinterpret_cast<const Tin**>(base + lay.tt);  // [N][K] conv input rows
     int* trow = reinterpret_cast<int*>(base + lay.tr);                // [N][K] the same rows in sv
     Tin* sv = reinterpret_cast<Tin*>(base + lay.sv);                  // [N + K - 1][kDV]
     int* alist = reinterpret_cast<int*>(base + lay.alist);
@@ -246,7 +248,6 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             for (int q = 0; q < K; ++q) {
                 const int back = K - 1 - q;
                 const int r = back == 0 ? n : (back <= d ? alist[n * kMD + back - 1] : N + (K - 1 - (back - d)));
-                taps[n * K + q] = r < N ? xb + (long)r * C : csb + (long)(r - N) * C;
                 trow[n * K + q] = r;
             }
         }
@@ -283,75 +284,81 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     const int srow0 = (int)((lb * p.Hv + (long)g * p.R) * kDV);
     if (tid == 0) tc::prefetch_tmap(&tm_s);
 
-    // ---- conv + SiLU + L2 norm of q and k: half-warp per (node, q|k); a lane takes channels
-    //      4 sub .. 4 sub + 3 and 64 + 4 sub .. 64 + 4 sub + 3 of its half, so that each
-    //      16-byte store of the swizzled tile is free of bank conflicts
+    // ---- conv + SiLU + L2 norm of q and k: the group's q and k channel rows of every node
+    //      and conv-state row are first copied into shared memory (16-byte cp.async, all in
+    //      flight together); then a warp takes a node and a lane four channels of q and of k,
+    //      so each norm is one warp reduction and each 16-byte store of the swizzled tile is
+    //      conflict-free
     {
-        const int half = lane >> 4, sub = lane & 15;
-        const int cb = (half == 0 ? g * kDK : p.Hk * kDK + g * kDK);
-        const int cA = cb + 4 * sub, cB = cb + 64 + 4 * sub;
-        float w[8][KT];
+        constexpr int kVec = kDK * (int)sizeof(Tin) / 16;
+        const int c4 = 4 * lane;
+        Tin* sk = reinterpret_cast<Tin*>(base + lay.sk);  // [N + K - 1][kDK], like sv
+        const int cbq = g * kDK, cbk = (p.Hk + g) * kDK;
+        for (int i = tid; i < 2 * (nn + K - 1) * kVec; i += kThr) {
+            const int part = i & 1, r = (i >> 1) / kVec, c = (i >> 1) % kVec;
+            const Tin* src = (r < nn ? xb + (long)r * C : csb + (long)(r - nn) * C) + (part ? cbk : cbq) +
+                             c * (16 / (int)sizeof(Tin));
+            const int rs = r < nn ? r : N + (r - nn);
+            cp_async16(reinterpret_cast<unsigned char*>((part ? sk : sv) + (long)rs * kDK) + c * 16, src);
+        }
+        cp_async_commit();
+        float w[2][4][KT];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
-            for (int q = 0; q < KT; ++q)
-                w[ch][q] = (q < K) ? to_f32(wl[(long)(ch < 4 ? cA + ch : cB + ch - 4) * K + q]) : 0.f;
-        // two nodes per pass, so their loads are in flight together
-        constexpr int kW = kThr / 32;
-        for (int n0 = warp; n0 < N; n0 += 2 * kW) {
-            float yy[2][8];
+            for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-                const int nc = min(n0 + s2 * kW, nn - 1);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) yy[s2][ch] = 0.f;
+                for (int q = 0; q < KT; ++q)
+                    w[part][ch][q] = (q < K) ? to_f32(wl[(long)((part ? cbk : cbq) + c4 + ch) * K + q]) : 0.f;
+        cp_async_wait_all();
+        __syncthreads();
+        for (int n = warp; n < N; n += kThr / 32) {
+            float y[2][4] = {};
+            if (n < nn) {
 #pragma unroll
                 for (int q = 0; q < KT; ++q) {
                     if (q < K) {
-                        float ia[4], ib[4];
-                        load4(taps[nc * K + q] + cA, ia);
-                        load4(taps[nc * K + q] + cB, ib);
+                        const int rs = trow[n * K + q];
+                        float in[2][4];
+                        load4(sv + (long)rs * kDK + c4, in[0]);
+                        load4(sk + (long)rs * kDK + c4, in[1]);
 #pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) {
-                            yy[s2][ch] = fmaf(w[ch][q], ia[ch], yy[s2][ch]);
-                            yy[s2][ch + 4] = fmaf(w[ch + 4][q], ib[ch], yy[s2][ch + 4]);
-                        }
+                        for (int part = 0; part < 2; ++part)
+#pragma unroll
+                            for (int ch = 0; ch < 4; ++ch) y[part][ch] = fmaf(w[part][ch][q], in[part][ch], y[part][ch]);
                     }
                 }
-            }
+                float ss[2] = {0.f, 0.f};
 #pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-            const int n = n0 + s2 * kW;
-            if (n >= N) break;
-            float y[8];
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) y[ch] = 0.f;
-            if (n < nn) {
-                float ss = 0.f;
+                    for (int ch = 0; ch < 4; ++ch) {
+                        y[part][ch] = silu_g(y[part][ch]);
+                        ss[part] = fmaf(y[part][ch], y[part][ch], ss[part]);
+                    }
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    y[ch] = silu_g(yy[s2][ch]);
-                    ss = fmaf(y[ch], y[ch], ss);
+                for (int o = 16; o > 0; o >>= 1) {
+                    ss[0] += __shfl_xor_sync(kFull, ss[0], o);
+                    ss[1] += __shfl_xor_sync(kFull, ss[1], o);
                 }
+                const float sc[2] = {rsqrtf(ss[0] + 1e-6f) * rsqrtf((float)kDK), rsqrtf(ss[1] + 1e-6f)};
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-                const float sc = rsqrtf(ss + 1e-6f) * (half == 0 ? rsqrtf((float)kDK) : 1.f);
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) y[ch] *= sc;
+                    for (int ch = 0; ch < 4; ++ch) y[part][ch] *= sc[part];
             }
-            const int row = half == 0 ? p.QOFF + n : n;
-            // y = hi + lo, hi rounded to tf32: the dense MMAs read hi, the Gram reads both
-            float lo[8];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const float hv = tc::tf32_rn(y[ch]);
-                lo[ch] = y[ch] - hv;
-                y[ch] = hv;
-            }
-            *reinterpret_cast<float4*>(sKQ + sw_off(row, 4 * sub, p.NPAD)) = make_float4(y[0], y[1], y[2], y[3]);
-            *reinterpret_cast<float4*>(sKQ + sw_off(row, 64 + 4 * sub, p.NPAD)) = make_float4(y[4], y[5], y[6], y[7]);
-            *reinterpret_cast<float4*>(sLO + sw_off(row, 4 * sub, p.NPAD)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<float4*>(sLO + sw_off(row, 64 + 4 * sub, p.NPAD)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
+            for (int part = 0; part < 2; ++part) {
+                const int row = part == 0 ? p.QOFF + n : n;
+                // y = hi + lo, hi rounded to tf32: the dense MMAs read hi, the Gram reads both
+                float hv[4], lo[4];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    hv[ch] = tc::tf32_rn(y[part][ch]);
+                    lo[ch] = y[part][ch] - hv[ch];
+                }
+                *reinterpret_cast<float4*>(sKQ + sw_off(row, c4, p.NPAD)) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<float4*>(sLO + sw_off(row, c4, p.NPAD)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         // padding rows of the tile
