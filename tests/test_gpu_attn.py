@@ -107,3 +107,19 @@ def test_attn_bf16_split_kv_and_big_tree():
     r = _gpu(tree, inp)
     _check(r["o"], _oracle(tree, inp, 128), tree)
     assert r["status"].cpu().tolist() == [0, 0]
+
+
+def test_attn_bf16_values_past_fp16_range():
+    """V values far past fp16's range (prefix keys, the last row of a shifted prefix
+    tile, a tree key) are applied at bf16 precision like any other."""
+    tree, inp, N = _case(3, 2, 2, 24, 4, 256, [300, 130], 64, torch.bfloat16)
+    vc = inp.v_cache.float()
+    vc[0, 0, 1, 70:72] *= 3e5      # one prefix tile of request 0, kv head 1
+    vc[1, 1, 2, 129] = 7e4         # the last prefix row of request 1 (a shifted tile)
+    inp.v_cache = vc.to(torch.bfloat16)
+    vt = inp.v_tree.float()
+    vt[1, 0, 3, 0] = -2e5          # a tree key of request 0, kv head 0
+    inp.v_tree = vt.to(torch.bfloat16)
+    r = _gpu(tree, inp)
+    _check(r["o"], _oracle(tree, inp, 256), tree)
+    assert r["status"].cpu().tolist() == [0, 0]
