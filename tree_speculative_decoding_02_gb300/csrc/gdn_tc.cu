@@ -487,8 +487,19 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
         const int quad = e >> 7;      // which third of the node chunks
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         bool dead = false;
+        // gates of the head after the current one are loaded a head ahead (registers)
+        float dec_nx = 0.f, beta_nx = 0.f;
+        if (e < nn) {
+            dec_nx = p.decay[(lb * N + e) * p.Hv + g * p.R];
+            beta_nx = p.beta[(lb * N + e) * p.Hv + g * p.R];
+        }
         for (int hi = 0; hi < p.R; ++hi) {
             const int h = g * p.R + hi, db = hi & 1;
+            // conv weights of this head's v channel (used by the R pass)
+            const int cv = 2 * p.Hk * kDK + h * kDV + j;
+            float wv[KT];
+#pragma unroll
+            for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
             if (warp == 0 && lane == 0 && hi + 1 < p.R && tc::mbar_wait(s_free, hi & 1, abort_flag)) {
                 tc::mbar_expect_tx(full, kDV * kDK * 4);  // S0 of the next head over the read one
                 for (int blk = 0; blk < kDK / 32; ++blk)
@@ -511,8 +522,12 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 cp_async_commit();
             }
             if (e < nn) {
-                sdec[e] = p.decay[(lb * N + e) * p.Hv + h];
-                sbeta[e] = p.beta[(lb * N + e) * p.Hv + h];
+                sdec[e] = dec_nx;
+                sbeta[e] = beta_nx;
+                if (hi + 1 < p.R) {
+                    dec_nx = p.decay[(lb * N + e) * p.Hv + h + 1];
+                    beta_nx = p.beta[(lb * N + e) * p.Hv + h + 1];
+                }
             }
             named_bar(1, kEpi);
             if (e < nn) {
@@ -565,10 +580,6 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             tc::tc_fence_after();
             const uint32_t dcol = tmem + lane_base + db * p.NPAD;
             // pass A: R_t = b_t (v_t - g_t (S0 k_t)); v_t by the conv along the node's path
-            const int cv = 2 * p.Hk * kDK + h * kDV + j;
-            float wv[KT];
-#pragma unroll
-            for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
             // each thread takes whole 8-node chunks (the three warps of a lane quarter take
             // every third chunk), so every loaded column is used and 8 nodes are in flight
             for (int c = quad; c * 8 < nn; c += 3) {
