@@ -88,11 +88,11 @@ __global__ void k_commit_kv(int B, int N, int A, int Hkv, int d, int Pcap, int v
 
 __device__ __forceinline__ float silu_c(float z) { return z / (1.f + __expf(-z)); }
 
-// One CTA per (value head, request, layer), 2 threads per state row (DV rows): the state
-// lives in registers, DK/2 entries a thread.  Prologue: conv + SiLU of the k and v
+// One CTA per (value head, request, layer), 2 threads per state row on average (DV rows):
+// the state lives in registers, DK/2 entries a thread.  Prologue: conv + SiLU of the k and v
 // channels of every accepted node (all loads in flight together), k norms and gates into
-// shared memory.  Then the a + 1 delta steps need no barrier: each row's S k is a pair
-// of partial dots joined by one shuffle, and the rank-one update is in registers.
+// shared memory.  Then the a + 1 delta steps need no barrier: each row's S k is eight
+// partial dots joined by three shuffles, and the rank-one update is in registers.
 template <typename Tx, int DK, int DV>
 __global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, int Hk, int Hv, int K, int cap_check,
                                                        int Pcap, const Tx* __restrict__ x,
@@ -150,19 +150,26 @@ __global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, i
         s_g[2 * t + 1] = beta[(lb * N + path[t]) * Hv + h];
     }
     __syncthreads();
-    // the state rows (their loads overlap the k normalisation): row j = tid / 2,
-    // columns 8m + 4 (tid & 1) .. + 3 for m < DK / 8
-    const int j = tid >> 1, hf = tid & 1;
+    // the state rows (their loads overlap the k normalisation).  A warp holds 16 rows; the
+    // eight lanes of row group rg = lane / 8 share rows 16 warp + rg + 4 i (i < 4) and lane
+    // sub = lane % 8 takes 16-byte chunks sub + 8 m of each, so every load or store of the
+    // warp covers four whole 128-byte row segments
+    static_assert(DK % 32 == 0 && DV % 16 == 0, "state tile: 8 lanes x 16-byte chunks per row, 16 rows a warp");
+    constexpr int kC = DK / 32;  // chunks a lane takes per row
+    const int sub = lane & 7, rg = lane >> 3;
     float* Sg = S + (lb * Hv + h) * (long)DV * DK;
     float sr[kH];
 #pragma unroll
-    for (int m = 0; m < DK / 8; ++m) {
-        const float4 v4 = *reinterpret_cast<const float4*>(Sg + (long)j * DK + 8 * m + 4 * hf);
-        sr[4 * m] = v4.x;
-        sr[4 * m + 1] = v4.y;
-        sr[4 * m + 2] = v4.z;
-        sr[4 * m + 3] = v4.w;
-    }
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < kC; ++m) {
+            const float4 v4 =
+                *reinterpret_cast<const float4*>(Sg + (long)(16 * warp + rg + 4 * i) * DK + 4 * (sub + 8 * m));
+            sr[(i * kC + m) * 4] = v4.x;
+            sr[(i * kC + m) * 4 + 1] = v4.y;
+            sr[(i * kC + m) * 4 + 2] = v4.z;
+            sr[(i * kC + m) * 4 + 3] = v4.w;
+        }
 
     // k normalisation: one warp per node
     for (int t = warp; t <= a; t += kT / 32) {
@@ -178,31 +185,35 @@ __global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, i
     for (int t = 0; t <= a; ++t) {
         const float* kt = s_k + t * DK;
         const float at = s_g[2 * t], bt = s_g[2 * t + 1];
-        float part = 0.f;
+        float kv[kC * 4];
 #pragma unroll
-        for (int m = 0; m < DK / 8; ++m) {
-            const float4 k4 = *reinterpret_cast<const float4*>(kt + 8 * m + 4 * hf);
-            part = fmaf(sr[4 * m], k4.x, part);
-            part = fmaf(sr[4 * m + 1], k4.y, part);
-            part = fmaf(sr[4 * m + 2], k4.z, part);
-            part = fmaf(sr[4 * m + 3], k4.w, part);
+        for (int m = 0; m < kC; ++m) {
+            const float4 k4 = *reinterpret_cast<const float4*>(kt + 4 * (sub + 8 * m));
+            kv[4 * m] = k4.x;
+            kv[4 * m + 1] = k4.y;
+            kv[4 * m + 2] = k4.z;
+            kv[4 * m + 3] = k4.w;
         }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        const float u = bt * (s_v[t * DV + j] - at * part);   // u = b (v - a S k^)
-        __syncwarp();  // re-read k below rather than keep DK/2 more values live
 #pragma unroll
-        for (int m = 0; m < DK / 8; ++m) {                     // S <- a S + u k^T
-            const float4 k4 = *reinterpret_cast<const float4*>(kt + 8 * m + 4 * hf);
-            sr[4 * m] = fmaf(at, sr[4 * m], u * k4.x);
-            sr[4 * m + 1] = fmaf(at, sr[4 * m + 1], u * k4.y);
-            sr[4 * m + 2] = fmaf(at, sr[4 * m + 2], u * k4.z);
-            sr[4 * m + 3] = fmaf(at, sr[4 * m + 3], u * k4.w);
+        for (int i = 0; i < 4; ++i) {
+            float part = 0.f;
+#pragma unroll
+            for (int c = 0; c < kC * 4; ++c) part = fmaf(sr[i * kC * 4 + c], kv[c], part);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            part += __shfl_xor_sync(0xffffffffu, part, 4);
+            const float u = bt * (s_v[t * DV + 16 * warp + rg + 4 * i] - at * part);  // u = b (v - a S k^)
+#pragma unroll
+            for (int c = 0; c < kC * 4; ++c) sr[i * kC * 4 + c] = fmaf(at, sr[i * kC * 4 + c], u * kv[c]);  // S <- a S + u k^T
         }
     }
 #pragma unroll
-    for (int m = 0; m < DK / 8; ++m)
-        *reinterpret_cast<float4*>(Sg + (long)j * DK + 8 * m + 4 * hf) =
-            make_float4(sr[4 * m], sr[4 * m + 1], sr[4 * m + 2], sr[4 * m + 3]);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < kC; ++m)
+            *reinterpret_cast<float4*>(Sg + (long)(16 * warp + rg + 4 * i) * DK + 4 * (sub + 8 * m)) =
+                make_float4(sr[(i * kC + m) * 4], sr[(i * kC + m) * 4 + 1], sr[(i * kC + m) * 4 + 2],
+                            sr[(i * kC + m) * 4 + 3]);
 }
 
 template <typename Tx>
