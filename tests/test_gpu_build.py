@@ -90,3 +90,13 @@ def test_build_nonfinite_logits_flagged():
     out = _run(logits, [0, 0], [0, 0], 4, 8)
     assert out["status"][0] == 0 and out["status"][1] == 6
     assert out["n_nodes"][1] == 1
+
+
+@pytest.mark.parametrize("k", [1, 8, 32])
+def test_build_many_ties_wide_vocab(k):
+    """Integer-valued logits over a 20000-token vocabulary (three chunks, the last one
+    ragged): thousands of exact ties in every chunk, so the lowest-id rule decides which
+    entries make each top k."""
+    rng = np.random.default_rng(40 + k)
+    logits = torch.as_tensor(rng.integers(-2, 3, size=(2, 5, 20000)).astype(np.float32)).to(torch.bfloat16)
+    _compare(logits, [1, 2], [10, 20], k, 40)

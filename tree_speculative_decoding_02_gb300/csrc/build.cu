@@ -10,7 +10,8 @@
 // GB300 layout of the work:
 //   k_build_partial  grid (chunks, D, B): one HBM pass over the logits.  Each CTA
 //                    reduces one 8192-token chunk of one depth row to (max, sum of
-//                    exp(v - max), top-k list) with warp-parallel sorted insertion.
+//                    exp(v - max), top-k list): a threshold from the lane bests, one
+//                    bitonic sort per warp, bitonic merges of the warp lists.
 //   k_build_tree     grid B: per request, warp-per-depth merge of the chunk partials
 //                    (LSE and top-k), then one warp runs the best-first selection over a
 //                    shared-memory frontier, then the CTA renumbers breadth first and
@@ -85,23 +86,79 @@ __global__ void __launch_bounds__(256, 4) k_build_partial(const T* __restrict__ 
             if (e < len && !finite_f32(v[j * 8 + u])) bad = 1;
         }
 
-    // warp top-k over the thread's candidates
-    WarpTopK tk;
-    tk.init(k);
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
-        tk.insert(e < len ? v[j] : vid_empty().v, e < len ? start + e : 0x7fffffff);
-    }
-
+    // warp top-k.  The k-th best of the 32 lane bests is beaten or equalled by at least k
+    // entries, so every entry of the warp's top k is at or above it: only those entries
+    // are kept.  When at most 32 qualify (the usual case) they are sorted in one bitonic
+    // pass; otherwise they are inserted one at a time.
     __shared__ float s_v[8][32];
     __shared__ int s_id[8][32];
     __shared__ float s_max[8];
     __shared__ double s_sum[8];
     __shared__ int s_bad[8];
-    s_v[warp][lane] = tk.v;
-    s_id[warp][lane] = tk.id;
-    const float wmax = __shfl_sync(kFull, tk.v, 0);
+    const VId emp = vid_empty();
+    float bv = emp.v;
+    int bid = emp.id;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
+        if (e < len && beats(v[j], start + e, bv, bid)) {
+            bv = v[j];
+            bid = start + e;
+        }
+    }
+    warp_sort_best_first(bv, bid);
+    const float thv = __shfl_sync(kFull, bv, k - 1);
+    const int thid = __shfl_sync(kFull, bid, k - 1);
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
+        cnt += (e < len && !beats(thv, thid, v[j], start + e)) ? 1 : 0;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int nb = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += nb;
+    }
+    const int total = __shfl_sync(kFull, incl, 31);
+    float wv;
+    int wid;
+    if (total <= 32) {
+        int pos = incl - cnt;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
+            if (e < len && !beats(thv, thid, v[j], start + e)) {
+                s_v[warp][pos] = v[j];
+                s_id[warp][pos] = start + e;
+                ++pos;
+            }
+        }
+        __syncwarp();
+        wv = lane < total ? s_v[warp][lane] : emp.v;
+        wid = lane < total ? s_id[warp][lane] : emp.id;
+        warp_sort_best_first(wv, wid);
+    } else {
+        WarpTopK tk;
+        tk.init(k);
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
+            const bool q = e < len && !beats(thv, thid, v[j], start + e);
+            if (__any_sync(kFull, q)) tk.insert(q ? v[j] : emp.v, q ? start + e : emp.id);
+        }
+        wv = tk.v;
+        wid = tk.id;
+    }
+    if (lane >= k) {
+        wv = emp.v;
+        wid = emp.id;
+    }
+    __syncwarp();
+    s_v[warp][lane] = wv;
+    s_id[warp][lane] = wid;
+    const float wmax = __shfl_sync(kFull, wv, 0);
     if (lane == 0) s_max[warp] = wmax;
     const int wbad = __any_sync(kFull, bad);
     if (lane == 0) s_bad[warp] = wbad;
@@ -129,13 +186,13 @@ __global__ void __launch_bounds__(256, 4) k_build_partial(const T* __restrict__ 
     // merge the eight warp lists in warp 0
     __syncthreads();
     if (warp == 0) {
-        WarpTopK fin;
-        fin.init(k);
-        for (int w = 0; w < 8; ++w) fin.insert(s_v[w][lane], s_id[w][lane]);
+        float fv = s_v[0][lane];
+        int fid = s_id[0][lane];
+        for (int w = 1; w < 8; ++w) warp_merge_best_first(fv, fid, s_v[w][lane], s_id[w][lane]);
         const long p = ((long)b * D + d) * nch + c;
         if (lane < k) {
-            pv[p * k + lane] = fin.v;
-            pid[p * k + lane] = fin.id;
+            pv[p * k + lane] = fv;
+            pid[p * k + lane] = fid;
         }
         if (lane == 0) {
             double tot = 0.0;

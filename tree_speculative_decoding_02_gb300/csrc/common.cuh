@@ -126,6 +126,40 @@ struct WarpTopK {
     }
 };
 
+// Bitonic networks over one (value, id) entry per lane, best first in the beats order.
+// cmpx: exchange with lane ^ stride and keep the better (or the worse) of the pair.
+__device__ __forceinline__ void cmpx(float& v, int& id, int stride, bool keep_better) {
+    const float ov = __shfl_xor_sync(kFull, v, stride);
+    const int oid = __shfl_xor_sync(kFull, id, stride);
+    if (beats(ov, oid, v, id) == keep_better) {
+        v = ov;
+        id = oid;
+    }
+}
+// sorts the warp's 32 entries, best in lane 0
+__device__ __forceinline__ void warp_sort_best_first(float& v, int& id) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+            cmpx(v, id, stride, ((lane & stride) == 0) == ((lane & size) == 0));
+}
+// (v, id) and (bv, bid) each sorted best first across the warp: leaves the best 32 of
+// their union in (v, id), sorted (the lane-wise better of one list and the other one
+// reversed is bitonic and holds the best 32; a half-cleaner cascade sorts it)
+__device__ __forceinline__ void warp_merge_best_first(float& v, int& id, float bv, int bid) {
+    const int lane = threadIdx.x & 31;
+    const float rv = __shfl_sync(kFull, bv, 31 - lane);
+    const int rid = __shfl_sync(kFull, bid, 31 - lane);
+    if (beats(rv, rid, v, id)) {
+        v = rv;
+        id = rid;
+    }
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) cmpx(v, id, stride, (lane & stride) == 0);
+}
+
 // ------------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
