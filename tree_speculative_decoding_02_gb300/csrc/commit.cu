@@ -217,10 +217,10 @@ __global__ void __launch_bounds__(2 * DV, 2) k_commit_gdn(int B, int N, int A, i
 }
 
 template <typename Tx>
-__global__ void k_commit_conv(int B, int N, int A, int C, int K, int cap_check, int Pcap, const Tx* __restrict__ x,
-                              Tx* __restrict__ conv_state, const int32_t* __restrict__ acc_nodes,
-                              const int32_t* __restrict__ acc_len, const int32_t* __restrict__ prefix_len,
-                              const KvPages pg) {
+__global__ void k_commit_conv(int B, int N, int A, int C, int K, int cap_check, int Pcap, int vec,
+                              const Tx* __restrict__ x, Tx* __restrict__ conv_state,
+                              const int32_t* __restrict__ acc_nodes, const int32_t* __restrict__ acc_len,
+                              const int32_t* __restrict__ prefix_len, const KvPages pg) {
     const int l = blockIdx.x, b = blockIdx.y;
     __shared__ int s_ok;
     if (threadIdx.x == 0) s_ok = commit_check(b, N, A, cap_check, Pcap, acc_nodes, acc_len, prefix_len, pg) == DDT_OK;
@@ -231,12 +231,22 @@ __global__ void k_commit_conv(int B, int N, int A, int C, int K, int cap_check, 
     Tx* cs = conv_state + lb * (K - 1) * C;
     const Tx* xb = x + lb * N * C;
     const int32_t* path = acc_nodes + (long)b * A;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        // new row r = entry r + n of [cs ; path rows]; rows read before they are rewritten
-        for (int r = 0; r < K - 1; ++r) {
-            const int src = r + n;
-            cs[(long)r * C + c] = (src < K - 1) ? cs[(long)src * C + c] : xb[(long)path[src - (K - 1)] * C + c];
-        }
+    // new row r = entry r + n of [cs ; path rows]; each element is read before it is
+    // rewritten (r + n > r, and one thread owns a column chunk across all rows)
+    if (vec) {  // 16-byte chunks of a row
+        const int nc = C * (int)sizeof(Tx) / 16;
+        for (int q = threadIdx.x; q < nc; q += blockDim.x)
+            for (int r = 0; r < K - 1; ++r) {
+                const int src = r + n;
+                const Tx* from = (src < K - 1) ? cs + (long)src * C : xb + (long)path[src - (K - 1)] * C;
+                reinterpret_cast<uint4*>(cs + (long)r * C)[q] = reinterpret_cast<const uint4*>(from)[q];
+            }
+    } else {
+        for (int c = threadIdx.x; c < C; c += blockDim.x)
+            for (int r = 0; r < K - 1; ++r) {
+                const int src = r + n;
+                cs[(long)r * C + c] = (src < K - 1) ? cs[(long)src * C + c] : xb[(long)path[src - (K - 1)] * C + c];
+            }
     }
 }
 
@@ -321,20 +331,22 @@ cudaError_t launch_commit(int B, int N, int A, int La, int Hkv, int d, int Pcap,
     }
     if (Lg > 0) {
         const int C = 2 * Hk * dk + Hv * dv;
+        const int cvec = ((C * (x_dtype == DDT_BF16 ? 2 : 4)) % 16 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                         (reinterpret_cast<uintptr_t>(conv_state) % 16 == 0);
         if (x_dtype == DDT_BF16) {
             e = commit_gdn_dims<__nv_bfloat16>(dk, dv, B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, conv_w, conv_state, beta,
                                                decay, S, acc_nodes, acc_len, prefix_len, pg, st);
             if (e != cudaSuccess) return e;
             if (K > 1)
                 k_commit_conv<__nv_bfloat16><<<counted(dim3(Lg, B)), 256, 0, st>>>(
-                    B, N, A, C, K, cap, Pcap, static_cast<const __nv_bfloat16*>(x),
+                    B, N, A, C, K, cap, Pcap, cvec, static_cast<const __nv_bfloat16*>(x),
                     static_cast<__nv_bfloat16*>(conv_state), acc_nodes, acc_len, prefix_len, pg);
         } else {
             e = commit_gdn_dims<float>(dk, dv, B, N, A, Lg, Hk, Hv, K, cap, Pcap, x, conv_w, conv_state, beta, decay,
                                        S, acc_nodes, acc_len, prefix_len, pg, st);
             if (e != cudaSuccess) return e;
             if (K > 1)
-                k_commit_conv<float><<<counted(dim3(Lg, B)), 256, 0, st>>>(B, N, A, C, K, cap, Pcap, static_cast<const float*>(x),
+                k_commit_conv<float><<<counted(dim3(Lg, B)), 256, 0, st>>>(B, N, A, C, K, cap, Pcap, cvec, static_cast<const float*>(x),
                                                                   static_cast<float*>(conv_state), acc_nodes, acc_len,
                                                                   prefix_len, pg);
         }

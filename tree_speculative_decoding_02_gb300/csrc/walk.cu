@@ -7,13 +7,16 @@
 // target's bonus token is emitted but must not be fed back as an accepted draft.
 //
 //   k_walk_argmax   grid (chunks, N, B): one HBM pass over the target logits; each CTA
-//                   reduces an 8192-token chunk of one row to (max, lowest argmax id).
+//                   reduces a 16384-token chunk of one row to (max, lowest argmax id).
 //   k_walk_descend  grid B: warp-per-row merge of the chunk partials, tree check, then
 //                   one warp walks down with a ballot over the rows per step.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace ddt {
+
+// vocabulary entries one argmax CTA reduces (eight 16-byte loads a thread in flight)
+constexpr int kWalkChunk = 16384;
 
 struct ArgPartial {
     float v;
@@ -23,7 +26,7 @@ struct ArgPartial {
 };
 
 size_t walk_ws_bytes(int B, int N, int V) {
-    const long nch = (V + kBuildChunk - 1) / kBuildChunk;
+    const long nch = (V + kWalkChunk - 1) / kWalkChunk;
     return (((size_t)B * N * nch * sizeof(ArgPartial)) + 255) & ~(size_t)255;
 }
 
@@ -36,13 +39,13 @@ __global__ void __launch_bounds__(256) k_walk_argmax(const T* __restrict__ logit
     if (i >= nn || nn > N) return;  // rows past the tree are not needed
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long row = ((long)b * N + i) * V;
-    const int start = c * kBuildChunk;
-    const int len = min(kBuildChunk, V - start);
+    const int start = c * kWalkChunk;
+    const int len = min(kWalkChunk, V - start);
     float bv = vid_empty().v;
     int bid = 0x7fffffff;
     int bad = 0;
 #pragma unroll
-    for (int j = 0; j < kBuildChunk / 2048; ++j) {
+    for (int j = 0; j < kWalkChunk / 2048; ++j) {
         const int e = tid * 8 + j * 2048;
         float t8[8];
         if (vec && e + 8 <= len) {
@@ -216,7 +219,7 @@ cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void*
                         const int32_t* token, const int32_t* parent, const int32_t* n_nodes, int32_t* acc_nodes,
                         int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted, int32_t* status,
                         void* ws, int flat, cudaStream_t st) {
-    const int nch = (V + kBuildChunk - 1) / kBuildChunk;
+    const int nch = (V + kWalkChunk - 1) / kWalkChunk;
     ArgPartial* part = static_cast<ArgPartial*>(ws);
     if (logits) {
         dim3 g(nch, N, B);
