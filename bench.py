@@ -169,8 +169,9 @@ def round_bytes(r):
 # keyed by the SHA-256 of the kernel's sources: once they change, the figure is stale
 # and the bench reports null until it is captured again.
 ATTN_TRAFFIC = {
-    # ncu: dram__bytes_read.sum 40,360,228,608 B + dram__bytes_write.sum 403,364,864 B, batched round
-    "d92a3bf06d730f88590e5bd9a119a869878c9e9d91dbd15859e35960e42260b8": {"workload": 5, "bytes": 40763593472.0},
+    # ncu, batched round, mean of the three timed launches of one capture:
+    # dram__bytes_read.sum 40,355,525,803 B + dram__bytes_write.sum 399,649,707 B
+    "b254561bfd1e7a475760cfc72bb81d6f27dedd9495a1746ae329695fa4f863f7": {"workload": 5, "bytes": 40755175509.0},
 }
 ATTN_SOURCES = ("attn_tc.cu", "tc.cuh")
 

@@ -10,8 +10,8 @@
 // query rows (row = node * G + head-in-group, G = Hq/Hkv, so the whole GQA group shares
 // one K/V stream), and a chunk of the prefix.  The chunk holding the prefix's end also
 // takes the tree rows as keys.  Keys stream in tiles of 64:
-//   warp 0      TMA producer: K and V tiles into a 4-stage shared-memory ring (128-byte
-//               swizzle).  Prefix tiles come from a 3-D map (d, position, layer*B*Hkv);
+//   warp 0      TMA producer: K and V tiles into a shared-memory ring of 6 (d = 256) or
+//               8 stages (128-byte swizzle).  Prefix tiles come from a 3-D map (d, position, layer*B*Hkv);
 //               the ragged last tile is shifted to end exactly at prefix_len, so no row
 //               past the prefix is ever read (positions < 0 are zero-filled by TMA).
 //               Tree tiles come from a 4-D map (d, kv head, node, layer*B).
@@ -19,8 +19,9 @@
 //               kept in TMEM); O += P_j V_j with P_j read back from TMEM (written over S_j)
 //               and V_j MN-major in shared memory.  P_j is stored as two bf16 parts,
 //               P = P_hi + P_lo, and both are applied (two MMAs): bf16 P alone would leave
-//               ~3e-3 relative error in O, the pair ~1e-5.  The tensor core has the time:
-//               this kernel is bound by the softmax and data movement, not the MMAs.
+//               ~3e-3 relative error in O, the pair ~1e-5.  This thread bounds the kernel:
+//               a 64-key tile is 16 QK MMAs of N = 64 (which run at about half the tensor
+//               rate) and 8 P.V MMAs of N = 256, and the softmax keeps ahead of it.
 //   warps 4-11  softmax: two warpgroups per row set, each taking half of every S tile's
 //               columns and half of O's; ancestor mask on tree tiles, running max with
 //               lazy O rescaling (only when the max grows by more than 2^8); zeroes V rows
