@@ -84,14 +84,14 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     L.ca = off;
     off += (size_t)N * kMD * 4;
     L.cb = off;
-    off += (size_t)N * kMD * 4;
+    off += (size_t)2 * N * kMD * 4;          // two heads' buffers
     off = (off + 15) & ~(size_t)15;
     L.tr = off;                              // 16-byte aligned: four taps load as one int4
     off += (size_t)N * kMaxK * 4;            // conv input rows as staging-row indices
     L.alist = off;
     off += (size_t)N * kMD * 4;
     L.small = off;
-    off += (size_t)N * 4 * 7;                // dep, par, qself, gcum, beta, decay, spare
+    off += (size_t)N * 4 * 9;                // dep, par, qself, gcum[2], beta[2], decay[2]
     off = (off + 15) & ~(size_t)15;
     L.sv = off;                              // one value head's v channels: node rows, then conv-state rows
     off += (size_t)(N + K - 1) * kDV * esz;
@@ -176,9 +176,9 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     int* sdep = reinterpret_cast<int*>(base + lay.small);
     int* spar = sdep + N;
     float* sqself = reinterpret_cast<float*>(spar + N);
-    float* sg = sqself + N;
-    float* sbeta = sg + N;
-    float* sdec = sbeta + N;
+    float* sg = sqself + N;     // [2][N] (two heads' buffers, as sbeta, sdec and scb)
+    float* sbeta = sg + 2 * N;
+    float* sdec = sbeta + 2 * N;
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + lay.bars);
     uint64_t* full = bars;        // S0 landed
     uint64_t* s_free = bars + 1;  // MMA done reading S0
@@ -487,73 +487,73 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
         const int quad = e >> 7;      // which third of the node chunks
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         bool dead = false;
-        // gates of the head after the current one are loaded a head ahead (registers)
+        // Per-head arrays come in two buffers (head hi uses buffer hi & 1), so that the
+        // gates, chain coefficients and back substitution of head hi + 1 overlap the R and
+        // output passes of head hi: two barriers a head.
+        //   top of head hi:  back substitution (hi); R pass (hi); gates (hi + 1)
+        //   barrier 1:       R rows, M rows (hi) and gates (hi + 1) visible; v rows free
+        //                    v rows (hi + 1) staged; chain coefficients (hi + 1); output
+        //                    pass (hi)
+        //   barrier 2:       coefficients (hi + 1) and v rows (hi + 1) visible; R rows free
         float dec_nx = 0.f, beta_nx = 0.f;
         if (e < nn) {
             dec_nx = p.decay[(lb * N + e) * p.Hv + g * p.R];
             beta_nx = p.beta[(lb * N + e) * p.Hv + g * p.R];
         }
-        for (int hi = 0; hi < p.R; ++hi) {
-            const int h = g * p.R + hi, db = hi & 1;
-            // conv weights of this head's v channel (used by the R pass)
-            const int cv = 2 * p.Hk * kDK + h * kDV + j;
-            float wv[KT];
-#pragma unroll
-            for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
-            if (warp == 0 && lane == 0 && hi + 1 < p.R && tc::mbar_wait(s_free, hi & 1, abort_flag)) {
-                tc::mbar_expect_tx(full, kDV * kDK * 4);  // S0 of the next head over the read one
-                for (int blk = 0; blk < kDK / 32; ++blk)
-                    tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0 + (hi + 1) * kDV);
+        // stage a head's v channels of the node rows and conv-state rows (16-byte cp.async)
+        auto stage_v = [&](int h) {
+            constexpr int kVec = kDV * (int)sizeof(Tin) / 16;
+            const long cv0 = 2L * p.Hk * kDK + (long)h * kDV;
+            for (int i = e; i < (nn + K - 1) * kVec; i += kEpi) {
+                const int r = i / kVec, c = i % kVec;
+                const Tin* src = (r < nn ? xb + (long)r * C : csb + (long)(r - nn) * C) + cv0 + c * (16 / (int)sizeof(Tin));
+                const int rs = r < nn ? r : N + (r - nn);
+                cp_async16(reinterpret_cast<unsigned char*>(sv + (long)rs * kDV) + c * 16, src);
             }
-            __syncwarp();
-            // gates of this head; per-node decay products and chain coefficients
-            //   A(t, s_m) = b_t G(t, s_m) (k_s.k_t),  B(t, s_m) = G(t, s_m) (k_s.q_t)
-            // stage this head's v channels of the node rows and conv-state rows (16-byte
-            // cp.async); the copies land while the gates and chain coefficients are computed
-            {
-                constexpr int kVec = kDV * (int)sizeof(Tin) / 16;
-                const long cv0 = 2L * p.Hk * kDK + (long)h * kDV;
-                for (int i = e; i < (nn + K - 1) * kVec; i += kEpi) {
-                    const int r = i / kVec, c = i % kVec;
-                    const Tin* src = (r < nn ? xb + (long)r * C : csb + (long)(r - nn) * C) + cv0 + c * (16 / (int)sizeof(Tin));
-                    const int rs = r < nn ? r : N + (r - nn);
-                    cp_async16(reinterpret_cast<unsigned char*>(sv + (long)rs * kDV) + c * 16, src);
-                }
-                cp_async_commit();
-            }
+            cp_async_commit();
+        };
+        // gates of head hi (already in registers) into buffer hi & 1; next head's into registers
+        auto gates = [&](int hi) {
             if (e < nn) {
-                sdec[e] = dec_nx;
-                sbeta[e] = beta_nx;
+                sdec[(hi & 1) * N + e] = dec_nx;
+                sbeta[(hi & 1) * N + e] = beta_nx;
                 if (hi + 1 < p.R) {
-                    dec_nx = p.decay[(lb * N + e) * p.Hv + h + 1];
-                    beta_nx = p.beta[(lb * N + e) * p.Hv + h + 1];
+                    dec_nx = p.decay[(lb * N + e) * p.Hv + g * p.R + hi + 1];
+                    beta_nx = p.beta[(lb * N + e) * p.Hv + g * p.R + hi + 1];
                 }
             }
-            named_bar(1, kEpi);
+        };
+        // chain coefficients A(t, s_m) = b_t G(t, s_m) (k_s.k_t), B(t, s_m) = G(t, s_m) (k_s.q_t)
+        // and the path decay g_t of head hi (node e's own row)
+        auto coefs = [&](int hi) {
             if (e < nn) {
+                const float* dec = sdec + (hi & 1) * N;
                 const int dep = sdep[e];
-                float gam = sdec[e];
-                const float bt = sbeta[e];
+                float gam = dec[e];
+                const float bt = sbeta[(hi & 1) * N + e];
+                float* cb = scb + (hi & 1) * N * kMD;
                 for (int m = 0; m < dep; ++m) {
                     const int s = alist[e * kMD + m];
                     sca[e * kMD + m] = bt * gam * skk[e * kMD + m];
-                    scb[e * kMD + m] = gam * sqk[e * kMD + m];
-                    gam *= sdec[s];
+                    cb[e * kMD + m] = gam * sqk[e * kMD + m];
+                    gam *= dec[s];
                 }
-                sg[e] = gam;
+                sg[(hi & 1) * N + e] = gam;
             }
-            named_bar(1, kEpi);
-            // M = B (I + A)^-1 one row per node, by back substitution along the node's own
-            // path p_0 = t, p_k = k-th ancestor:  M(t, p_k) = B(t, p_k) - sum_{i<k} M(t, p_i)
-            // A(p_i, p_k), M(t, t) = q_t.k_t.  Then o_t = g_t S0 q_t + sum_k M(t, p_k) R_{p_k}.
+        };
+        // M = B (I + A)^-1 one row per node, by back substitution along the node's own path
+        // p_0 = t, p_k = k-th ancestor:  M(t, p_k) = B(t, p_k) - sum_{i<k} M(t, p_i) A(p_i, p_k),
+        // M(t, t) = q_t.k_t.  Then o_t = g_t S0 q_t + sum_k M(t, p_k) R_{p_k}.
+        auto backsub = [&](int hi) {
             if (e < nn) {
                 const int dep = sdep[e];
+                float* cb = scb + (hi & 1) * N * kMD;
                 float mrow[kMD + 1];
                 mrow[0] = sqself[e];
 #pragma unroll
                 for (int k = 1; k <= kMD; ++k) {
                     if (k > dep) break;
-                    float acc = scb[e * kMD + k - 1];
+                    float acc = cb[e * kMD + k - 1];
                     acc = fmaf(-mrow[0], sca[e * kMD + k - 1], acc);
 #pragma unroll
                     for (int i = 1; i < k; ++i) {
@@ -565,94 +565,125 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
 #pragma unroll
                 for (int k = 1; k <= kMD; ++k) {
                     if (k > dep) break;
-                    scb[e * kMD + k - 1] = mrow[k];  // own row only: B(t, .) is not read by others
+                    cb[e * kMD + k - 1] = mrow[k];  // own row only: B(t, .) is not read by others
                 }
             }
-            cp_async_wait_all();
-            named_bar(1, kEpi);
+        };
+        stage_v(g * p.R);
+        gates(0);
+        named_bar(1, kEpi);
+        coefs(0);
+        cp_async_wait_all();
+        named_bar(1, kEpi);
+        for (int hi = 0; hi < p.R; ++hi) {
+            const int h = g * p.R + hi, db = hi & 1, cur = hi & 1;
+            // conv weights of this head's v channel (used by the R pass)
+            const int cv = 2 * p.Hk * kDK + h * kDV + j;
+            float wv[KT];
+#pragma unroll
+            for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
+            if (warp == 0 && lane == 0 && hi + 1 < p.R && tc::mbar_wait(s_free, hi & 1, abort_flag)) {
+                tc::mbar_expect_tx(full, kDV * kDK * 4);  // S0 of the next head over the read one
+                for (int blk = 0; blk < kDK / 32; ++blk)
+                    tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0 + (hi + 1) * kDV);
+            }
+            __syncwarp();
+            // the sca entries read here were written before the last barrier; the next
+            // head's coefficients overwrite them only after the next one
+            backsub(hi);
             // after a timeout the warp keeps meeting the named barriers but does no work
             if (!dead) dead = !__all_sync(kFull, tc::mbar_wait(d_full + db, (hi >> 1) & 1, abort_flag));
-            if (dead) {
-                named_bar(1, kEpi);
-                named_bar(1, kEpi);
-                continue;
-            }
-            tc::tc_fence_after();
+            const float* sbc = sbeta + cur * N;
+            const float* sgc = sg + cur * N;
+            const float* scbc = scb + cur * N * kMD;
             const uint32_t dcol = tmem + lane_base + db * p.NPAD;
-            // pass A: R_t = b_t (v_t - g_t (S0 k_t)); v_t by the conv along the node's path
-            // each thread takes whole 8-node chunks (the three warps of a lane quarter take
-            // every third chunk), so every loaded column is used and 8 nodes are in flight
-            for (int c = quad; c * 8 < nn; c += 3) {
-                const int t0 = c * 8;
-                uint32_t ks[8];
-                tmem_ld8(dcol + t0, ks);
-                float vin[8][KT];
+            if (!dead) {
+                tc::tc_fence_after();
+                // pass A: R_t = b_t (v_t - g_t (S0 k_t)); v_t by the conv along the node's path.
+                // Each thread takes whole 8-node chunks (the three warps of a lane quarter
+                // take every third chunk), so every loaded column is used and 8 nodes are in
+                // flight.
+                for (int c = quad; c * 8 < nn; c += 3) {
+                    const int t0 = c * 8;
+                    uint32_t ks[8];
+                    tmem_ld8(dcol + t0, ks);
+                    float vin[8][KT];
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = min(t0 + uu, nn - 1);
-                    if constexpr (KT == 4) {
-                        const int4 r4 = *reinterpret_cast<const int4*>(trow + t * 4);
-                        vin[uu][0] = to_f32(sv[r4.x * kDV + j]);
-                        vin[uu][1] = to_f32(sv[r4.y * kDV + j]);
-                        vin[uu][2] = to_f32(sv[r4.z * kDV + j]);
-                        vin[uu][3] = to_f32(sv[r4.w * kDV + j]);
-                    } else {
+                    for (int uu = 0; uu < 8; ++uu) {
+                        const int t = min(t0 + uu, nn - 1);
+                        if constexpr (KT == 4) {
+                            const int4 r4 = *reinterpret_cast<const int4*>(trow + t * 4);
+                            vin[uu][0] = to_f32(sv[r4.x * kDV + j]);
+                            vin[uu][1] = to_f32(sv[r4.y * kDV + j]);
+                            vin[uu][2] = to_f32(sv[r4.z * kDV + j]);
+                            vin[uu][3] = to_f32(sv[r4.w * kDV + j]);
+                        } else {
 #pragma unroll
-                        for (int q = 0; q < KT; ++q) vin[uu][q] = (q < K) ? to_f32(sv[trow[t * K + q] * kDV + j]) : 0.f;
+                            for (int q = 0; q < KT; ++q)
+                                vin[uu][q] = (q < K) ? to_f32(sv[trow[t * K + q] * kDV + j]) : 0.f;
+                        }
                     }
-                }
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = t0 + uu;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int q = 0; q < KT; ++q) acc = fmaf(wv[q], vin[uu][q], acc);
-                    if (t < nn) ubuf[t * kDV + j] = sbeta[t] * (silu_g(acc) - sg[t] * __uint_as_float(ks[uu]));
-                }
-            }
-            named_bar(1, kEpi);
-            if (warp == 1 && lane == 0 && hi + 1 < p.R) issue_mma(hi + 1);
-            __syncwarp();
-            // pass C: outputs as independent sums over each node's own path; the 8 nodes of
-            // a chunk advance one ancestor level at a time, so their loads overlap
-            for (int c = quad; c * 8 < N; c += 3) {
-                const int t0 = c * 8;
-                uint32_t qs[8];
-                if (t0 < nn) {
-                    tmem_ld8(dcol + p.QOFF + t0, qs);
                     tc::tmem_wait_ld();
-                }
-                float ot[8];
-                int dp[8];
-                int md = 0;
-#pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = t0 + uu;
-                    dp[uu] = 0;
-                    ot[uu] = 0.f;
-                    if (t < nn) {
-                        dp[uu] = sdep[t];
-                        ot[uu] = fmaf(sg[t], __uint_as_float(qs[uu]), sqself[t] * ubuf[t * kDV + j]);
-                    }
-                    md = max(md, dp[uu]);
-                }
-                for (int a = 0; a < md; ++a) {
 #pragma unroll
                     for (int uu = 0; uu < 8; ++uu) {
                         const int t = t0 + uu;
-                        if (a < dp[uu]) ot[uu] = fmaf(scb[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot[uu]);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int q = 0; q < KT; ++q) acc = fmaf(wv[q], vin[uu][q], acc);
+                        if (t < nn) ubuf[t * kDV + j] = sbc[t] * (silu_g(acc) - sgc[t] * __uint_as_float(ks[uu]));
                     }
                 }
-#pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    const int t = t0 + uu;
-                    if (t < N) obase[((long)t * p.Hv + h) * kDV + j] = from_f32<Tout>(ot[uu]);
-                }
             }
-            tc::tc_fence_before();
-            tc::mbar_arrive(d_free + db);
-            named_bar(1, kEpi);  // ubuf and the per-head arrays are rewritten by the next head
+            if (hi + 1 < p.R) gates(hi + 1);
+            named_bar(1, kEpi);
+            if (warp == 1 && lane == 0 && hi + 1 < p.R && !dead) issue_mma(hi + 1);
+            __syncwarp();
+            if (hi + 1 < p.R) {
+                stage_v(h + 1);
+                coefs(hi + 1);
+            }
+            if (!dead) {
+                // pass C: outputs as independent sums over each node's own path; the 8 nodes
+                // of a chunk advance one ancestor level at a time, so their loads overlap
+                for (int c = quad; c * 8 < N; c += 3) {
+                    const int t0 = c * 8;
+                    uint32_t qs[8];
+                    if (t0 < nn) {
+                        tmem_ld8(dcol + p.QOFF + t0, qs);
+                        tc::tmem_wait_ld();
+                    }
+                    float ot[8];
+                    int dp[8];
+                    int md = 0;
+#pragma unroll
+                    for (int uu = 0; uu < 8; ++uu) {
+                        const int t = t0 + uu;
+                        dp[uu] = 0;
+                        ot[uu] = 0.f;
+                        if (t < nn) {
+                            dp[uu] = sdep[t];
+                            ot[uu] = fmaf(sgc[t], __uint_as_float(qs[uu]), sqself[t] * ubuf[t * kDV + j]);
+                        }
+                        md = max(md, dp[uu]);
+                    }
+                    for (int a = 0; a < md; ++a) {
+#pragma unroll
+                        for (int uu = 0; uu < 8; ++uu) {
+                            const int t = t0 + uu;
+                            if (a < dp[uu]) ot[uu] = fmaf(scbc[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot[uu]);
+                        }
+                    }
+#pragma unroll
+                    for (int uu = 0; uu < 8; ++uu) {
+                        const int t = t0 + uu;
+                        if (t < N) obase[((long)t * p.Hv + h) * kDV + j] = from_f32<Tout>(ot[uu]);
+                    }
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(d_free + db);
+            }
+            cp_async_wait_all();
+            named_bar(1, kEpi);  // coefficients and v rows of the next head visible; R rows free
         }
     }
     if (warp == 1 && lane == 0) {  // every MMA has completed before TMEM is freed
