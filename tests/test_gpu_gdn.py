@@ -90,11 +90,11 @@ def test_gdn_tree_workload_sampled():
 
 @pytest.mark.parametrize("Hk,Hv,dtype,budget", [(2, 2, torch.bfloat16, 16), (1, 4, torch.float32, 64),
                                                  (2, 4, torch.float32, 32), (3, 6, torch.bfloat16, 0),
-                                                 (1, 3, torch.bfloat16, 65)])
+                                                 (1, 3, torch.bfloat16, 65), (1, 2, torch.float32, 62)])
 def test_gdn_head128_variants(Hk, Hv, dtype, budget):
     """Head size 128: one or several value heads per key head, fp32 or bf16 inputs, root-only
-    trees, and the largest tree the tensor-core path stages for bf16 (66 rows); larger
-    fp32 trees take the CUDA-core path."""
+    trees, and the largest trees the tensor-core path stages (66 rows for bf16, 63 for
+    fp32); larger fp32 trees take the CUDA-core path."""
     tree, _ = C.tree_from_logits(4, 2, 15, 3000, 8, budget)
     gi = synth.gdn_inputs(2, 2, budget + 1, Hk, Hv, 128, 128, 4, workload=4, dtype=dtype)
     r = _gpu(tree, gi, Hk)
