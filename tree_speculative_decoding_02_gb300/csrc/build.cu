@@ -232,24 +232,37 @@ __device__ __forceinline__ int cand_token(const TreeSmem& S, int k, const Cand& 
 }
 
 // Lexicographic order of the two candidates' token paths (lower ids first, a prefix
-// before its extensions); only consulted on an exact score tie.
+// before its extensions); only consulted on an exact score tie.  The deeper candidate is
+// lifted to the other's depth (meeting it means one path is a prefix of the other), then
+// both climb in step until their parents agree: the tokens below that common ancestor
+// differ and decide.  No path is materialised.
 __device__ bool lex_less(const TreeSmem& S, int k, const Cand& a, const Cand& b) {
-    int pa[kMaxDepth], pb[kMaxDepth];
-    int na = a.depth, nb = b.depth;
-    pa[na - 1] = cand_token(S, k, a);
-    for (int i = na - 2, p = a.parent; i >= 0; --i) {
-        pa[i] = cand_token(S, k, S.sel[p]);
-        p = S.sel[p].parent;
+    int da = a.depth, db = b.depth;
+    int ta = cand_token(S, k, a), tb = cand_token(S, k, b);
+    int pa = a.parent, pb = b.parent;  // rows of S.sel; -1 = the root
+    while (da > db) {
+        const Cand& u = S.sel[pa];
+        ta = cand_token(S, k, u);
+        pa = u.parent;
+        --da;
     }
-    pb[nb - 1] = cand_token(S, k, b);
-    for (int i = nb - 2, p = b.parent; i >= 0; --i) {
-        pb[i] = cand_token(S, k, S.sel[p]);
-        p = S.sel[p].parent;
+    if (a.depth > b.depth && pa == pb && ta == tb) return false;  // b is a prefix of a
+    while (db > da) {
+        const Cand& u = S.sel[pb];
+        tb = cand_token(S, k, u);
+        pb = u.parent;
+        --db;
     }
-    const int n = na < nb ? na : nb;
-    for (int i = 0; i < n; ++i)
-        if (pa[i] != pb[i]) return pa[i] < pb[i];
-    return na < nb;
+    if (b.depth > a.depth && pa == pb && ta == tb) return true;   // a is a proper prefix of b
+    while (pa != pb) {
+        const Cand& u = S.sel[pa];
+        const Cand& v = S.sel[pb];
+        ta = cand_token(S, k, u);
+        tb = cand_token(S, k, v);
+        pa = u.parent;
+        pb = v.parent;
+    }
+    return ta < tb;
 }
 
 __device__ __forceinline__ bool cand_better(const TreeSmem& S, int k, const Cand& a, const Cand& b) {
@@ -356,8 +369,11 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int V, int k, in
                 if (best < 0 || cand_better(S, k, S.front[i], S.front[best])) best = i;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
+                // lanes that already agree skip the compare: on equal scores it walks both
+                // token paths, which for an entry against itself is the whole path
                 const int other = __shfl_xor_sync(kFull, best, o);
-                if (other >= 0 && (best < 0 || cand_better(S, k, S.front[other], S.front[best]))) best = other;
+                if (other >= 0 && other != best && (best < 0 || cand_better(S, k, S.front[other], S.front[best])))
+                    best = other;
             }
             best = __shfl_sync(kFull, best, 0);
             int nf = 0;
