@@ -78,6 +78,15 @@ const char* ddt_version(void);
  * counterpart in the pages: bookkeeping for measurement. */
 uint64_t ddt_launch_count(void);
 
+/* Runs one bounded device wait on an mbarrier that nothing ever signals -- the same
+ * wait, with the same limit (about one second of SM clock cycles), that every pipeline
+ * barrier of the tensor-core kernels uses -- and writes its outcome to status[0]:
+ * DDT_ERR_TIMEOUT when the wait gave up, as it must.  The kernel then returns normally,
+ * so the context stays usable.  This exercises the failure path of the bounded waits
+ * without a fault.  status: one int32 on the device.  Returns DDT_ERR_INVALID_ARG for a
+ * null status, DDT_ERR_CUDA if the launch fails.  No counterpart in the pages. */
+ddt_status ddt_wait_selftest(int32_t* status, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * ddt_build_tree -- [ARCH] best-first tree construction and flattening; [CHALL] 2.
  *

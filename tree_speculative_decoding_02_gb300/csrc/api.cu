@@ -47,6 +47,11 @@ const char* ddt_version(void) { return "ddt 0.1 sm_103a"; }
 
 uint64_t ddt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+ddt_status ddt_wait_selftest(int32_t* status, cudaStream_t stream) {
+    if (!status) return DDT_ERR_INVALID_ARG;
+    return launch_wait_selftest(status, stream) == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------------- build
 size_t ddt_build_tree_workspace(int B, int D, int V, int top_k) {
     if (B < 1 || D < 1 || V < 1 || top_k < 1) return 0;

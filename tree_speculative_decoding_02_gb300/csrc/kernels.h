@@ -61,6 +61,8 @@ cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap
                            const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
                            void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st);
 
+// one bounded wait on an mbarrier nothing signals; status[0] = its outcome
+cudaError_t launch_wait_selftest(int32_t* status, cudaStream_t st);
 cudaError_t launch_rope_tree(int L, int B, int N, int Hq, int Hkv, int d, int rot, double theta, ddt_dtype dtype,
                              const int32_t* position, const int32_t* n_nodes, void* q, void* k, cudaStream_t st);
 bool gdn_tc_supported(int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in);

@@ -33,6 +33,7 @@ _SIGS = {
     "ddt_status_string": ([_c_int], ctypes.c_char_p),
     "ddt_version": ([], ctypes.c_char_p),
     "ddt_launch_count": ([], ctypes.c_uint64),
+    "ddt_wait_selftest": ([_c_p, _c_p], _c_int),
     "ddt_build_tree_workspace": ([_c_int] * 4, _c_size),
     "ddt_build_tree": ([_c_int] * 6 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_build_tree_noalloc": ([_c_int] * 6 + [_c_p] * 11 + [_c_p], _c_int),
@@ -84,6 +85,17 @@ def load(build_if_missing: bool = True):
 def ddt_launch_count() -> int:
     """Kernel launches the library has issued in this process so far."""
     return int(load().ddt_launch_count())
+
+
+def ddt_wait_selftest(stream=None) -> int:
+    """Runs one bounded device wait that nothing signals and returns the status it wrote
+    (DDT_ERR_TIMEOUT = 5 when the wait gave up, as it should); synchronises the stream."""
+    lib = _gpu()
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    s = stream or torch.cuda.current_stream()
+    _check(lib.ddt_wait_selftest(_ptr(st), ctypes.c_void_p(s.cuda_stream)), "ddt_wait_selftest")
+    s.synchronize()
+    return int(st.item())
 
 
 def _gpu():
