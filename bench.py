@@ -170,8 +170,8 @@ def round_bytes(r):
 # and the bench reports null until it is captured again.
 ATTN_TRAFFIC = {
     # ncu, batched round, mean of the three timed launches of one capture:
-    # dram__bytes_read.sum 40,355,525,803 B + dram__bytes_write.sum 399,649,707 B
-    "b254561bfd1e7a475760cfc72bb81d6f27dedd9495a1746ae329695fa4f863f7": {"workload": 5, "bytes": 40755175509.0},
+    # dram__bytes_read.sum 40,355,763,541 B + dram__bytes_write.sum 400,794,795 B
+    "bfdc4160d21e99d36f74f45bb592cfea7ca3e4b2aade0e9bd2f1fe0da592e0a8": {"workload": 5, "bytes": 40756558336.0},
 }
 ATTN_SOURCES = ("attn_tc.cu", "tc.cuh")
 
