@@ -59,7 +59,7 @@ typedef enum {
     DDT_ERR_UNSUPPORTED = 2, /* size/dtype combination not compiled in */
     DDT_ERR_CAPACITY = 3,    /* prefix_len + committed rows would exceed the cache */
     DDT_ERR_CUDA = 4,        /* a launch failed; see cudaGetLastError semantics */
-    DDT_ERR_TIMEOUT = 5,     /* reserved: a bounded device wait gave up */
+    DDT_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (per request, tensor-core kernels) */
     DDT_ERR_NONFINITE = 6,   /* NaN or +-Inf logits */
     DDT_ERR_TREE = 7         /* malformed tree arrays (parent >= child, bad token) */
 } ddt_status;
@@ -85,7 +85,7 @@ uint64_t ddt_launch_count(void);
  * so the context stays usable.  This exercises the failure path of the bounded waits
  * without a fault.  status: one int32 on the device.  Returns DDT_ERR_INVALID_ARG for a
  * null status, DDT_ERR_CUDA if the launch fails.  No counterpart in the pages. */
-ddt_status ddt_wait_selftest(int32_t* status, cudaStream_t stream);
+ddt_status ddt_wait_selftest(int32_t* status, ddt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * ddt_build_tree -- [ARCH] best-first tree construction and flattening; [CHALL] 2.
@@ -125,8 +125,11 @@ ddt_status ddt_build_tree(int B, int D, int V, int top_k, int budget, ddt_dtype 
  * because they synchronise the device.  Same arguments and results as ddt_build_tree,
  * without the workspace: the scratch is a fixed 4 MiB device array inside the library,
  * present on every GPU that loads the library until the process exits.
- *   - The first call on a device looks up that array's device address (once per
- *     device, with the device current); make that first call before any stream capture.
+ *   - The first call on a device looks up that array's device address (with the device
+ *     current) and caches it with the CUDA context it belongs to; a call made in another
+ *     context of that device (after cudaDeviceReset, or once the primary context was
+ *     released and created again) looks it up anew.  Make the first call in a context
+ *     before any stream capture.
  *   - Every call on a device shares the array, which keeps the last call's contents:
  *     calls whose kernels overlap on the GPU race on it and must be ordered by the caller.
  *   - Returns DDT_ERR_CAPACITY, before launching anything, when the call needs more
@@ -149,7 +152,9 @@ ddt_status ddt_build_tree_noalloc(int B, int D, int V, int top_k, int budget, dd
  * For layer l, request b, row i < n_nodes[b], query head h (kv head g = h / (Hq/Hkv)):
  *   o = softmax(scale * q . K^T) V over keys {k_cache rows 0..prefix_len[b]-1} and
  *       {k_tree rows j : bit j of anc[b][i]}.
- * Inputs are taken after any rotary embedding.
+ * scale is the caller's softmax scale (1/sqrt(d) for standard attention); the library
+ * applies it as given and supplies no default.  Inputs are taken after any rotary
+ * embedding.
  *   q [L][B][N][Hq][d], k_tree, v_tree [L][B][N][Hkv][d]  (in_dtype)
  *   k_cache, v_cache [L][B][Hkv][Pcap][d] (in_dtype): only rows < prefix_len[b] are
  *     read; the rest may hold anything.  Tree rows >= n_nodes[b] are never read.
@@ -234,6 +239,12 @@ ddt_status ddt_rope_tree(int n_layers, int B, int N, int Hq, int Hkv, int d, int
  *   beta, decay [L][B][N][Hv] fp32;  S [L][B][Hv][dv][dk] fp32 (read only)
  *   parent [B][N], n_nodes [B] as written by ddt_build_tree
  *   o [L][B][N][Hv][dv] (out_dtype); padding rows are zeros.
+ *   S_node_debug: NULL, or [L][B][N][Hv][dv][dk] fp32 that receives every node's own
+ *     branch-local state S_n, computed the literal way: node n reads its parent's state
+ *     from this buffer (the root reads S) and writes its own row, parents before
+ *     children.  A debugging aid for small trees (it writes N states per head, so it is
+ *     not for full-size workloads); the fast path never forms these states.  Padding
+ *     rows are zeros.  The o outputs are those of the normal path either way.
  *   status [B]: DDT_ERR_TREE for a malformed parent array, DDT_ERR_UNSUPPORTED for a
  *     tree deeper than the head-128 limit below (that request's outputs are then zero).
  * Limits: dk, dv in {32, 64, 128} (dk = dv = 128 runs on the tensor cores and takes
@@ -245,8 +256,8 @@ ddt_status ddt_tree_gdn(int n_layers, int B, int N, int Hk, int Hv, int dk, int 
                         ddt_dtype in_dtype, ddt_dtype out_dtype, const void* x,
                         const void* conv_w, const void* conv_state, const float* beta,
                         const float* decay, const float* S, const int32_t* parent,
-                        const int32_t* n_nodes, void* o, int32_t* status, void* workspace,
-                        size_t ws_bytes, ddt_stream_t stream);
+                        const int32_t* n_nodes, void* o, float* S_node_debug, int32_t* status,
+                        void* workspace, size_t ws_bytes, ddt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * ddt_walk_accept -- [ARCH] follow_verified_tree; [NOTES] "What broke along the way"

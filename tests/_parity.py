@@ -47,13 +47,23 @@ def assert_tree_equal(gpu, orc, b, check_scores=True):
         md = orc["margin_depth"][b]
         near = orc["margin"][b] < NEAR_TIE and md[0] != md[1]
         assert near, f"request {b}: tree differs from the oracle (margin {orc['margin'][b]:.3g})"
-        # near-tie: the node sets may differ only by swaps within the tie window
-        sg = set(tree_sequences(gpu["token"][b], gpu["parent"][b], n_g).values())
+        # near-tie: the node sets may differ only by swaps within the tie window, on both
+        # sides: every oracle node the GPU left out scores within NEAR_TIE of the cut (the
+        # oracle's lowest selected score), and so does every GPU node the oracle left out
+        # (by the GPU's own score, which differs from the exact one by ~1e-7)
+        sg = tree_sequences(gpu["token"][b], gpu["parent"][b], n_g)
         so = tree_sequences(orc["token"][b], orc["parent"][b], n_o)
         cut = min(orc["score"][b][1:n_o])
+        set_g, set_o = set(sg.values()), set(so.values())
         for i, s in so.items():
-            if s not in sg:
-                assert orc["score"][b][i] - cut < NEAR_TIE
+            if s not in set_g:
+                assert orc["score"][b][i] - cut < NEAR_TIE, f"request {b}: oracle node {s} left out"
+        extra = [i for i, s in sg.items() if s not in set_o]
+        assert len(extra) == sum(1 for s in so.values() if s not in set_g)
+        if extra:
+            assert gpu.get("score") is not None, "a near-tie swap can only be checked with the GPU's scores"
+            for i in extra:
+                assert abs(float(gpu["score"][b][i]) - cut) < NEAR_TIE, f"request {b}: GPU node {sg[i]} outside the tie window"
         return
     if check_scores and gpu.get("score") is not None:
         sg = np.asarray(gpu["score"][b][:n_g])

@@ -71,21 +71,16 @@ def test_gdn_malformed_tree_flagged():
     assert (r["o"][:, 1] == 0).all()
 
 
-def test_gdn_tree_workload_sampled():
-    """48 layers, Hk=16, Hv=48, dk=dv=128, budget-64 tree from a drafter-vocab build; sampled
-    (layer, value head) units against the oracle."""
+def test_gdn_tree_workload_full():
+    """48 layers, Hk=16, Hv=48, dk=dv=128, budget-64 tree from a drafter-vocab build: every
+    (layer, node, value head) output against the oracle, with fp32 and with bf16 outputs."""
     tree, _ = C.tree_from_logits(4, 1, 15, 151936, 8, 64)
     gi = synth.gdn_inputs(48, 1, 65, 16, 48, 128, 128, 4, workload=4, dtype=torch.bfloat16)
-    r = _gpu(tree, gi, 16)
-    got = r["o"].cpu().double().numpy()
-    rng = np.random.default_rng(1)
-    for _ in range(8):
-        l, h = int(rng.integers(48)), int(rng.integers(48))
-        u = oracle.gdn_unit(C.f64(gi.x[l, 0]), C.f64(gi.conv_w[l]), C.f64(gi.conv_state[l, 0]),
-                            C.f64(gi.beta[l, 0]), C.f64(gi.decay[l, 0]), C.f64(gi.S[l, 0, h]), tree["parent"][0],
-                            tree["n_nodes"][0], 16, 48, h)
-        err = normwise(got[l, 0, :, h], u["o"], axes=-1)
-        assert err.max() <= TOL, (l, h, err.max())
+    want = _oracle(tree, gi, 16)
+    for dt in (torch.float32, torch.bfloat16):
+        r = _gpu(tree, gi, 16, out_dtype=dt)
+        _check(r["o"], want, tree)
+        assert int(r["status"][0]) == 0
 
 
 @pytest.mark.parametrize("Hk,Hv,dtype,budget", [(2, 2, torch.bfloat16, 16), (1, 4, torch.float32, 64),
@@ -127,3 +122,54 @@ def test_gdn_head128_conv_widths(K):
     r = _gpu(tree, gi, 2)
     _check(r["o"], _oracle(tree, gi, 2), tree)
     assert (r["status"].cpu() == 0).all()
+
+
+@pytest.mark.parametrize("Hk,Hv,L", [(2, 6, 2), (16, 48, 1)])
+def test_gdn_bf16_output_instance(Hk, Hv, L):
+    """The instance the batched round runs (bf16 inputs and outputs, head 128, conv 4,
+    budget-64 tree): within the tolerance of the oracle, and each element within one bf16
+    rounding of the same call with fp32 outputs."""
+    tree, _ = C.tree_from_logits(4, 2, 15, 3000, 8, 64)
+    gi = synth.gdn_inputs(L, 2, 65, Hk, Hv, 128, 128, 4, workload=4, dtype=torch.bfloat16)
+    r32 = _gpu(tree, gi, Hk)
+    r16 = _gpu(tree, gi, Hk, out_dtype=torch.bfloat16)
+    assert r16["o"].dtype == torch.bfloat16
+    _check(r16["o"], _oracle(tree, gi, Hk), tree)
+    a, bq = r32["o"].float(), r16["o"].float()
+    ulp = torch.clamp(a.abs(), min=1e-30) * 2.0 ** -7
+    assert ((a - bq).abs() <= ulp).all()
+    assert (r16["status"].cpu() == 0).all()
+
+
+@pytest.mark.parametrize("case", ["tiny_fp32", "head128_bf16", "dk64_dv128"])
+def test_gdn_node_states_match_oracle(case):
+    """The optional per-node state output: every node's own branch-local state S_n, formed
+    by reading its parent's state and writing its own scratch copy, against the oracle's
+    per-node states (normwise per (layer, request, node, head) matrix); padding rows stay
+    zero, and the outputs o (the normal path) still match."""
+    if case == "tiny_fp32":
+        tree, _ = C.tree_from_logits(1, 1, 8, 1024, 8, 16, std=2.0, boost=0.0)
+        L, B, Hk, Hv, dk, dv, dt = 1, 1, 2, 2, 32, 32, torch.float32
+    elif case == "head128_bf16":
+        tree, _ = C.tree_from_logits(4, 2, 15, 3000, 8, 12)
+        L, B, Hk, Hv, dk, dv, dt = 2, 2, 1, 3, 128, 128, torch.bfloat16
+    else:
+        tree, _ = C.tree_from_logits(4, 2, 6, 300, 3, 10, std=2.0, boost=0.0)
+        L, B, Hk, Hv, dk, dv, dt = 1, 2, 2, 4, 64, 128, torch.float32
+    N = tree["token"].shape[1]
+    gi = synth.gdn_inputs(L, B, N, Hk, Hv, dk, dv, 4, workload=4, dtype=dt)
+    t = C.tree_to_dev(tree)
+    S_dev = gi.S.transpose(-1, -2).contiguous().cuda()
+    sn = torch.full((L, B, N, Hv, dv, dk), float("nan"), device="cuda")
+    r = ddt.ddt_tree_gdn(gi.x.cuda(), gi.conv_w.cuda(), gi.conv_state.cuda(), gi.beta.cuda(), gi.decay.cuda(),
+                         S_dev, t["parent"], t["n_nodes"], Hk=Hk, out_dtype=torch.float32, S_node_debug=sn)
+    torch.cuda.synchronize()
+    want = oracle.tree_gdn(C.f64(gi.x), C.f64(gi.conv_w), C.f64(gi.conv_state), C.f64(gi.beta), C.f64(gi.decay),
+                           C.f64(gi.S), tree["parent"], tree["n_nodes"], Hk, want_states=True)
+    got = np.swapaxes(sn.cpu().double().numpy(), -1, -2)      # -> [..][dk][dv] like the oracle
+    for b in range(B):
+        n = int(tree["n_nodes"][b])
+        err = normwise(got[:, b, :n], want["S_node"][:, b, :n], axes=(-2, -1))
+        assert err.max() <= TOL, f"request {b}: node-state error {err.max():.3g}"
+        assert (got[:, b, n:] == 0).all()
+    _check(r["o"], want["o"], tree)

@@ -44,7 +44,7 @@ def _gpu_attn(c, tree, out_dtype=torch.float32):
     t = C.tree_to_dev(tree)
     r = ddt.ddt_tree_attn_paged(c["q"].cuda(), c["k_tree"].cuda(), c["v_tree"].cuda(), c["k_pages"].cuda(),
                                 c["v_pages"].cuda(), c["table"].cuda(), torch.as_tensor(c["P"]).cuda(), t["n_nodes"],
-                                t["anc"], out_dtype=out_dtype)
+                                t["anc"], scale=1.0 / math.sqrt(c["q"].shape[-1]), out_dtype=out_dtype)
     torch.cuda.synchronize()
     return r
 

@@ -165,8 +165,8 @@ def test_commit_capacity_refused():
 
 
 def test_commit_gdn_workload_forced_path():
-    """48 GDN layers, Hk=16, Hv=48, dk=dv=128: commit of a seeded root-to-leaf path; sampled
-    (layer, head) states against the oracle."""
+    """48 GDN layers, Hk=16, Hv=48, dk=dv=128: commit of a seeded root-to-leaf path; every
+    (layer, value head) state and every layer's conv state against the oracle."""
     tree, _ = C.tree_from_logits(4, 1, 15, 151936, 8, 64)
     rng = np.random.default_rng(4)
     path = [0]
@@ -188,10 +188,8 @@ def test_commit_gdn_workload_forced_path():
                        Hk=16)
     torch.cuda.synchronize()
     assert int(r["status"][0]) == 0 and int(pld[0]) == len(path)
-    for (l, h) in [(0, 0), (47, 47), (13, 5), (30, 22)]:
-        o = oracle.commit(acc, al, [0], x=C.f64(gi.x[l:l + 1]), conv_w=C.f64(gi.conv_w[l:l + 1]),
-                          beta=C.f64(gi.beta[l:l + 1]), decay=C.f64(gi.decay[l:l + 1]), S=C.f64(gi.S[l:l + 1]),
-                          conv_state=C.f64(gi.conv_state[l:l + 1]), Hk=16)
-        err = normwise(C.s_to_oracle(S[l, 0, h]), o["S"][0, 0, h], axes=(-2, -1))
-        assert err <= TOL, (l, h, err)
-        np.testing.assert_array_equal(C.f64(cs[l]), o["conv_state"][0])
+    o = oracle.commit(acc, al, [0], x=C.f64(gi.x), conv_w=C.f64(gi.conv_w), beta=C.f64(gi.beta),
+                      decay=C.f64(gi.decay), S=C.f64(gi.S), conv_state=C.f64(gi.conv_state), Hk=16)
+    err = normwise(C.s_to_oracle(S), o["S"], axes=(-2, -1))
+    assert err.max() <= TOL, err.max()
+    np.testing.assert_array_equal(C.f64(cs), o["conv_state"])

@@ -64,7 +64,7 @@ def test_host_checks_fail_fast(lib):
     assert lib.ddt_tree_attn(1, 1, 5, 4, 1, 96, 10, 1, 1, *([p] * 8), 1.0, p, p, p, 256, nul) == 2
     assert lib.ddt_tree_attn(1, 1, 5, 5, 2, 64, 10, 1, 1, *([p] * 8), 1.0, p, p, p, 256, nul) == 1
     # GDN: unsupported head dims
-    assert lib.ddt_tree_gdn(1, 1, 5, 1, 1, 48, 48, 4, 1, 1, *([p] * 10), p, 256, nul) == 2
+    assert lib.ddt_tree_gdn(1, 1, 5, 1, 1, 48, 48, 4, 1, 1, *([p] * 11), p, 256, nul) == 2
     # walk / commit: bad sizes
     assert lib.ddt_walk_accept(0, 5, 10, 4, 1, *([p] * 11), p, 256, nul) == 1
     assert lib.ddt_commit(1, 5, 0, 0, 1, 64, 10, 1, p, p, p, p, 0, 1, 1, 32, 32, 4, 1, *([p] * 12), nul) == 1

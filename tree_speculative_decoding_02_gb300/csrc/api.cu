@@ -47,9 +47,10 @@ const char* ddt_version(void) { return "ddt 0.1 sm_103a"; }
 
 uint64_t ddt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-ddt_status ddt_wait_selftest(int32_t* status, cudaStream_t stream) {
+ddt_status ddt_wait_selftest(int32_t* status, ddt_stream_t stream) {
     if (!status) return DDT_ERR_INVALID_ARG;
-    return launch_wait_selftest(status, stream) == cudaSuccess ? DDT_OK : DDT_ERR_CUDA;
+    return launch_wait_selftest(status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DDT_OK
+                                                                                            : DDT_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------------- build
@@ -163,8 +164,8 @@ size_t ddt_tree_gdn_workspace(int n_layers, int B, int N, int Hk, int Hv, int dk
 ddt_status ddt_tree_gdn(int n_layers, int B, int N, int Hk, int Hv, int dk, int dv, int conv_k, ddt_dtype in_dtype,
                         ddt_dtype out_dtype, const void* x, const void* conv_w, const void* conv_state,
                         const float* beta, const float* decay, const float* S, const int32_t* parent,
-                        const int32_t* n_nodes, void* o, int32_t* status, void* workspace, size_t ws_bytes,
-                        ddt_stream_t stream) {
+                        const int32_t* n_nodes, void* o, float* S_node_debug, int32_t* status, void* workspace,
+                        size_t ws_bytes, ddt_stream_t stream) {
     (void)workspace; (void)ws_bytes;
     if (n_layers < 1 || B < 1 || N < 1 || Hk < 1 || Hv < 1 || Hv % Hk != 0 || conv_k < 1 || !dtype_ok(in_dtype) ||
         !dtype_ok(out_dtype))
@@ -175,15 +176,20 @@ ddt_status ddt_tree_gdn(int n_layers, int B, int N, int Hk, int Hv, int dk, int 
     if (!x || !conv_w || (conv_k > 1 && !conv_state) || !beta || !decay || !S || !parent || !n_nodes || !o ||
         !status || !aligned16(S))
         return DDT_ERR_INVALID_ARG;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
     // head size 128: dense part on the tensor cores (its 16-byte row copies want x and the
     // conv state 16-byte aligned); other sizes on the CUDA cores
     if (gdn_tc_supported(N, Hk, Hv, dk, dv, conv_k, in_dtype) && aligned16(x) && (conv_k == 1 || aligned16(conv_state)))
-        return from_cuda(launch_gdn_tc(n_layers, B, N, Hk, Hv, conv_k, in_dtype, out_dtype, x, conv_w, conv_state,
-                                       beta, decay, S, parent, n_nodes, o, status,
-                                       reinterpret_cast<cudaStream_t>(stream)));
-    return from_cuda(launch_gdn_tree(n_layers, B, N, Hk, Hv, dk, dv, conv_k, in_dtype, out_dtype, x, conv_w,
-                                     conv_state, beta, decay, S, parent, n_nodes, o, status,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+        e = launch_gdn_tc(n_layers, B, N, Hk, Hv, conv_k, in_dtype, out_dtype, x, conv_w, conv_state, beta, decay, S,
+                          parent, n_nodes, o, status, st);
+    else
+        e = launch_gdn_tree(n_layers, B, N, Hk, Hv, dk, dv, conv_k, in_dtype, out_dtype, x, conv_w, conv_state, beta,
+                            decay, S, parent, n_nodes, o, status, st);
+    if (e == cudaSuccess && S_node_debug)
+        e = launch_gdn_states(n_layers, B, N, Hk, Hv, dk, dv, conv_k, in_dtype, x, conv_w, conv_state, beta, decay,
+                              S, parent, n_nodes, S_node_debug, st);
+    return from_cuda(e);
 }
 
 // ----------------------------------------------------------------------------- walk
@@ -235,6 +241,7 @@ ddt_status ddt_commit(int B, int N, int A, int n_attn_layers, int Hkv, int d, in
                       const int32_t* acc_len, int32_t* prefix_len, int32_t* src_row, int32_t* dst_pos,
                       int32_t* status, ddt_stream_t stream) {
     if (B < 1 || N < 1 || A < 1 || n_attn_layers < 0 || n_gdn_layers < 0) return DDT_ERR_INVALID_ARG;
+    if (A > kMaxAccept + 1) return DDT_ERR_UNSUPPORTED;
     if (!acc_nodes || !acc_len || !prefix_len || !src_row || !dst_pos || !status) return DDT_ERR_INVALID_ARG;
     if (n_attn_layers > 0) {
         if (Hkv < 1 || d < 1 || Pcap < 1 || !dtype_ok(kv_dtype) || !k_tree || !v_tree || !k_cache || !v_cache)
@@ -264,6 +271,7 @@ ddt_status ddt_commit_paged(int B, int N, int A, int n_attn_layers, int Hkv, int
     if (n_attn_layers < 1 || !block_table || num_pages < 1 || max_pages < 1) return DDT_ERR_INVALID_ARG;
     if (!page_rows_ok(page_size) || (long)page_size * max_pages > (1L << 30)) return DDT_ERR_UNSUPPORTED;
     if (B < 1 || N < 1 || A < 1 || n_gdn_layers < 0) return DDT_ERR_INVALID_ARG;
+    if (A > kMaxAccept + 1) return DDT_ERR_UNSUPPORTED;
     if (!acc_nodes || !acc_len || !prefix_len || !src_row || !dst_pos || !status) return DDT_ERR_INVALID_ARG;
     if (Hkv < 1 || d < 1 || !dtype_ok(kv_dtype) || !k_tree || !v_tree || !k_pages || !v_pages)
         return DDT_ERR_INVALID_ARG;

@@ -16,6 +16,7 @@
 //                    (LSE and top-k), then one warp runs the best-first selection over a
 //                    shared-memory frontier, then the CTA renumbers breadth first and
 //                    writes the flattened tree and its bit-packed ancestor mask.
+#include <cuda.h>
 #include <float.h>
 #include <math.h>
 
@@ -528,35 +529,71 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
 // one file-scope device array instead of a caller-supplied workspace.
 //
 // The array is a fixed kStaticScratchBytes (4 MiB) on every GPU that loads this library,
-// held until the process exits.  Its device address is looked up once per device with
+// held until the process exits.  Its device address is looked up with
 // cudaGetSymbolAddress (on the host the symbol is only a stand-in, never a device
-// pointer); the first call on each device does that lookup, so make it before any
-// stream capture.  All calls on a device share the array: calls whose kernels overlap on
-// the GPU (different streams, or different host threads without ordering) race on it and
-// must be serialised by the caller.  The partial kernel writes every record the tree
-// kernel reads, so nothing in the array has to start at zero.
+// pointer) once per device and context: the address is cached with the id of the CUDA
+// context it was looked up in, and looked up again when the device's current context is
+// another one (after cudaDeviceReset, or once the primary context was released and made
+// again, the old address would point into an unloaded module).  The first call in each
+// context does that lookup, so make it before any stream capture.  All calls on a device
+// share the array: calls whose kernels overlap on the GPU (different streams, or
+// different host threads without ordering) race on it and must be serialised by the
+// caller.  The partial kernel writes every record the tree kernel reads, so nothing in
+// the array has to start at zero.
 namespace ddt {
 namespace {
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
 constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_build_scratch[kStaticScratchBytes];
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id;  // 0: not looked up yet
+    void* ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of g_build_scratch on the current device (looked up once per device).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current CUDA context (0 if none, or if the driver cannot
+// tell); ids are never reused within a process, unlike context handles.
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_cur = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_build_scratch in the current device's current context.
 cudaError_t static_scratch(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    const unsigned long long id = current_ctx_id();
+    ScratchAddr& c = g_scratch_addr[dev];
+    if (id == 0 || c.ctx_id != id) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_build_scratch);
+        e = cudaGetSymbolAddress(&p, g_build_scratch);  // makes the primary context current if none is
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        c.ptr = p;
+        c.ctx_id = current_ctx_id();  // 0 when the driver cannot tell: look up again next time
     }
-    *out = g_scratch_addr[dev];
+    *out = c.ptr;
     return cudaSuccess;
 }
 }  // namespace

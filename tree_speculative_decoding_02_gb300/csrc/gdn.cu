@@ -285,4 +285,107 @@ cudaError_t launch_gdn_tree(int L, int B, int N, int Hk, int Hv, int dk, int dv,
                                   o, status, st);
 }
 
+// ---------------------------------------------------------------------------------
+// Debugging aid: every node's branch-local state S_n formed the literal way the pages
+// describe ("DDTree on vLLM", "Why hybrid attention makes it hard": a node reads its
+// parent's recurrent state and writes its own scratch copy, never the committed one).
+// One CTA per (value head, request, layer) walks the nodes in row order (every parent
+// row precedes its children); thread j owns value row j of every state, so a child
+// reads back exactly the row its own thread wrote for the parent.  S_node is
+// [L][B][N][Hv][dv][dk]; rows of padding nodes (and of a malformed tree) are zeros.
+template <typename Tin>
+__global__ void __launch_bounds__(128) k_gdn_states(int B, int N, int Hk, int Hv, int dk, int dv, int K,
+                                                    const Tin* __restrict__ x, const Tin* __restrict__ conv_w,
+                                                    const Tin* __restrict__ conv_state,
+                                                    const float* __restrict__ beta, const float* __restrict__ decay,
+                                                    const float* __restrict__ S, const int32_t* __restrict__ parent,
+                                                    const int32_t* __restrict__ n_nodes, float* __restrict__ S_node) {
+    __shared__ float sk[128], sv[128], rnorm;
+    __shared__ int bad;
+    const int h = blockIdx.x, b = blockIdx.y, l = blockIdx.z, tid = threadIdx.x;
+    const int C = 2 * Hk * dk + Hv * dv, g = h / (Hv / Hk);
+    const long lb = (long)l * B + b;
+    const int nn = n_nodes[b];
+    if (tid == 0) {
+        int e = nn < 1 || nn > N;
+        for (int n = 0; n < nn && !e; ++n) {
+            const int p = parent[(long)b * N + n];
+            e = (n == 0) ? p != -1 : (p < 0 || p >= n);
+        }
+        bad = e;
+    }
+    __syncthreads();
+    const size_t mat = (size_t)dv * dk;
+    float* out_b = S_node + (size_t)lb * N * Hv * mat;
+    const int nv = bad ? 0 : nn;
+    const Tin* xb = x + lb * N * C;
+    const Tin* cs = conv_state + lb * (K - 1) * C;
+    const Tin* wl = conv_w + (long)l * C * K;
+    for (int n = 0; n < nv; ++n) {
+        // conv window of node n: its own ancestor path, newest last; taps past the root
+        // read the committed conv state (row K-2 newest)
+        int chain[8], dep = 0;
+        chain[0] = n;
+        for (int j = 1; j < K; ++j) {
+            const int pj = chain[j - 1] >= 0 ? parent[(long)b * N + chain[j - 1]] : -1;
+            chain[j] = pj;
+            if (pj >= 0) dep = j;
+        }
+        // the state update needs k (key head g) and v (value head h); q only enters o
+        for (int c = tid; c < dk + dv; c += 128) {
+            const int ch = c < dk ? Hk * dk + g * dk + c : 2 * Hk * dk + h * dv + (c - dk);
+            float acc = 0.f;
+            for (int j = 0; j < K; ++j) {
+                const int back = K - 1 - j;
+                const float in = back <= dep ? to_f32(xb[(long)chain[back] * C + ch])
+                                             : to_f32(cs[(long)(K - 1 - (back - dep)) * C + ch]);
+                acc = fmaf(to_f32(wl[(long)ch * K + j]), in, acc);
+            }
+            const float y = acc / (1.f + expf(-acc));  // SiLU
+            if (c < dk) sk[c] = y; else sv[c - dk] = y;
+        }
+        __syncthreads();
+        if (tid < 32) {  // k is L2-normalised per key head
+            float a = 0.f;
+            for (int i = tid; i < dk; i += 32) a = fmaf(sk[i], sk[i], a);
+            a = warp_sum(a);
+            if (tid == 0) rnorm = 1.f / sqrtf(a + 1e-6f);
+        }
+        __syncthreads();
+        const float rk = rnorm;
+        const float al = decay[(lb * N + n) * Hv + h], be = beta[(lb * N + n) * Hv + h];
+        const int p = parent[(long)b * N + n];
+        for (int j = tid; j < dv; j += 128) {
+            const float* Sp = p < 0 ? S + ((size_t)lb * Hv + h) * mat + (size_t)j * dk
+                                    : out_b + ((size_t)p * Hv + h) * mat + (size_t)j * dk;
+            float* Sn = out_b + ((size_t)n * Hv + h) * mat + (size_t)j * dk;
+            float pk = 0.f;
+            for (int i = 0; i < dk; ++i) pk = fmaf(Sp[i], sk[i] * rk, pk);
+            const float u = be * (sv[j] - al * pk);
+            for (int i = 0; i < dk; ++i) Sn[i] = fmaf(al, Sp[i], u * sk[i] * rk);
+        }
+        __syncthreads();
+    }
+    for (int n = nv; n < N; ++n)
+        for (size_t e = tid; e < mat; e += 128) out_b[((size_t)n * Hv + h) * mat + e] = 0.f;
+}
+
+cudaError_t launch_gdn_states(int L, int B, int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in,
+                              const void* x, const void* conv_w, const void* conv_state, const float* beta,
+                              const float* decay, const float* S, const int32_t* parent, const int32_t* n_nodes,
+                              float* S_node, cudaStream_t st) {
+    if (dk > 128 || dv > 128 || K > 8) return cudaErrorInvalidValue;
+    dim3 grid(Hv, B, L);
+    if (in == DDT_BF16)
+        k_gdn_states<__nv_bfloat16><<<counted(grid), 128, 0, st>>>(
+            B, N, Hk, Hv, dk, dv, K, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(conv_w),
+            static_cast<const __nv_bfloat16*>(conv_state), beta, decay, S, parent, n_nodes, S_node);
+    else
+        k_gdn_states<float><<<counted(grid), 128, 0, st>>>(B, N, Hk, Hv, dk, dv, K, static_cast<const float*>(x),
+                                                          static_cast<const float*>(conv_w),
+                                                          static_cast<const float*>(conv_state), beta, decay, S,
+                                                          parent, n_nodes, S_node);
+    return cudaGetLastError();
+}
+
 }  // namespace ddt

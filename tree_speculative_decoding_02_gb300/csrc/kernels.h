@@ -14,6 +14,7 @@ constexpr int kMaxDepth = 64;      // deepest tree the build supports
 constexpr int kMaxTopK = 32;
 constexpr int kMaxBudget = 1023;
 constexpr int kMaxRows = 1024;     // N = budget + 1
+constexpr int kMaxAccept = kMaxDepth;  // accepted rows a commit takes (acc_len <= tree depth)
 constexpr int kGdnMaxNodes = 128;
 constexpr int kGdnMaxDepth = 32;
 
@@ -71,6 +72,11 @@ cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype 
                           const float* S, const int32_t* parent, const int32_t* n_nodes, void* o, int32_t* status,
                           cudaStream_t st);
 size_t gdn_smem_bytes(int N, int dk, int dv);
+// every node's branch-local state, the literal way (debugging aid for small trees)
+cudaError_t launch_gdn_states(int L, int B, int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in,
+                              const void* x, const void* conv_w, const void* conv_state, const float* beta,
+                              const float* decay, const float* S, const int32_t* parent, const int32_t* n_nodes,
+                              float* S_node, cudaStream_t st);
 cudaError_t launch_gdn_tree(int L, int B, int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in,
                             ddt_dtype out, const void* x, const void* conv_w, const void* conv_state,
                             const float* beta, const float* decay, const float* S, const int32_t* parent,

@@ -11,7 +11,6 @@ callers that manage memory themselves can pass `out=` dicts of preallocated tens
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 
@@ -40,7 +39,7 @@ _SIGS = {
     "ddt_tree_attn_workspace": ([_c_int] * 7, _c_size),
     "ddt_tree_attn": ([_c_int] * 9 + [_c_p] * 8 + [_c_float, _c_p, _c_p, _c_p, _c_size, _c_p], _c_int),
     "ddt_tree_gdn_workspace": ([_c_int] * 7, _c_size),
-    "ddt_tree_gdn": ([_c_int] * 10 + [_c_p] * 10 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_tree_gdn": ([_c_int] * 10 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_walk_accept_workspace": ([_c_int] * 3, _c_size),
     "ddt_walk_accept": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_walk_accept_flat": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
@@ -192,9 +191,10 @@ def ddt_build_tree_noalloc(draft_logits, root_token, prefix_len, top_k: int, bud
 
 
 # ----------------------------------------------------------------------- attention
-def ddt_tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc, *, scale=None,
+def ddt_tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc, *, scale: float,
                   out_dtype=None, out=None, status=None, workspace=None):
-    """q [L][B][N][Hq][d]; k/v_tree [L][B][N][Hkv][d]; k/v_cache [L][B][Hkv][Pcap][d]."""
+    """q [L][B][N][Hq][d]; k/v_tree [L][B][N][Hkv][d]; k/v_cache [L][B][Hkv][Pcap][d];
+    scale: the softmax scale, passed through as given (1/sqrt(d) for standard attention)."""
     lib = _gpu()
     L, B, N, Hq, d = q.shape
     Hkv = k_tree.shape[3]
@@ -212,7 +212,7 @@ def ddt_tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc,
     o = out if out is not None else torch.empty((L, B, N, Hq, d), dtype=out_dtype, device=q.device)
     _need(o, (L, B, N, Hq, d), out_dtype, "o")
     st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=q.device)
-    scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    scale = float(scale)
     need = lib.ddt_tree_attn_workspace(L, B, N, Hq, Hkv, d, Pcap)
     ws = workspace if workspace is not None else _ws(need, q.device)
     rc = lib.ddt_tree_attn(L, B, N, Hq, Hkv, d, Pcap, _DT[dt], _DT[out_dtype], _ptr(q), _ptr(k_tree), _ptr(v_tree),
@@ -223,9 +223,9 @@ def ddt_tree_attn(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc,
 
 
 def ddt_tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, prefix_len, n_nodes, anc, *,
-                        scale=None, out_dtype=None, out=None, status=None, workspace=None):
+                        scale: float, out_dtype=None, out=None, status=None, workspace=None):
     """q [L][B][N][Hq][d]; k/v_tree [L][B][N][Hkv][d]; k/v_pages [L][num_pages][Hkv][page_size][d] (bf16);
-    block_table [B][max_pages] int32."""
+    block_table [B][max_pages] int32; scale as in ddt_tree_attn."""
     lib = _gpu()
     L, B, N, Hq, d = q.shape
     Hkv = k_tree.shape[3]
@@ -245,7 +245,7 @@ def ddt_tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, prefix
     o = out if out is not None else torch.empty((L, B, N, Hq, d), dtype=out_dtype, device=q.device)
     _need(o, (L, B, N, Hq, d), out_dtype, "o")
     st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=q.device)
-    scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    scale = float(scale)
     need = lib.ddt_tree_attn_paged_workspace(L, B, N, Hq, Hkv, d, page, max_pages)
     ws = workspace if workspace is not None else _ws(need, q.device)
     rc = lib.ddt_tree_attn_paged(L, B, N, Hq, Hkv, d, page, num_pages, max_pages, _DT[dt], _DT[out_dtype], _ptr(q),
@@ -274,9 +274,10 @@ def ddt_rope_tree(q, k_tree, position, n_nodes, *, rot_dim=None, theta=10000.0):
 
 # ----------------------------------------------------------------------------- GDN
 def ddt_tree_gdn(x, conv_w, conv_state, beta, decay, S, parent, n_nodes, *, Hk: int, out_dtype=None, out=None,
-                 status=None, workspace=None):
+                 status=None, workspace=None, S_node_debug=None):
     """x [L][B][N][C]; conv_w [L][C][K]; conv_state [L][B][K-1][C]; beta/decay [L][B][N][Hv] fp32;
-    S [L][B][Hv][dv][dk] fp32; parent [B][N]; n_nodes [B]."""
+    S [L][B][Hv][dv][dk] fp32; parent [B][N]; n_nodes [B].  S_node_debug: optional
+    [L][B][N][Hv][dv][dk] fp32 tensor that receives every node's own state (small trees)."""
     lib = _gpu()
     L, B, N, C = x.shape
     Hv, dv, dk = S.shape[2], S.shape[3], S.shape[4]
@@ -296,11 +297,13 @@ def ddt_tree_gdn(x, conv_w, conv_state, beta, decay, S, parent, n_nodes, *, Hk: 
     o = out if out is not None else torch.empty((L, B, N, Hv, dv), dtype=out_dtype, device=x.device)
     _need(o, (L, B, N, Hv, dv), out_dtype, "o")
     st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=x.device)
+    if S_node_debug is not None:
+        _need(S_node_debug, (L, B, N, Hv, dv, dk), torch.float32, "S_node_debug")
     need = lib.ddt_tree_gdn_workspace(L, B, N, Hk, Hv, dk, dv)
     ws = workspace if workspace is not None else _ws(need, x.device)
     rc = lib.ddt_tree_gdn(L, B, N, Hk, Hv, dk, dv, K, _DT[dt], _DT[out_dtype], _ptr(x), _ptr(conv_w),
                           _ptr(conv_state), _ptr(beta), _ptr(decay), _ptr(S), _ptr(parent), _ptr(n_nodes), _ptr(o),
-                          _ptr(st), _ptr(ws), ws.numel(), _stream())
+                          _ptr(S_node_debug), _ptr(st), _ptr(ws), ws.numel(), _stream())
     _check(rc, "ddt_tree_gdn")
     return {"o": o, "status": st}
 
