@@ -48,6 +48,7 @@ constexpr float kTau = 8.f;  // rescale O only when the row max grows by more th
 
 struct TcParams {
     int L, B, N, Hq, Hkv, G, MT, S, chunk, Pcap, W;
+    int MP;  // pair kernel: 256-row tiles per (layer, request, kv head); MT = 2 MP there
     // paged prefix caches: page_rows positions a page, block_table [B][max_pages] of
     // physical pages out of num_pages (paged == 0: one contiguous slab per request)
     int paged, page_rows, num_pages, max_pages;
@@ -526,6 +527,502 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && *abort_flag) atomicExch(p.status + b, (int)DDT_ERR_TIMEOUT);
 }
 
+// ------------------------------------------------------------------------------------
+// The CTA-pair kernel (head sizes 128 and 256).  Two CTAs on a pair of SMs (a cluster of
+// two) share each MMA (tcgen05 cta_group::2): one 256-row M tile, 128 query rows per
+// CTA, and 128 keys per tile, so S = Q K^T runs as N = 128 MMAs at the full tensor rate
+// and every MMA does twice the work of a one-SM instruction.  Each CTA keeps its own
+// 128 query rows in shared memory (the A operand), loads half of every key tile (64 keys
+// x d for Q K^T, all 128 keys x d/2 value columns for P V), and receives its rows of S
+// and O in its own tensor memory: S/P double buffer in columns [0, 256), O in
+// [256, 256 + d).  Roles:
+//   warp 0      TMA producer in each CTA (its own halves).  K halves report to the even
+//               CTA's barrier (the MMA waits there for both); V halves to the CTA's own,
+//               which its softmax warps wait on.
+//   warp 1      MMA issuer, even CTA only.
+//   warps 4-11  softmax, as in k_attn_tc but over 64 keys per thread; once P_j is in
+//               tensor memory and the CTA's V_j half has landed (padding rows zeroed),
+//               each warp arrives on the even CTA's P barrier: that arrival certifies
+//               both P and V of the CTA.
+// Every wait is bounded; the even CTA drains both CTAs' K loads, each CTA its own V loads,
+// and a cluster barrier keeps either CTA from leaving while the pair may still touch it.
+namespace {
+constexpr int kPN = 128;  // keys per tile of the pair kernel
+
+template <int D>
+struct Tc2Cfg {
+    static constexpr int kBlocks = D / 64;
+    static constexpr int kQBytes = 128 * D * 2;     // this CTA's query rows
+    static constexpr int kStageBytes = 64 * D * 2;  // a K half (64 keys x D) or a V half (128 keys x D/2)
+    static constexpr int kStages = D == 256 ? 4 : 8;
+    static constexpr int kOCol = 2 * kPN;
+    static constexpr int kBarBytes = 512;
+    static constexpr int kXchBytes = 3072;
+    static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + kBarBytes + kXchBytes;
+};
+
+__device__ __forceinline__ Tile tile2_of(int j, int n_pre, int c0, int c1, bool ragged) {
+    Tile t;
+    if (j < n_pre) {
+        t.tree = 0;
+        t.lo = c0 + j * kPN;
+        t.y = (j == n_pre - 1 && ragged) ? c1 - kPN : t.lo;
+    } else {
+        t.tree = 1;
+        t.y = (j - n_pre) * kPN;
+        t.lo = 0;
+    }
+    return t;
+}
+
+// visibility bits of 32 consecutive keys starting at key k0 of a prefix tile
+__device__ __forceinline__ uint32_t prefix_vis(int lo, int c1, int k0) {
+    const int skip = lo - k0, lim = c1 - k0;
+    uint32_t v = skip <= 0 ? ~0u : (skip >= 32 ? 0u : (~0u << skip));
+    v &= lim >= 32 ? ~0u : (lim <= 0 ? 0u : ((1u << lim) - 1u));
+    return v;
+}
+}  // namespace
+
+template <int D, typename Tout>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_attn_tc2(const TcParams p, const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+               const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+    using Cfg = Tc2Cfg<D>;
+    constexpr int kStages = Cfg::kStages;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* sQ = base;
+    unsigned char* sRing = base + Cfg::kQBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * Cfg::kStageBytes);
+    uint64_t* full = bars;                 // [kStages] even: K halves of both CTAs (even CTA); odd: own V half
+    uint64_t* sfree = bars + kStages;      // [kStages] the MMAs that read the stage are done (both CTAs)
+    uint64_t* s_full = bars + 2 * kStages; // [2] S_j in tensor memory (both CTAs)
+    // [2] P_j and V_j ready: in the even CTA its 8 softmax warps plus one arrival forwarded
+    // from the odd CTA; in the odd CTA its own 8 warps (which a forwarding thread waits on)
+    uint64_t* p_full = s_full + 2;
+    uint64_t* drain = p_full + 2;
+    uint64_t* o_final = drain + 1;         // single phase: O complete (both CTAs)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    float* xch = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bars) + Cfg::kBarBytes);
+
+    const uint32_t rank = tc::cluster_ctarank();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int x = blockIdx.x >> 1;
+    const int s = x % p.S;
+    x /= p.S;
+    const int mp = x % p.MP;
+    x /= p.MP;
+    const int g = x % p.Hkv;
+    const int l = x / p.Hkv;
+    const int b = p.perm[blockIdx.y];
+    const long lb = (long)l * p.B + b;
+    const int row0 = mp * 256 + (int)rank * 128;  // this CTA's first query row
+    const int P = p.prefix_len[b], nn = p.n_nodes[b];
+    bool bad = P < 0 || P > p.Pcap || nn < 1 || nn > p.N;
+    int bad_table = 0;
+    if (p.paged && !bad) {  // every page the prefix uses must exist
+        const int np = (P + p.page_rows - 1) / p.page_rows;
+        for (int i = tid; i < np; i += kThreads) {
+            const int pg = p.block_table[(long)b * p.max_pages + i];
+            bad_table |= (pg < 0 || pg >= p.num_pages);
+        }
+    }
+    bad_table = __syncthreads_or(bad_table);
+    bad = bad || bad_table;
+    const long prow0 = ((((long)s * p.L + l) * p.B + b) * p.Hkv + g) * (long)(p.MP * 256) + row0;
+    // (both CTAs of a pair see the same request, so they leave here together)
+    if (bad) {
+        if (tid == 0 && rank == 0 && s == 0 && mp == 0 && g == 0 && l == 0)
+            p.status[b] = (P < 0 || P > p.Pcap) ? DDT_ERR_CAPACITY : (bad_table ? DDT_ERR_INVALID_ARG : DDT_ERR_TREE);
+        if (p.S == 1) {
+            for (int e = tid; e < 128 * D; e += kThreads) {
+                const int R = row0 + e / D;
+                if (R >= p.N * p.G) continue;
+                const int node = R / p.G, h = g * p.G + R % p.G;
+                static_cast<Tout*>(p.o)[((lb * p.N + node) * p.Hq + h) * D + e % D] = from_f32<Tout>(0.f);
+            }
+        } else if (tid < 128) {
+            p.part_ml[prow0 + tid] = make_float2(-INFINITY, 0.f);
+        }
+        return;
+    }
+    const int c0 = s * p.chunk;
+    const int s_last = P > 0 ? (P - 1) / p.chunk : 0;
+    int n_pre = 0, c1 = c0;
+    if (c0 < P) {
+        c1 = min(c0 + p.chunk, P);
+        n_pre = (c1 - c0 + kPN - 1) / kPN;
+    }
+    const int n_tree = (s == s_last) ? (nn + kPN - 1) / kPN : 0;
+    const int T = n_pre + n_tree;
+    const bool ragged = !p.paged && ((c1 - c0) % kPN) != 0;
+    if (T == 0) {
+        if (tid < 128) p.part_ml[prow0 + tid] = make_float2(-INFINITY, 0.f);
+        return;
+    }
+
+    // ---- setup: barriers, tensor memory (allocated for the pair), Q rows into shared memory
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(full + i, 1);
+            tc::mbar_init(sfree + i, 1);
+        }
+        tc::mbar_init(s_full, 1);
+        tc::mbar_init(s_full + 1, 1);
+        tc::mbar_init(p_full, rank == 0 ? 9 : 8);
+        tc::mbar_init(p_full + 1, rank == 0 ? 9 : 8);
+        tc::mbar_init(drain, 1);
+        tc::mbar_init(o_final, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc2(tmem_slot, 512);
+        tc::tmem_relinquish2();
+    }
+    if (tid == 64) {
+        tc::prefetch_tmap(&tm_kc);
+        tc::prefetch_tmap(&tm_vc);
+        tc::prefetch_tmap(&tm_kt);
+        tc::prefetch_tmap(&tm_vt);
+    }
+    // Q: 128 rows x D bf16, K-major with the 128-byte swizzle (64-column blocks of 128 rows)
+    for (int e = tid; e < 128 * (D / 8); e += kThreads) {
+        const int r = e / (D / 8), c = e % (D / 8);
+        const int R = row0 + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (R < p.N * p.G) {
+            const int node = R / p.G, h = g * p.G + R % p.G;
+            if (node < nn) v = __ldg(reinterpret_cast<const uint4*>(p.q + ((lb * p.N + node) * p.Hq + h) * D) + c);
+        }
+        *reinterpret_cast<uint4*>(sQ + (c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    }
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
+    tc::cluster_sync();  // both CTAs' barriers, tensor memory and Q before the pipeline starts
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            const int grp = (int)((lb * p.Hkv) + g);
+            const uint32_t full_c = tc::mapa_shared(tc::smem_u32(full), 0);  // the even CTA's K barriers
+            int issued = 0;
+            for (int j = 0; j < T && !*abort_flag; ++j) {
+                const Tile t = tile2_of(j, n_pre, c0, c1, ragged);
+                if (j + 2 < T && !p.paged) {
+                    // warm L2 with tile j + 2's halves: their stages free up only as tile j's
+                    // MMAs finish, and the load must then land within about one tile's time
+                    const Tile t2 = tile2_of(j + 2, n_pre, c0, c1, ragged);
+                    const int yk = t2.y + 64 * (int)rank, xv = (int)rank * (D / 2);
+#pragma unroll
+                    for (int blk = 0; blk < Cfg::kBlocks; ++blk) {
+                        if (!t2.tree) tc::tma_prefetch_3d(&tm_kc, blk * 64, yk, grp);
+                        else tc::tma_prefetch_4d(&tm_kt, blk * 64, g, yk, (int)lb);
+                    }
+#pragma unroll
+                    for (int blk = 0; blk < Cfg::kBlocks / 2; ++blk) {
+                        if (!t2.tree) tc::tma_prefetch_3d(&tm_vc, xv + blk * 64, t2.y, grp);
+                        else tc::tma_prefetch_4d(&tm_vt, xv + blk * 64, g, t2.y, (int)lb);
+                    }
+                }
+                bool ok = true;
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int u = 2 * j + kv, st = u % kStages;
+                    ok = tc::mbar_wait(sfree + st, ((u / kStages) & 1) ^ 1, abort_flag);
+                    if (!ok) break;
+                    unsigned char* dst = sRing + st * Cfg::kStageBytes;
+                    if (kv == 0) {
+                        // K half: keys [y + 64 rank, +64), all D columns
+                        if (rank == 0) tc::mbar_expect_tx(full + st, 2 * Cfg::kStageBytes);
+                        const uint32_t cb = full_c + st * 8;
+                        const int y = t.y + 64 * (int)rank;
+                        if (!t.tree && p.paged) {
+                            const int sub = min(64, p.page_rows), last = (P - 1) / p.page_rows;
+                            for (int r0 = 0; r0 < 64; r0 += sub) {
+                                const int pos = y + r0;
+                                const int lp = min(pos / p.page_rows, last);
+                                const int phys = p.block_table[(long)b * p.max_pages + lp];
+                                const int plane = (int)(((long)l * p.num_pages + phys) * p.Hkv + g);
+#pragma unroll
+                                for (int blk = 0; blk < Cfg::kBlocks; ++blk)
+                                    tc::tma_load_3d_pair(dst + blk * (64 * 128) + r0 * 128, &tm_kc, cb, blk * 64,
+                                                         pos % p.page_rows, plane);
+                            }
+                        } else {
+#pragma unroll
+                            for (int blk = 0; blk < Cfg::kBlocks; ++blk) {
+                                if (!t.tree)
+                                    tc::tma_load_3d_pair(dst + blk * (64 * 128), &tm_kc, cb, blk * 64, y, grp);
+                                else
+                                    tc::tma_load_4d_pair(dst + blk * (64 * 128), &tm_kt, cb, blk * 64, g, y, (int)lb);
+                            }
+                        }
+                    } else {
+                        // V half: keys [y, +128), value columns [rank D/2, (rank + 1) D/2)
+                        tc::mbar_expect_tx(full + st, Cfg::kStageBytes);
+                        const int xc = (int)rank * (D / 2);
+                        if (!t.tree && p.paged) {
+                            const int sub = min(kPN, p.page_rows), last = (P - 1) / p.page_rows;
+                            for (int r0 = 0; r0 < kPN; r0 += sub) {
+                                const int pos = t.y + r0;
+                                const int lp = min(pos / p.page_rows, last);
+                                const int phys = p.block_table[(long)b * p.max_pages + lp];
+                                const int plane = (int)(((long)l * p.num_pages + phys) * p.Hkv + g);
+#pragma unroll
+                                for (int blk = 0; blk < Cfg::kBlocks / 2; ++blk)
+                                    tc::tma_load_3d(dst + blk * (kPN * 128) + r0 * 128, &tm_vc, full + st,
+                                                    xc + blk * 64, pos % p.page_rows, plane);
+                            }
+                        } else {
+#pragma unroll
+                            for (int blk = 0; blk < Cfg::kBlocks / 2; ++blk) {
+                                if (!t.tree)
+                                    tc::tma_load_3d(dst + blk * (kPN * 128), &tm_vc, full + st, xc + blk * 64, t.y,
+                                                    grp);
+                                else
+                                    tc::tma_load_4d(dst + blk * (kPN * 128), &tm_vt, full + st, xc + blk * 64, g, t.y,
+                                                    (int)lb);
+                            }
+                        }
+                    }
+                    issued = u + 1;
+                }
+                if (!ok) break;
+            }
+            // drain: the even CTA waits for every K stage (both halves) and its V stages,
+            // the odd CTA for its own V stages
+            for (int u = max(0, issued - kStages); u < issued; ++u)
+                if (rank == 0 || (u & 1)) drain_wait(full + u % kStages, (u / kStages) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc_qk = tc::idesc_bf16(256, kPN, false, false);
+            constexpr uint32_t idesc_pv = tc::idesc_bf16(256, D, false, true);
+            const uint32_t sRa = tc::smem_u32(sRing);
+            const uint64_t qdesc0 = tc::desc_sw128(tc::smem_u32(sQ), 16, 1024);
+            const uint64_t kdesc0 = tc::desc_sw128(sRa, 16, 1024);
+            const uint64_t vdesc0 = tc::desc_sw128(sRa, kPN * 128, 1024);
+            auto pv = [&](int i) -> bool {
+                // P_i and both V_i halves (padding rows zeroed) are ready once all 16
+                // softmax warps of the pair have arrived
+                if (!tc::mbar_wait_cluster(p_full + (i & 1), (i >> 1) & 1, abort_flag)) return false;
+                tc::tc_fence_after();
+                const int st = (2 * i + 1) % kStages;
+                const uint64_t vd = vdesc0 + static_cast<uint64_t>((st * Cfg::kStageBytes) >> 4);
+                const uint32_t pa = tmem + (i & 1) * kPN;
+#pragma unroll
+                for (int q = 0; q < 2 * (kPN / 16); ++q) {  // P_hi k-steps, then P_lo k-steps
+                    const int part = q / (kPN / 16), kk = q % (kPN / 16);
+                    tc::mma2_f16_ts(tmem + Cfg::kOCol, pa + part * (kPN / 2) + kk * 8,
+                                    vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (i > 0 || q > 0) ? 1u : 0u);
+                }
+                tc::mma2_commit_mc(sfree + st, 3);  // V stage free; also: O holds tile i
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < T && ok; ++j) {
+                const int u = 2 * j, st = u % kStages;
+                if (!tc::mbar_wait_cluster(full + st, (u / kStages) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint64_t kd = kdesc0 + static_cast<uint64_t>((st * Cfg::kStageBytes) >> 4);
+                const uint32_t sd = tmem + (j & 1) * kPN;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * (64 * 128) + (kk & 3) * 32;
+                    tc::mma2_f16_ss(sd, qdesc0 + static_cast<uint64_t>(qoff >> 4),
+                                    kd + static_cast<uint64_t>(koff >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                tc::mma2_commit_mc(sfree + st, 3);       // K stage free in both CTAs
+                tc::mma2_commit_mc(s_full + (j & 1), 3); // S_j ready in both CTAs
+                if (j >= 1) ok = pv(j - 1);
+            }
+            if (ok && pv(T - 1)) tc::mma2_commit_mc(o_final, 3);
+            tc::mma2_commit_mc(drain, 1);
+            drain_wait(drain, 0);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------- forwarder (odd CTA)
+        // one cluster-scope arrival a tile on the even CTA's P barrier, once this CTA's 8
+        // softmax warps have arrived locally (cheaper than 8 remote arrivals on their path)
+        if (lane == 0 && rank == 1) {
+            const uint32_t pf_remote = tc::mapa_shared(tc::smem_u32(p_full), 0);
+            for (int j = 0; j < T; ++j) {
+                if (!tc::mbar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag)) break;
+                tc::mbar_arrive_cluster(pf_remote + (j & 1) * 8);
+            }
+        }
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------------ softmax
+        const int hf = (warp - 4) >> 2, ws = (warp - 4) & 3, r = 32 * ws + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * ws) << 16;
+        const int R = row0 + r;
+        const bool in_rows = R < p.N * p.G;
+        const int node = in_rows ? R / p.G : 0;
+        const int h = g * p.G + (in_rows ? R % p.G : 0);
+        const bool live = in_rows && node < nn;
+        const uint32_t* anc_row = p.anc + ((long)b * p.N + node) * p.W;
+        float m_used = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < T; ++j) {
+            const Tile t = tile2_of(j, n_pre, c0, c1, ragged);
+            if (ok) ok = tc::mbar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag);
+            ok = __all_sync(kFull, ok);
+            float sv[64];  // scores in log2 units, -inf where the key is not visible
+            float mtile = -INFINITY;
+            if (ok) {
+                tc::tc_fence_after();
+                const int k0 = t.y + 64 * hf;  // this half's first key
+                uint32_t vis[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    if (!t.tree) {
+                        vis[w] = prefix_vis(t.lo, c1, k0 + 32 * w);
+                    } else {
+                        const int wd = (t.y >> 5) + 2 * hf + w;
+                        vis[w] = (live && wd < p.W) ? anc_row[wd] : 0u;
+                    }
+                }
+                const bool all_vis = __all_sync(kFull, (vis[0] & vis[1]) == ~0u);
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    uint32_t sr[32];
+                    tc::tmem_ld32(tmem + lane_base + (j & 1) * kPN + 64 * hf + 32 * w, sr);
+                    tc::tmem_wait_ld();
+                    if (all_vis) {  // every key of the half visible (nearly every prefix tile)
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) sv[32 * w + c] = __uint_as_float(sr[c]) * p.scale_log2;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            sv[32 * w + c] = ((vis[w] >> c) & 1u) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) mtile = fmaxf(mtile, sv[32 * w + c]);
+                }
+            }
+            float* xm = xch + (j & 1) * 256;
+            xm[hf * 128 + r] = mtile;
+            tc::named_bar(1, 256);
+            mtile = fmaxf(mtile, xm[(hf ^ 1) * 128 + r]);
+            if (!ok) continue;
+            const bool grow = mtile > m_used + kTau;
+            const bool need = grow && (m_used != -INFINITY);
+            if (__any_sync(kFull, need)) {
+                // O must hold tile j - 1 before it is rescaled: wait for that tile's P.V
+                const int u = 2 * (j - 1) + 1;
+                ok = __all_sync(kFull, tc::mbar_wait(sfree + u % kStages, (u / kStages) & 1, abort_flag));
+                if (!ok) continue;
+                tc::tc_fence_after();
+                const float f = need ? tc::ex2(m_used - mtile) : 1.f;
+#pragma unroll 1
+                for (int cb = hf * (D / 2); cb < (hf + 1) * (D / 2); cb += 32) {
+                    uint32_t ov[32];
+                    tc::tmem_ld32(tmem + lane_base + Cfg::kOCol + cb, ov);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+                    tc::tmem_st32(tmem + lane_base + Cfg::kOCol + cb, ov);
+                }
+                tc::tmem_wait_st();
+                if (need) l_run *= f;
+            }
+            if (grow) m_used = mtile;
+            float sum = 0.f;
+            // a row that has seen no visible key yet has no reference: its P is all zeros
+            const float mref = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                uint32_t phi[16], plo[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    // ex2(-inf) = 0 for keys that are not visible.  P = P_hi + P_lo with P_hi
+                    // the top 16 bits of P (exact as bf16) and P_lo = bf16(P - P_hi): the
+                    // pair carries P to ~2^-16 relative
+                    const float a = tc::ex2(sv[32 * w + c] - mref);
+                    const float bb = tc::ex2(sv[32 * w + c + 1] - mref);
+                    sum += a + bb;
+                    const uint32_t ah = __float_as_uint(a) & 0xffff0000u, bh = __float_as_uint(bb) & 0xffff0000u;
+                    phi[c >> 1] = (ah >> 16) | bh;
+                    plo[c >> 1] = pack_bf16(a - __uint_as_float(ah), bb - __uint_as_float(bh));
+                }
+                // P_hi in columns [0, 64) of the buffer, P_lo in [64, 128); this half's 64
+                // keys are 32 packed columns of each
+                tc::tmem_st16(tmem + lane_base + (j & 1) * kPN + 32 * hf + 16 * w, phi);
+                tc::tmem_st16(tmem + lane_base + (j & 1) * kPN + kPN / 2 + 32 * hf + 16 * w, plo);
+            }
+            l_run += sum;
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            // this CTA's V half of tile j: wait for it, and zero the rows the MMA must not
+            // see (padding tree nodes may hold anything, even NaN, and a zero P does not
+            // cancel NaN; paged tiles read rows past the prefix)
+            {
+                const int u = 2 * j + 1, st = u % kStages;
+                ok = __all_sync(kFull, tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag));
+                const int first = t.tree ? max(0, nn - t.y) : (t.y + kPN > c1 ? c1 - t.y : kPN);
+                if (ok && first < kPN) {
+                    unsigned char* vst = sRing + st * Cfg::kStageBytes;
+                    const int per_blk = (kPN - first) * 8;  // 16-byte chunks of the zeroed rows of a block
+                    for (int e = hf * 128 + r; e < per_blk * (Cfg::kBlocks / 2); e += 256) {
+                        const int blk = e / per_blk, rem = e % per_blk;
+                        *reinterpret_cast<uint4*>(vst + blk * (kPN * 128) + (first + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    tc::fence_proxy_async();
+                }
+            }
+            __syncwarp();
+            if (!ok) continue;
+            if (lane == 0) tc::mbar_arrive(p_full + (j & 1));
+        }
+        if (ok) ok = tc::mbar_wait(o_final, 0, abort_flag);
+        ok = __all_sync(kFull, ok);
+        xch[512 + hf * 128 + r] = l_run;
+        tc::named_bar(1, 256);
+        const float l_tot = l_run + xch[512 + (hf ^ 1) * 128 + r];
+        if (ok) {
+            tc::tc_fence_after();
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+#pragma unroll 1
+            for (int cb = hf * (D / 2); cb < (hf + 1) * (D / 2); cb += 32) {
+                uint32_t ov[32];
+                tc::tmem_ld32(tmem + lane_base + Cfg::kOCol + cb, ov);
+                tc::tmem_wait_ld();
+                float f[32];
+                if (p.S == 1) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = live ? __uint_as_float(ov[i]) * inv : 0.f;
+                    if (in_rows)
+                        store_row32<Tout>(static_cast<Tout*>(p.o) + ((lb * p.N + node) * p.Hq + h) * D + cb, f);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(ov[i]);
+                    store_row32<float>(p.part_o + (prow0 + r) * D + cb, f);
+                }
+            }
+            if (p.S > 1 && hf == 0) p.part_ml[prow0 + r] = make_float2(m_used, l_tot);
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::cluster_sync();  // neither CTA frees tensor memory or leaves while the pair may touch it
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc2(tmem, 512);
+    }
+    if (tid == 0 && *abort_flag) atomicExch(p.status + b, (int)DDT_ERR_TIMEOUT);
+}
+
 // Combines split-KV partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 template <int D, typename Tout>
 __global__ void __launch_bounds__(D) k_attn_merge(const TcParams p) {
@@ -623,16 +1120,22 @@ void choose_split(int L, int B, int Hkv, int MT, int Pcap, int n_sms, int* S, in
 
 }  // namespace
 
+// head sizes the CTA-pair kernel takes (the others use k_attn_tc)
+static bool pair_kernel(int d) { return d == 128 || d == 256; }
+
 size_t attn_tc_ws_bytes(int L, int B, int N, int Hq, int Hkv, int d, int Pcap) {
     const int G = Hq / Hkv;
-    const int MT = (N * G + kBM - 1) / kBM;
-    int S, chunk;
-    choose_split(L, B, Hkv, MT, Pcap, 256, &S, &chunk);  // 256 bounds the SM count from above
+    // rows of the split-KV partials: 128-row tiles, or 256-row pair tiles (the pair kernel
+    // splits by SM pairs); the workspace covers both
+    const int MT = (N * G + kBM - 1) / kBM, MP = (N * G + 255) / 256;
+    int S1, S2, chunk;
+    choose_split(L, B, Hkv, MT, Pcap, 256, &S1, &chunk);  // 256 bounds the SM count from above
+    choose_split(L, B, Hkv, MP, Pcap, 128, &S2, &chunk);
     size_t bytes = ((size_t)B * sizeof(int32_t) + 255) & ~(size_t)255;
-    if (S > 1) {
-        const size_t rows = (size_t)S * L * B * Hkv * MT * kBM;
-        bytes += rows * d * sizeof(float) + rows * sizeof(float2);
-    }
+    const size_t rows1 = S1 > 1 ? (size_t)S1 * L * B * Hkv * MT * kBM : 0;
+    const size_t rows2 = S2 > 1 ? (size_t)S2 * L * B * Hkv * MP * 256 : 0;
+    const size_t rows = rows1 > rows2 ? rows1 : rows2;
+    bytes += rows * d * sizeof(float) + rows * sizeof(float2);
     return bytes + 256;
 }
 
@@ -645,6 +1148,21 @@ static cudaError_t attn_tc_go(const TcParams& prm, const CUtensorMap* maps, cuda
     if (e != cudaSuccess) return e;
     dim3 grid(prm.S * prm.MT * prm.Hkv * prm.L, prm.B);
     k_attn_tc<D, Tout><<<counted(grid), kThreads, Cfg::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3]);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (prm.S > 1) {
+        k_attn_merge<D, Tout><<<counted(dim3(prm.N * prm.Hq, prm.L * prm.B)), D, 0, st>>>(prm);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+template <int D, typename Tout>
+static cudaError_t attn_tc2_go(const TcParams& prm, const CUtensorMap* maps, cudaStream_t st) {
+    using Cfg = Tc2Cfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tc2<D, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(2 * prm.S * prm.MP * prm.Hkv * prm.L, prm.B);
+    k_attn_tc2<D, Tout><<<counted(grid), kThreads, Cfg::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3]);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (prm.S > 1) {
         k_attn_merge<D, Tout><<<counted(dim3(prm.N * prm.Hq, prm.L * prm.B)), D, 0, st>>>(prm);
@@ -672,7 +1190,18 @@ static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, i
     prm.MT = (N * prm.G + kBM - 1) / kBM;
     prm.Pcap = Pcap;
     prm.W = (N + 31) / 32;
-    choose_split(L, B, Hkv, prm.MT, Pcap, sm_count(), &prm.S, &prm.chunk);
+    const bool pair = pair_kernel(d);
+    prm.MP = (N * prm.G + 255) / 256;
+    if (pair) {
+        // the pair kernel's units are SM pairs of 256 query rows; its partial rows are laid
+        // out as 2 MP tiles of 128 for the merge
+        choose_split(L, B, Hkv, prm.MP, Pcap, sm_count() / 2, &prm.S, &prm.chunk);
+        prm.chunk = ((prm.chunk + kPN - 1) / kPN) * kPN;
+        prm.S = Pcap > 0 ? (Pcap + prm.chunk - 1) / prm.chunk : 1;
+        prm.MT = 2 * prm.MP;
+    } else {
+        choose_split(L, B, Hkv, prm.MT, Pcap, sm_count(), &prm.S, &prm.chunk);
+    }
     if (ws_bytes < attn_tc_ws_bytes(L, B, N, Hq, Hkv, d, Pcap)) return cudaErrorInvalidValue;
     unsigned char* w = static_cast<unsigned char*>(ws);
     int32_t* perm = reinterpret_cast<int32_t*>(w);
@@ -697,13 +1226,18 @@ static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, i
     // tensor maps: caches (d, position, layer*B*Hkv), tree rows (d, kv head, node, layer*B)
     CUtensorMap maps[4];
     // (paged: the plane is (layer, physical page, kv head) and a box spans at most a page)
+    // box rows: the one-SM kernel loads 64 keys of K and of V; the pair kernel 64 keys of
+    // K and 128 of V per CTA (a box spans at most one page)
+    const int kbox = kBN, vbox = pair ? kPN : kBN;
     const int rows3 = pg ? pg->page_rows : (Pcap > 0 ? Pcap : 1);
-    const cuuint32_t box3[3] = {64, (cuuint32_t)(pg ? (pg->page_rows < kBN ? pg->page_rows : kBN) : kBN), 1};
+    const cuuint32_t box3k[3] = {64, (cuuint32_t)(pg ? (pg->page_rows < kbox ? pg->page_rows : kbox) : kbox), 1};
+    const cuuint32_t box3v[3] = {64, (cuuint32_t)(pg ? (pg->page_rows < vbox ? pg->page_rows : vbox) : vbox), 1};
     const cuuint32_t es3[3] = {1, 1, 1};
     const cuuint64_t dims3[3] = {(cuuint64_t)d, (cuuint64_t)rows3,
                                  (cuuint64_t)L * (pg ? (long)pg->num_pages : (long)B) * Hkv};
     const cuuint64_t str3[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows3 * d * 2};
-    const cuuint32_t box4[4] = {64, 1, (cuuint32_t)kBN, 1};
+    const cuuint32_t box4k[4] = {64, 1, (cuuint32_t)kbox, 1};
+    const cuuint32_t box4v[4] = {64, 1, (cuuint32_t)vbox, 1};
     const cuuint32_t es4[4] = {1, 1, 1, 1};
     const cuuint64_t dims4[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)N, (cuuint64_t)L * B};
     const cuuint64_t str4[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2, (cuuint64_t)N * Hkv * d * 2};
@@ -711,20 +1245,20 @@ static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, i
     const void* vc = Pcap > 0 ? v_cache : v_tree;
     CUresult r = CUDA_SUCCESS;
     r = r != CUDA_SUCCESS ? r
-                          : enc(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kc), dims3, str3, box3,
+                          : enc(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kc), dims3, str3, box3k,
                                 es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     r = r != CUDA_SUCCESS ? r
-                          : enc(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(vc), dims3, str3, box3,
+                          : enc(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(vc), dims3, str3, box3v,
                                 es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     r = r != CUDA_SUCCESS ? r
                           : enc(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k_tree), dims4, str4,
-                                box4, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                box4k, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     r = r != CUDA_SUCCESS ? r
                           : enc(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v_tree), dims4, str4,
-                                box4, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                box4v, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
@@ -734,8 +1268,8 @@ static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, i
     const bool bf = out == DDT_BF16;
     switch (d) {
         case 64: return bf ? attn_tc_go<64, __nv_bfloat16>(prm, maps, st) : attn_tc_go<64, float>(prm, maps, st);
-        case 128: return bf ? attn_tc_go<128, __nv_bfloat16>(prm, maps, st) : attn_tc_go<128, float>(prm, maps, st);
-        case 256: return bf ? attn_tc_go<256, __nv_bfloat16>(prm, maps, st) : attn_tc_go<256, float>(prm, maps, st);
+        case 128: return bf ? attn_tc2_go<128, __nv_bfloat16>(prm, maps, st) : attn_tc2_go<128, float>(prm, maps, st);
+        case 256: return bf ? attn_tc2_go<256, __nv_bfloat16>(prm, maps, st) : attn_tc2_go<256, float>(prm, maps, st);
     }
     return cudaErrorInvalidValue;
 }
