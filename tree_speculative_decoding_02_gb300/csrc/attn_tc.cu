@@ -554,11 +554,19 @@ struct Tc2Cfg {
     static constexpr int kBlocks = D / 64;
     static constexpr int kQBytes = 128 * D * 2;     // this CTA's query rows
     static constexpr int kStageBytes = 64 * D * 2;  // a K half (64 keys x D) or a V half (128 keys x D/2)
-    static constexpr int kStages = D == 256 ? 4 : 8;
+    // separate K and V rings: a K stage frees as its tile's Q K^T finishes, about 5000
+    // cycles before the tile two ahead needs it; a V stage frees only as its tile's P.V
+    // finishes, so V gets the deeper ring
+    static constexpr int kKS = D == 256 ? 2 : 4;
+    static constexpr int kVS = D == 256 ? 3 : 4;
+    static constexpr int kStages = kKS + kVS;
     static constexpr int kOCol = 2 * kPN;
-    static constexpr int kBarBytes = 512;
-    static constexpr int kXchBytes = 3072;
-    static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + kBarBytes + kXchBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kXchBytes = 2048;  // row maxima of the two column halves (two parities)
+    static constexpr int kUsed = kQBytes + kStages * kStageBytes + kBarBytes + kXchBytes;
+    // dynamic shared memory requested: what the layout uses plus room to align it to 1024
+    // bytes, capped at the per-block maximum; the kernel checks the slack it gets
+    static constexpr int kSmem = kUsed + 1024 <= 232448 ? kUsed + 1024 : 232448;
 };
 
 __device__ __forceinline__ Tile tile2_of(int j, int n_pre, int c0, int c1, bool ragged) {
@@ -589,13 +597,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_attn_tc2(const TcParams p, const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
     using Cfg = Tc2Cfg<D>;
-    constexpr int kStages = Cfg::kStages;
+    constexpr int kStages = Cfg::kStages, kKS = Cfg::kKS, kVS = Cfg::kVS;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t slack = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
+    unsigned char* base = smem_raw + slack;
     unsigned char* sQ = base;
-    unsigned char* sRing = base + Cfg::kQBytes;
+    unsigned char* sRing = base + Cfg::kQBytes;  // stages [0, kKS): K ring; [kKS, kStages): V ring
     uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + kStages * Cfg::kStageBytes);
-    uint64_t* full = bars;                 // [kStages] even: K halves of both CTAs (even CTA); odd: own V half
+    uint64_t* full = bars;                 // [kStages] K: both CTAs' halves (even CTA's copy); V: own half
     uint64_t* sfree = bars + kStages;      // [kStages] the MMAs that read the stage are done (both CTAs)
     uint64_t* s_full = bars + 2 * kStages; // [2] S_j in tensor memory (both CTAs)
     // [2] P_j and V_j ready: in the even CTA its 8 softmax warps plus one arrival forwarded
@@ -632,6 +641,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bad_table = __syncthreads_or(bad_table);
     bad = bad || bad_table;
     const long prow0 = ((((long)s * p.L + l) * p.B + b) * p.Hkv + g) * (long)(p.MP * 256) + row0;
+    if (slack + Cfg::kUsed > (uint32_t)Cfg::kSmem) {  // the layout would not fit: refuse, touch nothing
+        if (tid == 0) atomicExch(p.status + b, (int)DDT_ERR_UNSUPPORTED);
+        return;
+    }
     // (both CTAs of a pair see the same request, so they leave here together)
     if (bad) {
         if (tid == 0 && rank == 0 && s == 0 && mp == 0 && g == 0 && l == 0)
@@ -731,8 +744,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 bool ok = true;
                 for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const int u = 2 * j + kv, st = u % kStages;
-                    ok = tc::mbar_wait(sfree + st, ((u / kStages) & 1) ^ 1, abort_flag);
+                    const int st = kv == 0 ? j % kKS : kKS + j % kVS;
+                    const int ph = kv == 0 ? (j / kKS) & 1 : (j / kVS) & 1;
+                    ok = tc::mbar_wait(sfree + st, ph ^ 1, abort_flag);
                     if (!ok) break;
                     unsigned char* dst = sRing + st * Cfg::kStageBytes;
                     if (kv == 0) {
@@ -789,14 +803,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    issued = u + 1;
+                    issued = 2 * j + kv + 1;
                 }
                 if (!ok) break;
             }
-            // drain: the even CTA waits for every K stage (both halves) and its V stages,
+            // drain: the even CTA waits for its last K stages (both halves) and its V stages,
             // the odd CTA for its own V stages
-            for (int u = max(0, issued - kStages); u < issued; ++u)
-                if (rank == 0 || (u & 1)) drain_wait(full + u % kStages, (u / kStages) & 1);
+            const int nk = (issued + 1) / 2, nv = issued / 2;  // K and V tiles issued
+            if (rank == 0)
+                for (int i = max(0, nk - kKS); i < nk; ++i) drain_wait(full + i % kKS, (i / kKS) & 1);
+            for (int i = max(0, nv - kVS); i < nv; ++i) drain_wait(full + kKS + i % kVS, (i / kVS) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
@@ -812,7 +828,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // softmax warps of the pair have arrived
                 if (!tc::mbar_wait_cluster(p_full + (i & 1), (i >> 1) & 1, abort_flag)) return false;
                 tc::tc_fence_after();
-                const int st = (2 * i + 1) % kStages;
+                const int st = kKS + i % kVS;
                 const uint64_t vd = vdesc0 + static_cast<uint64_t>((st * Cfg::kStageBytes) >> 4);
                 const uint32_t pa = tmem + (i & 1) * kPN;
 #pragma unroll
@@ -826,8 +842,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             };
             bool ok = true;
             for (int j = 0; j < T && ok; ++j) {
-                const int u = 2 * j, st = u % kStages;
-                if (!tc::mbar_wait_cluster(full + st, (u / kStages) & 1, abort_flag)) {
+                const int st = j % kKS;
+                if (!tc::mbar_wait_cluster(full + st, (j / kKS) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -876,7 +892,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const Tile t = tile2_of(j, n_pre, c0, c1, ragged);
             if (ok) ok = tc::mbar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag);
             ok = __all_sync(kFull, ok);
-            float sv[64];  // scores in log2 units, -inf where the key is not visible
+            float sv[64];  // raw scores, -inf where the key is not visible
             float mtile = -INFINITY;
             if (ok) {
                 tc::tc_fence_after();
@@ -892,22 +908,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 const bool all_vis = __all_sync(kFull, (vis[0] & vis[1]) == ~0u);
+                uint32_t sr[32];
 #pragma unroll
                 for (int w = 0; w < 2; ++w) {
-                    uint32_t sr[32];
                     tc::tmem_ld32(tmem + lane_base + (j & 1) * kPN + 64 * hf + 32 * w, sr);
                     tc::tmem_wait_ld();
                     if (all_vis) {  // every key of the half visible (nearly every prefix tile)
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) sv[32 * w + c] = __uint_as_float(sr[c]) * p.scale_log2;
+                        for (int c = 0; c < 32; ++c) sv[32 * w + c] = __uint_as_float(sr[c]);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            sv[32 * w + c] = ((vis[w] >> c) & 1u) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
+                            sv[32 * w + c] = ((vis[w] >> c) & 1u) ? __uint_as_float(sr[c]) : -INFINITY;
                     }
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) mtile = fmaxf(mtile, sv[32 * w + c]);
                 }
+                // tile max as a tree (short dependency chains), then into log2 units
+                float mx[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) mx[c] = fmaxf(fmaxf(sv[c], sv[c + 16]), fmaxf(sv[c + 32], sv[c + 48]));
+#pragma unroll
+                for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                    for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+                mtile = mx[0] * p.scale_log2;
             }
             float* xm = xch + (j & 1) * 256;
             xm[hf * 128 + r] = mtile;
@@ -918,8 +941,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool need = grow && (m_used != -INFINITY);
             if (__any_sync(kFull, need)) {
                 // O must hold tile j - 1 before it is rescaled: wait for that tile's P.V
-                const int u = 2 * (j - 1) + 1;
-                ok = __all_sync(kFull, tc::mbar_wait(sfree + u % kStages, (u / kStages) & 1, abort_flag));
+                ok = __all_sync(kFull,
+                                tc::mbar_wait(sfree + kKS + (j - 1) % kVS, ((j - 1) / kVS) & 1, abort_flag));
                 if (!ok) continue;
                 tc::tc_fence_after();
                 const float f = need ? tc::ex2(m_used - mtile) : 1.f;
@@ -939,6 +962,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float sum = 0.f;
             // a row that has seen no visible key yet has no reference: its P is all zeros
             const float mref = m_used == -INFINITY ? 0.f : m_used;
+            const float sc = p.scale_log2;
 #pragma unroll
             for (int w = 0; w < 2; ++w) {
                 uint32_t phi[16], plo[16];
@@ -947,8 +971,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // ex2(-inf) = 0 for keys that are not visible.  P = P_hi + P_lo with P_hi
                     // the top 16 bits of P (exact as bf16) and P_lo = bf16(P - P_hi): the
                     // pair carries P to ~2^-16 relative
-                    const float a = tc::ex2(sv[32 * w + c] - mref);
-                    const float bb = tc::ex2(sv[32 * w + c + 1] - mref);
+                    const float a = tc::ex2(fmaf(sv[32 * w + c], sc, -mref));
+                    const float bb = tc::ex2(fmaf(sv[32 * w + c + 1], sc, -mref));
                     sum += a + bb;
                     const uint32_t ah = __float_as_uint(a) & 0xffff0000u, bh = __float_as_uint(bb) & 0xffff0000u;
                     phi[c >> 1] = (ah >> 16) | bh;
@@ -966,8 +990,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // see (padding tree nodes may hold anything, even NaN, and a zero P does not
             // cancel NaN; paged tiles read rows past the prefix)
             {
-                const int u = 2 * j + 1, st = u % kStages;
-                ok = __all_sync(kFull, tc::mbar_wait(full + st, (u / kStages) & 1, abort_flag));
+                const int st = kKS + j % kVS;
+                ok = __all_sync(kFull, tc::mbar_wait(full + st, (j / kVS) & 1, abort_flag));
                 const int first = t.tree ? max(0, nn - t.y) : (t.y + kPN > c1 ? c1 - t.y : kPN);
                 if (ok && first < kPN) {
                     unsigned char* vst = sRing + st * Cfg::kStageBytes;
@@ -986,9 +1010,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (ok) ok = tc::mbar_wait(o_final, 0, abort_flag);
         ok = __all_sync(kFull, ok);
-        xch[512 + hf * 128 + r] = l_run;
+        // row sums of both halves, through the max buffer of the parity tile T - 1 did not use
+        float* xs = xch + (T & 1) * 256;
+        xs[hf * 128 + r] = l_run;
         tc::named_bar(1, 256);
-        const float l_tot = l_run + xch[512 + (hf ^ 1) * 128 + r];
+        const float l_tot = l_run + xs[(hf ^ 1) * 128 + r];
         if (ok) {
             tc::tc_fence_after();
             const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;

@@ -236,25 +236,32 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-// arrive on an mbarrier of another CTA of the cluster (shared::cluster address)
+// arrive on an mbarrier of another CTA of the cluster (shared::cluster address).  The
+// arrival carries the default (CTA-scope) release: what the waiter consumes is tensor
+// memory written before a tcgen05 fence and shared memory published to the async proxy
+// by fence.proxy.async, both complete before the arrival.  (A cluster-scope release here
+// took 600-1000 ns to reach the waiter, a third of a tile.)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
-// local wait that also acquires what other CTAs of the cluster released before arriving
-__device__ __forceinline__ bool mbar_try_cluster(uint64_t* bar, uint32_t parity) {
+// local wait that also acquires what other CTAs of the cluster released before arriving.
+// It polls with test_wait, which never suspends the thread: a thread suspended in
+// try_wait was observed to wake only at its suspend time limit (about 2000 cycles) when
+// the completing arrival came from the peer CTA, which stalled the MMA issuer a tile.
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_cluster(bar, parity)) return true;
+    if (mbar_test_cluster(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_cluster(bar, parity)) return true;
+        if (mbar_test_cluster(bar, parity)) return true;
         if (*abort) return false;
         if (clock64() - t0 > kWaitCycles) {
             *abort = 1;
