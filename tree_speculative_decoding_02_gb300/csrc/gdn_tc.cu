@@ -226,6 +226,22 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     }
     __syncthreads();
     const int nv = (*err == DDT_OK) ? nn : 0;
+    // ---- the group's q and k channel rows of every node and conv-state row into shared
+    //      memory (16-byte cp.async, all in flight together), issued first so that they
+    //      land while the tree is parsed
+    constexpr int kVecQK = kDK * (int)sizeof(Tin) / 16;
+    Tin* sk = reinterpret_cast<Tin*>(base + lay.sk);  // [N + K - 1][kDK], like sv
+    {
+        const int cbq = g * kDK, cbk = (p.Hk + g) * kDK;
+        for (int i = tid; i < 2 * (nv > 0 ? nv + K - 1 : 0) * kVecQK; i += kThr) {
+            const int part = i & 1, r = (i >> 1) / kVecQK, c = (i >> 1) % kVecQK;
+            const Tin* src = (r < nv ? xb + (long)r * C : csb + (long)(r - nv) * C) + (part ? cbk : cbq) +
+                             c * (16 / (int)sizeof(Tin));
+            const int rs = r < nv ? r : N + (r - nv);
+            cp_async16(reinterpret_cast<unsigned char*>((part ? sk : sv) + (long)rs * kDK) + c * 16, src);
+        }
+        cp_async_commit();
+    }
     // ---- tree check, ancestor lists, conv input rows (the node's path, newest last,
     //      continued by the committed conv state past the root)
     for (int n = tid; n < nv; n += kThr) {
@@ -255,6 +271,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     __syncthreads();
     Tout* obase = static_cast<Tout*>(p.o) + lb * N * p.Hv * kDV;
     if (*err != DDT_OK) {
+        cp_async_wait_all();  // no copy may still be landing when the CTA leaves
         if (tid == 0 && g == 0 && l == 0) p.status[b] = *err;
         for (int hi = 0; hi < p.R; ++hi) {
             const int h = g * p.R + hi;
@@ -284,24 +301,13 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     const int srow0 = (int)((lb * p.Hv + (long)g * p.R) * kDV);
     if (tid == 0) tc::prefetch_tmap(&tm_s);
 
-    // ---- conv + SiLU + L2 norm of q and k: the group's q and k channel rows of every node
-    //      and conv-state row are first copied into shared memory (16-byte cp.async, all in
-    //      flight together); then a warp takes a node and a lane four channels of q and of k,
-    //      so each norm is one warp reduction and each 16-byte store of the swizzled tile is
-    //      conflict-free
+    // ---- conv + SiLU + L2 norm of q and k from the staged rows: a warp takes a node (three
+    //      at a time, so their load, SiLU and reduction chains overlap) and a lane four
+    //      channels of q and of k, so each norm is one warp reduction and each 16-byte store
+    //      of the swizzled tile is conflict-free
     {
-        constexpr int kVec = kDK * (int)sizeof(Tin) / 16;
         const int c4 = 4 * lane;
-        Tin* sk = reinterpret_cast<Tin*>(base + lay.sk);  // [N + K - 1][kDK], like sv
         const int cbq = g * kDK, cbk = (p.Hk + g) * kDK;
-        for (int i = tid; i < 2 * (nn + K - 1) * kVec; i += kThr) {
-            const int part = i & 1, r = (i >> 1) / kVec, c = (i >> 1) % kVec;
-            const Tin* src = (r < nn ? xb + (long)r * C : csb + (long)(r - nn) * C) + (part ? cbk : cbq) +
-                             c * (16 / (int)sizeof(Tin));
-            const int rs = r < nn ? r : N + (r - nn);
-            cp_async16(reinterpret_cast<unsigned char*>((part ? sk : sv) + (long)rs * kDK) + c * 16, src);
-        }
-        cp_async_commit();
         float w[2][4][KT];
 #pragma unroll
         for (int part = 0; part < 2; ++part)
@@ -312,6 +318,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                     w[part][ch][q] = (q < K) ? to_f32(wl[(long)((part ? cbk : cbq) + c4 + ch) * K + q]) : 0.f;
         cp_async_wait_all();
         __syncthreads();
+#pragma unroll 3
         for (int n = warp; n < N; n += kThr / 32) {
             float y[2][4] = {};
             if (n < nn) {
