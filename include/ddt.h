@@ -133,8 +133,9 @@ ddt_status ddt_build_tree(int B, int D, int V, int top_k, int budget, ddt_dtype 
  *   - Every call on a device shares the array, which keeps the last call's contents:
  *     calls whose kernels overlap on the GPU race on it and must be ordered by the caller.
  *   - Returns DDT_ERR_CAPACITY, before launching anything, when the call needs more
- *     than 4 MiB (ddt_build_tree_workspace(B, D, V, top_k) > 4 MiB), e.g. B = 32,
- *     D = 15, V = 151936 needs 0.7 MiB with top_k = 8 and 2.4 MiB with top_k = 32.
+ *     than 4 MiB (ddt_build_tree_workspace(B, D, V, top_k) = B*D*(16 + 8*top_k) bytes,
+ *     rounded up to 256, > 4 MiB), e.g. B = 32, D = 15 needs 38 KiB with top_k = 8;
+ *     B = 2048, D = 64, top_k = 32 (35 MiB) is refused.
  *   - Allocates nothing (no cudaMalloc, no allocating library call).
  * ------------------------------------------------------------------------------- */
 ddt_status ddt_build_tree_noalloc(int B, int D, int V, int top_k, int budget, ddt_dtype dtype,

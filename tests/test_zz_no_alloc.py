@@ -53,7 +53,7 @@ def test_noalloc_build_matches_workspace_build_twice():
 def test_noalloc_refuses_oversized_scratch():
     dev = torch.device("cuda")
     lib = ddt.load()
-    B, D, V, k = 64, 15, 151936, 32   # needs ~5 MiB of partials
+    B, D, V, k = 2048, 64, 1000, 32   # needs ~35 MiB of per-row results
     assert lib.ddt_build_tree_workspace(B, D, V, k) > (4 << 20)
     p = ctypes.c_void_p(torch.empty(16, device=dev).data_ptr())
     rc = lib.ddt_build_tree_noalloc(B, D, V, k, 64, 1, *([p] * 11), None)

@@ -8,16 +8,17 @@
 // mask).
 //
 // GB300 layout of the work:
-//   k_build_partial  grid (chunks, D, B): one HBM pass over the logits.  Each CTA
-//                    reduces one 8192-token chunk of one depth row to (max, sum of
-//                    exp(v - max), top-k list): a threshold from the lane bests, one
-//                    bitonic sort per warp, bitonic merges of the warp lists.
-//   k_build_tree     grid B: per request, warp-per-depth merge of the chunk partials
-//                    (LSE and top-k), then one warp runs the best-first selection over a
-//                    shared-memory frontier, then the CTA renumbers breadth first and
-//                    writes the flattened tree and its bit-packed ancestor mask.
+//   k_build_row      grid (D, B): one CTA per depth row of a request, one HBM pass plus
+//                    one L2 pass over the row: log-sum-exp and the exact top-k (a
+//                    threshold from the warps' lane bests, then the few entries at or
+//                    above it ranked by one warp).
+//   k_build_tree     grid B: per request, one warp runs the best-first selection over a
+//                    shared-memory frontier, then the CTA numbers the nodes breadth first
+//                    (one pass over all depths) and writes the flattened tree and its
+//                    bit-packed ancestor mask.
 #include <cuda.h>
 #include <float.h>
+#include <limits.h>
 #include <math.h>
 
 #include <mutex>
@@ -27,180 +28,174 @@
 
 namespace ddt {
 
-// ------------------------------------------------------------------------------ partial
-struct BuildPartial {
-    float m;        // chunk max
-    int nonfinite;  // 1 if the chunk holds NaN/Inf
-    double s;       // sum over the chunk of exp(v - m)
+// ---------------------------------------------------------------------------- row pass
+// One CTA per (depth, request) row of the drafter logits, two passes over the row:
+//   1. each thread's max and a non-finite check; a warp's k-th largest thread max is
+//      reached by k entries of the row, so the largest of those warp thresholds, tau, is
+//      at or below the value of the row's k-th best entry;
+//   2. (from L2) the sum of exp(v - max) and the entries whose value reaches tau (ties
+//      included), collected in shared memory -- usually a few dozen -- from which one
+//      warp takes the exact top-k by (value desc, id asc).
+// If more entries than the buffer holds reach tau (not seen on drafter-like rows), each
+// warp ranks its own entries with a warp top-k and the warp lists are merged instead.
+struct BuildRow {
+    double lse;  // log sum_v exp(logit_v)
+    int bad;     // 1 if the row holds NaN or +-Inf
+    int pad;
 };
 
 size_t build_ws_bytes(int B, int D, int V, int k) {
-    const long nch = (V + kBuildChunk - 1) / kBuildChunk;
-    const long parts = (long)B * D * nch;
-    size_t bytes = parts * sizeof(BuildPartial);
-    bytes += parts * k * (sizeof(float) + sizeof(int));
+    (void)V;
+    const long rows = (long)B * D;
+    size_t bytes = rows * sizeof(BuildRow) + rows * k * (sizeof(float) + sizeof(int));
     return (bytes + 255) & ~(size_t)255;
 }
 
+namespace {
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kCandCap = 1024;
+}  // namespace
+
 template <typename T>
-__global__ void __launch_bounds__(256, 4) k_build_partial(const T* __restrict__ logits, int D, int V, int k,
-                                                        int nch, int vec, BuildPartial* __restrict__ part,
-                                                        float* __restrict__ pv, int* __restrict__ pid) {
-    constexpr int kPer = kBuildChunk / 256;  // elements per thread (32)
-    const int c = blockIdx.x, d = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(kRowThreads) k_build_row(const T* __restrict__ logits, int D, int V, int k, int vec,
+                                                           BuildRow* __restrict__ rows, float* __restrict__ top_v,
+                                                           int* __restrict__ top_id) {
+    const int d = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long row = ((long)b * D + d) * V;
-    const int start = c * kBuildChunk;
-    const int len = min(kBuildChunk, V - start);
-
-    float v[kPer];
-    int bad = 0;
-    if (vec) {
-        // 8-wide vector loads: thread t covers elements [t*8 + j*2048, +8)
-#pragma unroll
-        for (int j = 0; j < kPer / 8; ++j) {
-            const int e = tid * 8 + j * 2048;
-            float t8[8];
-            if (e + 8 <= len) {
-                load8_stream(logits + row + start + e, t8);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) t8[u] = (e + u < len) ? to_f32(logits[row + start + e + u]) : vid_empty().v;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[j * 8 + u] = t8[u];
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kPer / 8; ++j)
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid * 8 + j * 2048 + u;
-                v[j * 8 + u] = (e < len) ? to_f32(logits[row + start + e]) : vid_empty().v;
-            }
-    }
-#pragma unroll
-    for (int j = 0; j < kPer / 8; ++j)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid * 8 + j * 2048 + u;
-            if (e < len && !finite_f32(v[j * 8 + u])) bad = 1;
-        }
-
-    // warp top-k.  The k-th best of the 32 lane bests is beaten or equalled by at least k
-    // entries, so every entry of the warp's top k is at or above it: only those entries
-    // are kept.  When at most 32 qualify (the usual case) they are sorted in one bitonic
-    // pass; otherwise they are inserted one at a time.
-    __shared__ float s_v[8][32];
-    __shared__ int s_id[8][32];
-    __shared__ float s_max[8];
-    __shared__ double s_sum[8];
-    __shared__ int s_bad[8];
+    const long r = (long)b * D + d;
+    const T* x = logits + r * V;
+    __shared__ float s_cv[kCandCap];
+    __shared__ int s_ci[kCandCap];
+    __shared__ float s_wv[kRowWarps * 32];
+    __shared__ int s_wi[kRowWarps * 32];
+    __shared__ float s_m[kRowWarps];
+    __shared__ double s_sum[kRowWarps];
+    __shared__ int s_nc, s_bad;
     const VId emp = vid_empty();
-    float bv = emp.v;
-    int bid = emp.id;
+    if (tid == 0) {
+        s_nc = 0;
+        s_bad = 0;
+    }
+
+    // ---- pass 1: each thread's max and a non-finite check.  The threshold keeps every
+    //      entry whose value reaches it (ties included), so it needs the values only.
+    float m = emp.v;
+    int bad = 0;
+    auto see = [&](float v) {
+        bad |= !finite_f32(v);
+        m = fmaxf(m, v);
+    };
+    if (vec) {  // V % 8 == 0 and 16-byte aligned rows: 8 entries a load
+#pragma unroll 4
+        for (int e = tid * 8; e < V; e += kRowThreads * 8) {
+            float t8[8];
+            load8_stream(x + e, t8);
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
-        if (e < len && beats(v[j], start + e, bv, bid)) {
-            bv = v[j];
-            bid = start + e;
+            for (int u = 0; u < 8; ++u) see(t8[u]);
         }
+    } else {
+#pragma unroll 4
+        for (int e = tid; e < V; e += kRowThreads) see(to_f32(x[e]));
     }
-    warp_sort_best_first(bv, bid);
-    const float thv = __shfl_sync(kFull, bv, k - 1);
-    const int thid = __shfl_sync(kFull, bid, k - 1);
-    int cnt = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
-        cnt += (e < len && !beats(thv, thid, v[j], start + e)) ? 1 : 0;
+    // the warp's k-th largest thread max: k entries of the warp reach it
+    float tv = m;
+    int ti = lane;
+    warp_sort_best_first(tv, ti);
+    const float wm = warp_max(m);
+    bad = warp_or(bad);
+    if (lane == 0) {
+        s_m[warp] = wm;
+        if (bad) s_bad = 1;
     }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int nb = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += nb;
+    if (lane == k - 1) s_wv[warp] = tv;
+    __syncthreads();
+    float M = s_m[0], tau_v = s_wv[0];
+#pragma unroll 1
+    for (int w = 1; w < kRowWarps; ++w) {
+        M = fmaxf(M, s_m[w]);
+        tau_v = fmaxf(tau_v, s_wv[w]);
     }
-    const int total = __shfl_sync(kFull, incl, 31);
-    float wv;
-    int wid;
-    if (total <= 32) {
-        int pos = incl - cnt;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
-            if (e < len && !beats(thv, thid, v[j], start + e)) {
-                s_v[warp][pos] = v[j];
-                s_id[warp][pos] = start + e;
-                ++pos;
+    const bool row_bad = s_bad != 0;
+
+    // ---- pass 2: sum of exp(v - M) (fp32 per load of 8 and per thread, fp64 across
+    //      threads) and the entries that reach tau
+    const float LOG2E = 1.4426950408889634f;
+    const float mb = M * LOG2E;
+    float acc = 0.f;
+    auto take = [&](float v, int id) {
+        if (v >= tau_v) {
+            const int pos = atomicAdd(&s_nc, 1);
+            if (pos < kCandCap) {
+                s_cv[pos] = v;
+                s_ci[pos] = id;
             }
         }
-        __syncwarp();
-        wv = lane < total ? s_v[warp][lane] : emp.v;
-        wid = lane < total ? s_id[warp][lane] : emp.id;
-        warp_sort_best_first(wv, wid);
-    } else {
+    };
+    if (!row_bad) {
+        if (vec) {
+#pragma unroll 4
+            for (int e = tid * 8; e < V; e += kRowThreads * 8) {
+                float t8[8];
+                load8(x + e, t8);
+                float s8 = 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    s8 += exp2f(fmaf(t8[u], LOG2E, -mb));
+                    take(t8[u], e + u);
+                }
+                acc += s8;
+            }
+        } else {
+#pragma unroll 4
+            for (int e = tid; e < V; e += kRowThreads) {
+                const float v = to_f32(x[e]);
+                acc += exp2f(fmaf(v, LOG2E, -mb));
+                take(v, e);
+            }
+        }
+    }
+    const double ws = warp_sum((double)acc);
+    if (lane == 0) s_sum[warp] = ws;
+    __syncthreads();
+    const int nc = s_nc;
+    if (nc > kCandCap && !row_bad) {
+        // overflow: every warp ranks its own entries, then the warp lists are merged
         WarpTopK tk;
         tk.init(k);
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
-            const bool q = e < len && !beats(thv, thid, v[j], start + e);
-            if (__any_sync(kFull, q)) tk.insert(q ? v[j] : emp.v, q ? start + e : emp.id);
+        for (int e0 = warp * 32; e0 < V; e0 += kRowThreads) {
+            const int e = e0 + lane;
+            const float v = e < V ? to_f32(x[e]) : emp.v;
+            const bool q = e < V && v >= tau_v;
+            if (__any_sync(kFull, q)) tk.insert(q ? v : emp.v, q ? e : emp.id);
         }
-        wv = tk.v;
-        wid = tk.id;
+        s_wv[warp * 32 + lane] = tk.v;
+        s_wi[warp * 32 + lane] = tk.id;
+        __syncthreads();
     }
-    if (lane >= k) {
-        wv = emp.v;
-        wid = emp.id;
-    }
-    __syncwarp();
-    s_v[warp][lane] = wv;
-    s_id[warp][lane] = wid;
-    const float wmax = __shfl_sync(kFull, wv, 0);
-    if (lane == 0) s_max[warp] = wmax;
-    const int wbad = __any_sync(kFull, bad);
-    if (lane == 0) s_bad[warp] = wbad;
-    __syncthreads();
-    float m = s_max[0];
-    int anybad = s_bad[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) {
-        m = fmaxf(m, s_max[w]);
-        anybad |= s_bad[w];
-    }
-
-    // sum of exp(v - m): fp32 over the thread's 32 terms, fp64 across threads
-    const float LOG2E = 1.4426950408889634f;
-    const float mb = m * LOG2E;
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = tid * 8 + (j >> 3) * 2048 + (j & 7);
-        if (e < len) acc += exp2f(fmaf(v[j], LOG2E, -mb));
-    }
-    double dacc = warp_sum((double)acc);
-    if (lane == 0) s_sum[warp] = dacc;
-
-    // merge the eight warp lists in warp 0
-    __syncthreads();
     if (warp == 0) {
-        float fv = s_v[0][lane];
-        int fid = s_id[0][lane];
-        for (int w = 1; w < 8; ++w) warp_merge_best_first(fv, fid, s_v[w][lane], s_id[w][lane]);
-        const long p = ((long)b * D + d) * nch + c;
+        WarpTopK tk;
+        tk.init(k);
+        if (!row_bad) {
+            if (nc <= kCandCap) {
+                for (int c0 = 0; c0 < nc; c0 += 32) {
+                    const int c = c0 + lane;
+                    tk.insert(c < nc ? s_cv[c] : emp.v, c < nc ? s_ci[c] : emp.id);
+                }
+            } else {
+                for (int w = 0; w < kRowWarps; ++w) tk.insert(s_wv[w * 32 + lane], s_wi[w * 32 + lane]);
+            }
+        }
         if (lane < k) {
-            pv[p * k + lane] = fv;
-            pid[p * k + lane] = fid;
+            top_v[r * k + lane] = tk.v;
+            top_id[r * k + lane] = tk.id;
         }
         if (lane == 0) {
             double tot = 0.0;
-            for (int w = 0; w < 8; ++w) tot += s_sum[w];
-            part[p].m = m;
-            part[p].nonfinite = anybad;
-            part[p].s = tot;
+            for (int w = 0; w < kRowWarps; ++w) tot += s_sum[w];
+            const double lse = (double)M + log(tot);
+            rows[r].lse = lse;
+            rows[r].bad = row_bad || !isfinite(lse);
         }
     }
 }
@@ -218,14 +213,15 @@ struct Cand {
 struct TreeSmem {
     // per depth
     float* top_v;   // [D][k]
+    double* top_vd; // [D][k] the same logits as doubles (converted once, not per push)
     int* top_id;    // [D][k]
     double* cum;    // [D+1] cumulative LSE, cum[0] = 0
     // selection
     Cand* sel;      // [budget]
-    Cand* front;    // [budget + 2]
+    Cand* front;    // [budget + 2] frontier entries
+    long long* fs;  // [budget + 2] their scores as order-preserving integer keys
     int* new_idx;   // [budget]
     int* out_par;   // [N]
-    int* depth_cnt; // [D + 2]
 };
 
 __device__ __forceinline__ int cand_token(const TreeSmem& S, int k, const Cand& c) {
@@ -266,16 +262,34 @@ __device__ bool lex_less(const TreeSmem& S, int k, const Cand& a, const Cand& b)
     return ta < tb;
 }
 
-__device__ __forceinline__ bool cand_better(const TreeSmem& S, int k, const Cand& a, const Cand& b) {
-    if (a.s != b.s) return a.s > b.s;
-    return lex_less(S, k, a, b);
+// A score (a log-probability: strictly negative, finite) as a 64-bit key with the same
+// order: flipping every bit but the sign of a negative double's pattern reverses the
+// integer order into the value order, and equal doubles get equal keys.  The selection
+// compares keys on the integer pipe (this chip's FP64 rate is a small fraction of its
+// FP32 rate, and the argmax is a dependent chain of compares).
+__device__ __forceinline__ long long score_key(double s) {
+    const long long b = __double_as_longlong(s);
+    return b < 0 ? (b ^ 0x7fffffffffffffffLL) : b;
+}
+
+// frontier entry i before entry j in the selection order (score, then token path)
+__device__ __forceinline__ bool front_before(const TreeSmem& S, int k, long long si, int i, long long sj, int j) {
+    if (si != sj) return si > sj;
+    return i != j && lex_less(S, k, S.front[i], S.front[j]);
+}
+
+// rank-path key of selected node i: the ranks along its path from the root, `bits` bits
+// a level, first level highest; within a depth its order is the breadth-first order
+__device__ __forceinline__ unsigned long long rank_key(const TreeSmem& S, int i, int bits) {
+    unsigned long long key = 0;
+    int sh = 0;
+    for (int a = i; a >= 0; a = S.sel[a].parent, sh += bits) key |= (unsigned long long)S.sel[a].rank << sh;
+    return key << (64 - sh);  // root-first levels at the top; depth is compared separately
 }
 
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads) k_build_tree(int D, int V, int k, int budget, int nch,
-                                                          const BuildPartial* __restrict__ part,
-                                                          const float* __restrict__ pv,
-                                                          const int* __restrict__ pid,
+__global__ void __launch_bounds__(kThreads) k_build_tree(int D, int k, int budget, const BuildRow* __restrict__ rows,
+                                                          const float* __restrict__ rtv, const int* __restrict__ rti,
                                                           const int32_t* __restrict__ root_token,
                                                           const int32_t* __restrict__ prefix_len,
                                                           int32_t* __restrict__ token, int32_t* __restrict__ parent,
@@ -285,70 +299,49 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int V, int k, in
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kWarps = kThreads / 32;
     const int N = budget + 1;
     const int W = (N + 31) / 32;
 
     TreeSmem S;
     unsigned char* p = smem_raw;
     S.cum = reinterpret_cast<double*>(p);      p += sizeof(double) * (kMaxDepth + 1);
+    S.fs = reinterpret_cast<long long*>(p);    p += sizeof(long long) * (budget + 2);
     S.sel = reinterpret_cast<Cand*>(p);        p += sizeof(Cand) * (budget + 1);
     S.front = reinterpret_cast<Cand*>(p);      p += sizeof(Cand) * (budget + 2);
+    S.top_vd = reinterpret_cast<double*>(p);   p += sizeof(double) * D * k;
     S.top_v = reinterpret_cast<float*>(p);     p += sizeof(float) * D * k;
     S.top_id = reinterpret_cast<int*>(p);      p += sizeof(int) * D * k;
     S.new_idx = reinterpret_cast<int*>(p);     p += sizeof(int) * (budget + 1);
     S.out_par = reinterpret_cast<int*>(p);     p += sizeof(int) * N;
-    S.depth_cnt = reinterpret_cast<int*>(p);   p += sizeof(int) * (kMaxDepth + 2);
-    __shared__ double s_lse[kMaxDepth];
     __shared__ int s_bad;
     __shared__ int s_nsel;
 
-    if (tid == 0) s_bad = 0;
-    __syncthreads();
-
-    // 1. per depth: merge the chunk partials into LSE and the depth's top-k
-    for (int d = warp; d < D; d += kWarps) {
-        const long base = ((long)b * D + d) * nch;
-        float M = vid_empty().v;
-        int bad = 0;
-        for (int c = lane; c < nch; c += 32) {
-            M = fmaxf(M, part[base + c].m);
-            bad |= part[base + c].nonfinite;
-        }
-        M = warp_max(M);
-        bad = warp_or(bad);
-        double sum = 0.0;
-        for (int c = lane; c < nch; c += 32) sum += part[base + c].s * exp((double)part[base + c].m - (double)M);
-        sum = warp_sum(sum);
-        WarpTopK tk;
-        tk.init(k);
-        for (int c0 = 0; c0 < nch * k; c0 += 32) {
-            const int e = c0 + lane;
-            const bool ok = e < nch * k;
-            tk.insert(ok ? pv[base * k + e] : vid_empty().v, ok ? pid[base * k + e] : 0x7fffffff);
-        }
-        if (lane < k) {
-            S.top_v[d * k + lane] = tk.v;
-            S.top_id[d * k + lane] = tk.id;
-        }
-        if (lane == 0) {
-            s_lse[d] = (double)M + log(sum);
-            if (bad || !isfinite(s_lse[d])) atomicOr(&s_bad, 1);
-        }
+    // 1. the depths' top-k lists and log-sum-exps (from the row pass)
+    for (int e = tid; e < D * k; e += kThreads) {
+        const float v = rtv[(long)b * D * k + e];
+        S.top_v[e] = v;
+        S.top_vd[e] = (double)v;
+        S.top_id[e] = rti[(long)b * D * k + e];
     }
-    __syncthreads();
-    const bool bad = s_bad != 0;
     if (tid == 0) {
+        int bad = 0;
         double c = 0.0;
         S.cum[0] = 0.0;
         for (int d = 0; d < D; ++d) {
-            c += s_lse[d];
+            const BuildRow rr = rows[(long)b * D + d];
+            bad |= rr.bad;
+            c += rr.lse;
             S.cum[d + 1] = c;
         }
+        s_bad = bad;
     }
     __syncthreads();
+    const bool bad = s_bad != 0;
 
-    // 2. best-first selection (one warp; the frontier lives in shared memory)
+    // 2. best-first selection: one warp keeps the frontier in shared memory (entries and
+    //    their scores).  A pop is a warp argmax over the scores -- the token-path order is
+    //    consulted only on an exact score tie -- after which lane 0 moves the best entry
+    //    to the selected list and pushes its next-ranked sibling and its best child.
     if (warp == 0) {
         int n_sel = 0, n_front = 0;
         if (budget > 0 && !bad) {
@@ -357,30 +350,49 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int V, int k, in
                 c0.depth = 1;
                 c0.rank = 0;
                 c0.parent = -1;
-                c0.L = 0.0 + (double)S.top_v[0];
+                c0.L = S.top_vd[0];
                 c0.s = c0.L - S.cum[1];
                 S.front[0] = c0;
+                S.fs[0] = score_key(c0.s);
             }
             n_front = 1;
         }
         __syncwarp();
         while (n_sel < budget && n_front > 0) {
             int best = -1;
-            for (int i = lane; i < n_front; i += 32)
-                if (best < 0 || cand_better(S, k, S.front[i], S.front[best])) best = i;
+            long long bs = 0;
+            for (int i = lane; i < n_front; i += 32) {
+                const long long si = S.fs[i];
+                if (best < 0 || front_before(S, k, si, i, bs, best)) {
+                    best = i;
+                    bs = si;
+                }
+            }
+            // warp argmax on the integer keys alone; the token-path order decides only
+            // between lanes that hold the same top key (exact score ties, which bf16
+            // logits make common: every pair of nodes below two tied siblings ties too)
+            long long mk = best >= 0 ? bs : LLONG_MIN;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-                // lanes that already agree skip the compare: on equal scores it walks both
-                // token paths, which for an entry against itself is the whole path
-                const int other = __shfl_xor_sync(kFull, best, o);
-                if (other >= 0 && other != best && (best < 0 || cand_better(S, k, S.front[other], S.front[best])))
-                    best = other;
+                const long long om = __shfl_xor_sync(kFull, mk, o);
+                mk = om > mk ? om : mk;
             }
-            best = __shfl_sync(kFull, best, 0);
+            const unsigned tied = __ballot_sync(kFull, best >= 0 && bs == mk);
+            if (__popc(tied) == 1) {
+                best = __shfl_sync(kFull, best, __ffs(tied) - 1);
+            } else {
+                int w = -1;
+                for (unsigned t = tied; t; t &= t - 1) {
+                    const int idx = __shfl_sync(kFull, best, __ffs(t) - 1);
+                    if (w < 0 || lex_less(S, k, S.front[idx], S.front[w])) w = idx;
+                }
+                best = w;
+            }
             int nf = 0;
             if (lane == 0) {
                 const Cand c = S.front[best];
                 S.front[best] = S.front[n_front - 1];
+                S.fs[best] = S.fs[n_front - 1];
                 nf = n_front - 1;
                 const int me = n_sel;
                 S.sel[me] = c;
@@ -388,18 +400,20 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int V, int k, in
                 if (c.rank + 1 < k) {  // next-ranked sibling: same parent, same depth
                     Cand sib = c;
                     sib.rank = c.rank + 1;
-                    sib.L = L_par + (double)S.top_v[(c.depth - 1) * k + sib.rank];
+                    sib.L = L_par + S.top_vd[(c.depth - 1) * k + sib.rank];
                     sib.s = sib.L - S.cum[c.depth];
-                    S.front[nf++] = sib;
+                    S.front[nf] = sib;
+                    S.fs[nf++] = score_key(sib.s);
                 }
                 if (c.depth < D) {  // best child
                     Cand ch;
                     ch.depth = c.depth + 1;
                     ch.rank = 0;
                     ch.parent = me;
-                    ch.L = c.L + (double)S.top_v[c.depth * k];
+                    ch.L = c.L + S.top_vd[c.depth * k];
                     ch.s = ch.L - S.cum[c.depth + 1];
-                    S.front[nf++] = ch;
+                    S.front[nf] = ch;
+                    S.fs[nf++] = score_key(ch.s);
                 }
             }
             n_front = __shfl_sync(kFull, nf, 0);
@@ -411,31 +425,43 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int V, int k, in
     __syncthreads();
     const int n_sel = s_nsel;
 
-    // 3. canonical breadth-first numbering: depth, then parent's new row, then rank
-    for (int i = tid; i < kMaxDepth + 2; i += kThreads) S.depth_cnt[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n_sel; i += kThreads) atomicAdd(&S.depth_cnt[S.sel[i].depth], 1);
-    __syncthreads();
-    int base = 1;
-    for (int dd = 1; dd <= D; ++dd) {
-        const int cnt = S.depth_cnt[dd];
-        if (cnt == 0) break;
-        for (int i = tid; i < n_sel; i += kThreads) {
-            const Cand& ci = S.sel[i];
-            if (ci.depth != dd) continue;
-            const int pi = ci.parent < 0 ? 0 : S.new_idx[ci.parent];
-            int r = 0;
-            for (int j = 0; j < n_sel; ++j) {
-                const Cand& cj = S.sel[j];
-                if (cj.depth != dd) continue;
-                const int pj = cj.parent < 0 ? 0 : S.new_idx[cj.parent];
-                r += (pj < pi) || (pj == pi && cj.rank < ci.rank);
-            }
-            S.new_idx[i] = base + r;
-        }
-        base += cnt;
+    // 3. canonical breadth-first numbering (depth, then parent's row, then rank), all depths
+    //    in one pass: within a depth that order is the lexicographic order of the nodes'
+    //    rank paths from the root.  When the path fits 64 bits (ceil(log2 k) bits a level)
+    //    it is packed into a key; otherwise two nodes climb to where their parents agree.
+    {
+        int bits = 1;
+        while ((1 << bits) < k) ++bits;
+        const bool packed = bits * D <= 64;
+        unsigned long long* key = reinterpret_cast<unsigned long long*>(S.front);  // free now
+        if (packed)
+            for (int i = tid; i < n_sel; i += kThreads) key[i] = rank_key(S, i, bits);
         __syncthreads();
+        for (int i = tid; i < n_sel; i += kThreads) {
+            const int di = S.sel[i].depth;
+            const unsigned long long ki = packed ? key[i] : 0ull;
+            int r = 1;
+            for (int j = 0; j < n_sel; ++j) {
+                const int dj = S.sel[j].depth;
+                if (dj < di) {
+                    ++r;
+                } else if (dj == di && j != i) {
+                    if (packed) {
+                        r += key[j] < ki;
+                    } else {
+                        int a = i, c = j;
+                        while (S.sel[a].parent != S.sel[c].parent) {
+                            a = S.sel[a].parent;
+                            c = S.sel[c].parent;
+                        }
+                        r += S.sel[c].rank < S.sel[a].rank;
+                    }
+                }
+            }
+            S.new_idx[i] = r;
+        }
     }
+    __syncthreads();
 
     // 4. flattened outputs
     const long ob = (long)b * N;
@@ -482,9 +508,9 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int V, int k, in
 
 size_t build_tree_smem(int D, int k, int budget) {
     const int N = budget + 1;
-    size_t b = sizeof(double) * (kMaxDepth + 1) + sizeof(Cand) * (budget + 1) + sizeof(Cand) * (budget + 2) +
-               sizeof(float) * D * k + sizeof(int) * D * k + sizeof(int) * (budget + 1) + sizeof(int) * N +
-               sizeof(int) * (kMaxDepth + 2);
+    size_t b = sizeof(double) * (kMaxDepth + 1) + sizeof(long long) * (budget + 2) + sizeof(Cand) * (budget + 1) +
+               sizeof(Cand) * (budget + 2) + sizeof(double) * D * k + sizeof(float) * D * k + sizeof(int) * D * k +
+               sizeof(int) * (budget + 1) + sizeof(int) * N;
     return (b + 15) & ~(size_t)15;
 }
 
@@ -492,20 +518,20 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
                               const int32_t* root_token, const int32_t* prefix_len, int32_t* token,
                               int32_t* parent, int32_t* depth, int32_t* position, int32_t* n_nodes,
                               uint32_t* anc, double* score, int32_t* status, void* ws, cudaStream_t st) {
-    const int nch = (V + kBuildChunk - 1) / kBuildChunk;
-    const long parts = (long)B * D * nch;
+    const long nrows = (long)B * D;
     unsigned char* w = static_cast<unsigned char*>(ws);
-    BuildPartial* part = reinterpret_cast<BuildPartial*>(w);
-    float* pv = reinterpret_cast<float*>(w + parts * sizeof(BuildPartial));
-    int* pid = reinterpret_cast<int*>(w + parts * sizeof(BuildPartial) + parts * k * sizeof(float));
-    dim3 g1(nch, D, B);
+    BuildRow* rows = reinterpret_cast<BuildRow*>(w);
+    float* tv = reinterpret_cast<float*>(w + nrows * sizeof(BuildRow));
+    int* ti = reinterpret_cast<int*>(w + nrows * sizeof(BuildRow) + nrows * k * sizeof(float));
+    if (B > 65535) return cudaErrorInvalidValue;
+    const dim3 g1(D, B);
     const int vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
     if (dtype == DDT_BF16)
-        k_build_partial<__nv_bfloat16><<<counted(g1), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), D, V, k, nch,
-                                                          vec, part, pv, pid);
+        k_build_row<__nv_bfloat16><<<counted(g1), kRowThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), D, V,
+                                                                          k, vec, rows, tv, ti);
     else
-        k_build_partial<float><<<counted(g1), 256, 0, st>>>(static_cast<const float*>(logits), D, V, k, nch, vec, part, pv,
-                                                  pid);
+        k_build_row<float><<<counted(g1), kRowThreads, 0, st>>>(static_cast<const float*>(logits), D, V, k,
+                                                                  vec && (V % 8 == 0), rows, tv, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t sm = build_tree_smem(D, k, budget);
@@ -513,8 +539,8 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
         e = cudaFuncSetAttribute(k_build_tree<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return e;
     }
-    k_build_tree<512><<<counted(B), 512, sm, st>>>(D, V, k, budget, nch, part, pv, pid, root_token, prefix_len, token,
-                                          parent, depth, position, n_nodes, anc, score, status);
+    k_build_tree<512><<<counted(B), 512, sm, st>>>(D, k, budget, rows, tv, ti, root_token, prefix_len, token, parent,
+                                                   depth, position, n_nodes, anc, score, status);
     return cudaGetLastError();
 }
 
@@ -525,8 +551,9 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
 // memory.  Some hosts of this library have no device allocator of their own (a plain C
 // program, or a plugin living inside a process whose GPU memory is owned by another
 // runtime), and some must not call cudaMalloc/cudaFree in their decode loop because
-// those calls synchronise the device.  For them the build's per-chunk partials live in
-// one file-scope device array instead of a caller-supplied workspace.
+// those calls synchronise the device.  For them the build's per-row results (the
+// log-sum-exp and top-k list of every depth row) live in one file-scope device array
+// instead of a caller-supplied workspace.
 //
 // The array is a fixed kStaticScratchBytes (4 MiB) on every GPU that loads this library,
 // held until the process exits.  Its device address is looked up with
@@ -612,7 +639,7 @@ extern "C" ddt_status ddt_build_tree_noalloc(int B, int D, int V, int top_k, int
     if (!draft_logits || !root_token || !prefix_len || !token || !parent || !depth || !position || !n_nodes || !anc ||
         !status)
         return DDT_ERR_INVALID_ARG;
-    // the partials of this call must fit the static array
+    // the per-row results of this call must fit the static array
     if (build_ws_bytes(B, D, V, top_k) > kStaticScratchBytes) return DDT_ERR_CAPACITY;
     if (build_tree_smem(D, top_k, budget) > 200 * 1024) return DDT_ERR_UNSUPPORTED;
     void* scratch = nullptr;

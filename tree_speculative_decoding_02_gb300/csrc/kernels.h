@@ -9,7 +9,7 @@
 
 namespace ddt {
 
-constexpr int kBuildChunk = 8192;  // tokens per CTA in the build's logit pass
+
 constexpr int kMaxDepth = 64;      // deepest tree the build supports
 constexpr int kMaxTopK = 32;
 constexpr int kMaxBudget = 1023;
