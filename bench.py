@@ -270,18 +270,11 @@ def make_step(r, flat, ev):
                            workspace=r.build_ws)
         mark("build")
         kw = {}
-        if r.Lf and r.page:
-            a = r.attn
-            ddt.ddt_tree_attn_paged(a.q, a.k_tree, a.v_tree, r.k_pages, r.v_pages, r.block_table, r.prefix_len,
-                                    r.tree["n_nodes"], r.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out=r.attn_o,
-                                    status=r.attn_status, workspace=r.attn_ws)
-            mark("attn")
-        elif r.Lf:
-            a = r.attn
-            ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, r.prefix_len, r.tree["n_nodes"],
-                              r.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out=r.attn_o, status=r.attn_status,
-                              workspace=r.attn_ws)
-            kw.update(k_tree=a.k_tree, v_tree=a.v_tree, k_cache=a.k_cache, v_cache=a.v_cache)
+        if r.Lf:
+            r.attention()   # (with rotary embedding: the keys' in-place rotation, then the fused call)
+            if not r.page:
+                a = r.attn
+                kw.update(k_tree=a.k_tree, v_tree=a.v_tree, k_cache=a.k_cache, v_cache=a.v_cache)
             mark("attn")
         if r.Lg:
             g = r.gdn
@@ -373,6 +366,8 @@ def run_ours(args, rank, world, local):
         cfg["budget"] = max(cfg["budgets"])
     if args.kv_page:
         cfg["page"] = args.kv_page
+    if args.rope and cfg.get("Lf"):
+        cfg["rope"] = cfg["d"]
     cfg["flat"] = args.flat
     r = Round(cfg, device=dev, workload=args.workload)
     st = torch.cuda.current_stream()
@@ -446,10 +441,13 @@ def run_ours(args, rank, world, local):
                                        f"mean accepted drafted nodes {accepted:.2f}")
     if args.kv_page:
         out["config"]["kv"] = f"paged: {args.kv_page} rows a page, shuffled block table"
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg and not args.kv_page:
+    if args.rope:
+        out["config"]["rope"] = ("rotary embedding by depth: tree keys rotated in place, q rotated inside the "
+                                 "fused attention call (inputs taken before rotation)")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg and not (args.kv_page or args.rope):
         out["cpu_baseline"] = cpu_baseline(r, seconds=args.cpu_seconds)
     if rank == 0 and world == 1 and args.per_config and args.workload == WORKLOAD and not (
-            args.kv_page or args.flat or args.planted):
+            args.kv_page or args.flat or args.planted or args.rope):
         del r
         torch.cuda.empty_cache()
         out["per_config"] = [config_line(w, dev, peaks, tc_peak, tc_kind, not args.no_cpu_baseline)
@@ -801,6 +799,8 @@ def main():
     ap.add_argument("--flat", action="store_true", help="flat-commit safe mode: walk first children only")
     ap.add_argument("--planted", type=float, default=0.0,
                     help="plant accepted paths with this mean length (0: random targets, little accepted)")
+    ap.add_argument("--rope", action="store_true",
+                    help="rotary embedding by depth: keys rotated in place, q inside the fused attention call")
     ap.add_argument("--kv-page", type=int, default=0,
                     help="paged prefix caches with this many rows a page (0: contiguous)")
     args = ap.parse_args()

@@ -203,6 +203,39 @@ ddt_status ddt_tree_attn_paged(int n_layers, int B, int N, int Hq, int Hkv, int 
                                void* workspace, size_t ws_bytes, ddt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * ddt_tree_attn_rope / ddt_tree_attn_paged_rope -- [NOTES] "Where the next step is":
+ * branch attention over (paged) KV with rotary embedding by branch depth, fused.
+ *
+ * Same results as ddt_rope_tree on q followed by ddt_tree_attn (resp. _paged) -- bit for
+ * bit: q is given BEFORE rotary embedding and each of its rows is rotated at its node's
+ * position (position [B][N], as written by ddt_build_tree) while the kernel stages it, in
+ * the arithmetic of ddt_rope_tree, then rounded to bf16 once.  q is never committed, so
+ * nothing else changes; k_tree must already be rotated (ddt_rope_tree with q = NULL
+ * rotates the keys alone, in place, which the commit then copies).
+ *   rot_dim: a multiple of 16, 16 <= rot_dim <= d; theta > 1 (ddt_rope_tree's meaning).
+ *   bf16 with d in {128, 256} only (DDT_ERR_UNSUPPORTED otherwise).
+ *   workspace: the workspace of the plain call rounded up to 256 bytes, plus
+ *     B * N * rot_dim * 4 bytes for the per-row cos/sin table; 16-byte aligned.
+ * All other arguments, outputs and statuses are those of ddt_tree_attn / _paged.
+ * ------------------------------------------------------------------------------- */
+ddt_status ddt_tree_attn_rope(int n_layers, int B, int N, int Hq, int Hkv, int d, int Pcap,
+                              ddt_dtype in_dtype, ddt_dtype out_dtype, const void* q,
+                              const void* k_tree, const void* v_tree, const void* k_cache,
+                              const void* v_cache, const int32_t* prefix_len,
+                              const int32_t* n_nodes, const uint32_t* anc, const int32_t* position,
+                              int rot_dim, double theta, float scale, void* o, int32_t* status,
+                              void* workspace, size_t ws_bytes, ddt_stream_t stream);
+ddt_status ddt_tree_attn_paged_rope(int n_layers, int B, int N, int Hq, int Hkv, int d,
+                                    int page_size, int num_pages, int max_pages,
+                                    ddt_dtype in_dtype, ddt_dtype out_dtype, const void* q,
+                                    const void* k_tree, const void* v_tree, const void* k_pages,
+                                    const void* v_pages, const int32_t* block_table,
+                                    const int32_t* prefix_len, const int32_t* n_nodes,
+                                    const uint32_t* anc, const int32_t* position, int rot_dim,
+                                    double theta, float scale, void* o, int32_t* status,
+                                    void* workspace, size_t ws_bytes, ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * ddt_rope_tree -- [NOTES] "Where the next step is": position and RoPE correctness by
  * branch depth.  Rotary embedding of the tree rows, in place, at each node's own position
  * (position[b][n] from ddt_build_tree: prefix_len + depth, shared by siblings).
@@ -215,7 +248,9 @@ ddt_status ddt_tree_attn_paged(int n_layers, int B, int N, int Hq, int Hkv, int 
  * READING: the pages give no rotary formula; this is the half-split convention of
  * Qwen-style models, with partial rotation (rot_dim < d) allowed.  Rows of padding
  * nodes are left unchanged.  Call it before ddt_tree_attn / ddt_commit so that the
- * committed keys are the rotated ones.  rot_dim even, 2 <= rot_dim <= d; theta > 1.
+ * committed keys are the rotated ones.  q may be NULL: then only the keys are rotated
+ * (for the fused ddt_tree_attn_rope, which rotates q itself).  rot_dim even,
+ * 2 <= rot_dim <= d; theta > 1.
  * ------------------------------------------------------------------------------- */
 ddt_status ddt_rope_tree(int n_layers, int B, int N, int Hq, int Hkv, int d, int rot_dim,
                          double theta, ddt_dtype dtype, const int32_t* position,

@@ -149,10 +149,85 @@ ddt_status ddt_rope_tree(int n_layers, int B, int N, int Hq, int Hkv, int d, int
                          ddt_stream_t stream) {
     if (n_layers < 1 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || d < 2 || !dtype_ok(dtype)) return DDT_ERR_INVALID_ARG;
     if (rot_dim < 2 || rot_dim > d || rot_dim % 2 != 0 || !(theta > 1.0)) return DDT_ERR_INVALID_ARG;
-    if (!position || !n_nodes || !q || !k_tree) return DDT_ERR_INVALID_ARG;
+    if (!position || !n_nodes || !k_tree) return DDT_ERR_INVALID_ARG;  // q NULL: rotate the keys only
     if (B > 65535) return DDT_ERR_UNSUPPORTED;
     return from_cuda(launch_rope_tree(n_layers, B, N, Hq, Hkv, d, rot_dim, theta, dtype, position, n_nodes, q, k_tree,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Rotary variants: q is taken before rotary embedding and rotated while the attention
+// kernel stages it; the cos/sin table of every row's position goes to the end of the
+// workspace (after the ddt_tree_attn(_paged)_workspace bytes).
+static size_t rope_table_offset(size_t base) { return (base + 255) & ~(size_t)255; }
+
+static ddt_status rope_args_ok(int d, ddt_dtype in_dtype, int rot_dim, double theta, const int32_t* position) {
+    if (!position || rot_dim < 16 || rot_dim > d || rot_dim % 16 != 0 || !(theta > 1.0)) return DDT_ERR_INVALID_ARG;
+    if (in_dtype != DDT_BF16 || (d != 128 && d != 256)) return DDT_ERR_UNSUPPORTED;
+    return DDT_OK;
+}
+
+ddt_status ddt_tree_attn_rope(int n_layers, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype in_dtype,
+                              ddt_dtype out_dtype, const void* q, const void* k_tree, const void* v_tree,
+                              const void* k_cache, const void* v_cache, const int32_t* prefix_len,
+                              const int32_t* n_nodes, const uint32_t* anc, const int32_t* position, int rot_dim,
+                              double theta, float scale, void* o, int32_t* status, void* workspace, size_t ws_bytes,
+                              ddt_stream_t stream) {
+    if (n_layers < 1 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Pcap < 0 || Hq % Hkv != 0 || !dtype_ok(in_dtype) ||
+        !dtype_ok(out_dtype))
+        return DDT_ERR_INVALID_ARG;
+    if (N > kMaxRows || B > 65535) return DDT_ERR_UNSUPPORTED;
+    const ddt_status ra = rope_args_ok(d, in_dtype, rot_dim, theta, position);
+    if (ra != DDT_OK) return ra;
+    if (!q || !k_tree || !v_tree || (Pcap > 0 && (!k_cache || !v_cache)) || !prefix_len || !n_nodes || !anc || !o ||
+        !status || !workspace || !aligned16(workspace))
+        return DDT_ERR_INVALID_ARG;
+    const size_t base = attn_tc_ws_bytes(n_layers, B, N, Hq, Hkv, d, Pcap);
+    const size_t off = rope_table_offset(base);
+    if (ws_bytes < off + sizeof(float) * (size_t)B * N * rot_dim) return DDT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(o) ||
+        (Pcap > 0 && (!aligned16(k_cache) || !aligned16(v_cache))))
+        return DDT_ERR_INVALID_ARG;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* table = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + off);
+    cudaError_t e = launch_rope_table(B, N, rot_dim, theta, position, n_nodes, table, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    const AttnRope rope{rot_dim, table};
+    return from_cuda(launch_attn_tc(n_layers, B, N, Hq, Hkv, d, Pcap, out_dtype, q, k_tree, v_tree, k_cache, v_cache,
+                                    prefix_len, n_nodes, anc, scale, o, status, workspace, base, st, &rope));
+}
+
+ddt_status ddt_tree_attn_paged_rope(int n_layers, int B, int N, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                    int max_pages, ddt_dtype in_dtype, ddt_dtype out_dtype, const void* q,
+                                    const void* k_tree, const void* v_tree, const void* k_pages, const void* v_pages,
+                                    const int32_t* block_table, const int32_t* prefix_len, const int32_t* n_nodes,
+                                    const uint32_t* anc, const int32_t* position, int rot_dim, double theta,
+                                    float scale, void* o, int32_t* status, void* workspace, size_t ws_bytes,
+                                    ddt_stream_t stream) {
+    if (n_layers < 1 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || num_pages < 1 || max_pages < 1 ||
+        !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+        return DDT_ERR_INVALID_ARG;
+    if (!page_rows_ok(page_size) || (long)page_size * max_pages > (1L << 30)) return DDT_ERR_UNSUPPORTED;
+    if (N > kMaxRows || B > 65535) return DDT_ERR_UNSUPPORTED;
+    const ddt_status ra = rope_args_ok(d, in_dtype, rot_dim, theta, position);
+    if (ra != DDT_OK) return ra;
+    if (!q || !k_tree || !v_tree || !k_pages || !v_pages || !block_table || !prefix_len || !n_nodes || !anc || !o ||
+        !status || !workspace || !aligned16(workspace))
+        return DDT_ERR_INVALID_ARG;
+    const size_t base = attn_tc_ws_bytes(n_layers, B, N, Hq, Hkv, d, page_size * max_pages);
+    const size_t off = rope_table_offset(base);
+    if (ws_bytes < off + sizeof(float) * (size_t)B * N * rot_dim) return DDT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(o) || !aligned16(k_pages) ||
+        !aligned16(v_pages))
+        return DDT_ERR_INVALID_ARG;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* table = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + off);
+    cudaError_t e = launch_rope_table(B, N, rot_dim, theta, position, n_nodes, table, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    const AttnPaging pg{page_size, num_pages, max_pages, block_table};
+    const AttnRope rope{rot_dim, table};
+    return from_cuda(launch_attn_tc_paged(n_layers, B, N, Hq, Hkv, d, pg, out_dtype, q, k_tree, v_tree, k_pages,
+                                          v_pages, prefix_len, n_nodes, anc, scale, o, status, workspace, base, st,
+                                          &rope));
 }
 
 // ------------------------------------------------------------------------------ GDN

@@ -63,6 +63,11 @@ struct TcParams {
     float2* part_ml;      // [S][L][B][Hkv][MT*128] (row max in log2 units, row sum)
     int32_t* status;
     float scale_log2;
+    // rotary embedding of q by tree-row position (rope_rot == 0: q is already rotated):
+    // pairs (i, i + rope_rot / 2) of the first rope_rot channels, cos/sin per row from
+    // rope_table [B][N][rope_rot]
+    int rope_rot;
+    const float* rope_table;
 };
 
 constexpr int kThreads = 384;  // 0 TMA, 1 MMA, 2-3 setup, 4-11 softmax
@@ -701,16 +706,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::prefetch_tmap(&tm_kt);
         tc::prefetch_tmap(&tm_vt);
     }
-    // Q: 128 rows x D bf16, K-major with the 128-byte swizzle (64-column blocks of 128 rows)
-    for (int e = tid; e < 128 * (D / 8); e += kThreads) {
-        const int r = e / (D / 8), c = e % (D / 8);
-        const int R = row0 + r;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (R < p.N * p.G) {
-            const int node = R / p.G, h = g * p.G + R % p.G;
-            if (node < nn) v = __ldg(reinterpret_cast<const uint4*>(p.q + ((lb * p.N + node) * p.Hq + h) * D) + c);
+    // Q: 128 rows x D bf16, K-major with the 128-byte swizzle (64-column blocks of 128 rows).
+    // With a rotary table, 16-byte chunk c < rot/16 and its partner c + rot/16 are rotated
+    // together in fp32 (the arithmetic of ddt_rope_tree) and rounded once to bf16.
+    {
+        auto qstore = [&](int r, int c, uint4 v) {
+            *reinterpret_cast<uint4*>(sQ + (c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        };
+        const int rc = p.rope_rot / 8;  // rotated 16-byte chunks
+        for (int e = tid; e < 128 * (D / 8); e += blockDim.x) {
+            const int r = e / (D / 8), c = e % (D / 8);
+            if (c >= rc / 2 && c < rc) continue;  // second half of a rotary pair: with its partner
+            const int R = row0 + r;
+            const __nv_bfloat16* qrow = nullptr;
+            int node = 0;
+            if (R < p.N * p.G) {
+                node = R / p.G;
+                const int h = g * p.G + R % p.G;
+                if (node < nn) qrow = p.q + ((lb * p.N + node) * p.Hq + h) * D;
+            }
+            if (c >= rc) {
+                qstore(r, c, qrow ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0));
+                continue;
+            }
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+            if (qrow) {
+                const uint4 a = __ldg(reinterpret_cast<const uint4*>(qrow) + c);
+                const uint4 bq = __ldg(reinterpret_cast<const uint4*>(qrow) + c + rc / 2);
+                const float* cs = p.rope_table + ((long)b * p.N + node) * p.rope_rot + 8 * c;
+                const float* sn = cs + p.rope_rot / 2;
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
+                uint32_t ow0[4], ow1[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float x0[2], x1[2], y0[2], y1[2];
+                    x0[0] = __uint_as_float(aw[u] << 16);
+                    x0[1] = __uint_as_float(aw[u] & 0xffff0000u);
+                    x1[0] = __uint_as_float(bw[u] << 16);
+                    x1[1] = __uint_as_float(bw[u] & 0xffff0000u);
+#pragma unroll
+                    for (int z = 0; z < 2; ++z) {
+                        const float cz = cs[2 * u + z], sz = sn[2 * u + z];
+                        y0[z] = __fmaf_rn(x0[z], cz, __fmul_rn(-x1[z], sz));
+                        y1[z] = __fmaf_rn(x1[z], cz, __fmul_rn(x0[z], sz));
+                    }
+                    ow0[u] = pack_bf16(y0[0], y0[1]);
+                    ow1[u] = pack_bf16(y1[0], y1[1]);
+                }
+                lo = make_uint4(ow0[0], ow0[1], ow0[2], ow0[3]);
+                hi = make_uint4(ow1[0], ow1[1], ow1[2], ow1[3]);
+            }
+            qstore(r, c, lo);
+            qstore(r, c + rc / 2, hi);
         }
-        *reinterpret_cast<uint4*>(sQ + (c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
     }
     tc::fence_proxy_async();
     tc::tc_fence_before();
@@ -1203,7 +1251,7 @@ static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, i
                                   const void* q, const void* k_tree, const void* v_tree, const void* k_cache,
                                   const void* v_cache, const AttnPaging* pg, const int32_t* prefix_len,
                                   const int32_t* n_nodes, const uint32_t* anc, float scale, void* o, int32_t* status,
-                                  void* ws, size_t ws_bytes, cudaStream_t st) {
+                                  void* ws, size_t ws_bytes, cudaStream_t st, const AttnRope* rope) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     TcParams prm;
@@ -1248,6 +1296,9 @@ static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, i
     prm.num_pages = pg ? pg->num_pages : 0;
     prm.max_pages = pg ? pg->max_pages : 0;
     prm.block_table = pg ? pg->block_table : nullptr;
+    prm.rope_rot = rope ? rope->rot : 0;
+    prm.rope_table = rope ? rope->table : nullptr;
+    if (rope && !pair) return cudaErrorInvalidValue;  // q rotation is staged by the pair kernel only
 
     // tensor maps: caches (d, position, layer*B*Hkv), tree rows (d, kv head, node, layer*B)
     CUtensorMap maps[4];
@@ -1303,18 +1354,19 @@ static cudaError_t attn_tc_launch(int L, int B, int N, int Hq, int Hkv, int d, i
 cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out, const void* q,
                            const void* k_tree, const void* v_tree, const void* k_cache, const void* v_cache,
                            const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
-                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st) {
+                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st,
+                           const AttnRope* rope) {
     return attn_tc_launch(L, B, N, Hq, Hkv, d, Pcap, out, q, k_tree, v_tree, k_cache, v_cache, nullptr, prefix_len,
-                          n_nodes, anc, scale, o, status, ws, ws_bytes, st);
+                          n_nodes, anc, scale, o, status, ws, ws_bytes, st, rope);
 }
 
 cudaError_t launch_attn_tc_paged(int L, int B, int N, int Hq, int Hkv, int d, const AttnPaging& pg, ddt_dtype out,
                                  const void* q, const void* k_tree, const void* v_tree, const void* k_pages,
                                  const void* v_pages, const int32_t* prefix_len, const int32_t* n_nodes,
                                  const uint32_t* anc, float scale, void* o, int32_t* status, void* ws,
-                                 size_t ws_bytes, cudaStream_t st) {
+                                 size_t ws_bytes, cudaStream_t st, const AttnRope* rope) {
     return attn_tc_launch(L, B, N, Hq, Hkv, d, pg.max_pages * pg.page_rows, out, q, k_tree, v_tree, k_pages, v_pages,
-                          &pg, prefix_len, n_nodes, anc, scale, o, status, ws, ws_bytes, st);
+                          &pg, prefix_len, n_nodes, anc, scale, o, status, ws, ws_bytes, st, rope);
 }
 
 }  // namespace ddt

@@ -50,22 +50,30 @@ struct AttnPaging {
     int page_rows, num_pages, max_pages;
     const int32_t* block_table;  // [B][max_pages]
 };
+// rotary embedding of q applied by the attention kernel while it stages q
+struct AttnRope {
+    int rot;             // rotated channels (a multiple of 16, <= d)
+    const float* table;  // [B][N][rot] from launch_rope_table
+};
 cudaError_t launch_attn_tc_paged(int L, int B, int N, int Hq, int Hkv, int d, const AttnPaging& pg, ddt_dtype out,
                                  const void* q, const void* k_tree, const void* v_tree, const void* k_pages,
                                  const void* v_pages, const int32_t* prefix_len, const int32_t* n_nodes,
                                  const uint32_t* anc, float scale, void* o, int32_t* status, void* ws,
-                                 size_t ws_bytes, cudaStream_t st);
+                                 size_t ws_bytes, cudaStream_t st, const AttnRope* rope = nullptr);
 size_t attn_tc_ws_bytes(int L, int B, int N, int Hq, int Hkv, int d, int Pcap);
 bool attn_tc_supported(int d, ddt_dtype in);
 cudaError_t launch_attn_tc(int L, int B, int N, int Hq, int Hkv, int d, int Pcap, ddt_dtype out, const void* q,
                            const void* k_tree, const void* v_tree, const void* k_cache, const void* v_cache,
                            const int32_t* prefix_len, const int32_t* n_nodes, const uint32_t* anc, float scale,
-                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st);
+                           void* o, int32_t* status, void* ws, size_t ws_bytes, cudaStream_t st,
+                           const AttnRope* rope = nullptr);
 
 // one bounded wait on an mbarrier nothing signals; status[0] = its outcome
 cudaError_t launch_wait_selftest(int32_t* status, cudaStream_t st);
 cudaError_t launch_rope_tree(int L, int B, int N, int Hq, int Hkv, int d, int rot, double theta, ddt_dtype dtype,
                              const int32_t* position, const int32_t* n_nodes, void* q, void* k, cudaStream_t st);
+cudaError_t launch_rope_table(int B, int N, int rot, double theta, const int32_t* position, const int32_t* n_nodes,
+                              float* table, cudaStream_t st);
 bool gdn_tc_supported(int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in);
 cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype in, ddt_dtype out, const void* x,
                           const void* conv_w, const void* conv_state, const float* beta, const float* decay,

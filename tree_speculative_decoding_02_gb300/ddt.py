@@ -48,6 +48,10 @@ _SIGS = {
     "ddt_commit_paged": ([_c_int] * 9 + [_c_p] + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13,
                          _c_int),
     "ddt_rope_tree": ([_c_int] * 7 + [ctypes.c_double, _c_int] + [_c_p] * 5, _c_int),
+    "ddt_tree_attn_rope": ([_c_int] * 9 + [_c_p] * 9 + [_c_int, ctypes.c_double, _c_float, _c_p, _c_p, _c_p, _c_size,
+                                                     _c_p], _c_int),
+    "ddt_tree_attn_paged_rope": ([_c_int] * 11 + [_c_p] * 10 + [_c_int, ctypes.c_double, _c_float, _c_p, _c_p, _c_p,
+                                                                _c_size, _c_p], _c_int),
     "ddt_commit": ([_c_int] * 7 + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13, _c_int),
 }
 EXPORTS = tuple(_SIGS)
@@ -256,20 +260,95 @@ def ddt_tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, prefix
     return {"o": o, "status": st}
 
 
-def ddt_rope_tree(q, k_tree, position, n_nodes, *, rot_dim=None, theta=10000.0):
-    """In place: q [L][B][N][Hq][d], k_tree [L][B][N][Hkv][d] rotated at position [B][N]."""
+def ddt_rope_tree(q, k_tree, position, n_nodes, *, rot_dim=None, theta=10000.0, Hq=None):
+    """In place: q [L][B][N][Hq][d], k_tree [L][B][N][Hkv][d] rotated at position [B][N].
+    q may be None (keys only; then Hq is not needed)."""
     lib = _gpu()
-    L, B, N, Hq, d = q.shape
-    Hkv = k_tree.shape[3]
-    _need(q, (L, B, N, Hq, d), q.dtype, "q")
-    _need(k_tree, (L, B, N, Hkv, d), q.dtype, "k_tree")
+    L, B, N, Hkv, d = k_tree.shape
+    _need(k_tree, (L, B, N, Hkv, d), k_tree.dtype, "k_tree")
+    if q is not None:
+        Hq = q.shape[3]
+        _need(q, (L, B, N, Hq, d), k_tree.dtype, "q")
     _need(position, (B, N), torch.int32, "position")
     _need(n_nodes, (B,), torch.int32, "n_nodes")
     rot = int(rot_dim or d)
-    rc = lib.ddt_rope_tree(L, B, N, Hq, Hkv, d, rot, float(theta), _DT[q.dtype], _ptr(position), _ptr(n_nodes),
-                           _ptr(q), _ptr(k_tree), _stream())
+    rc = lib.ddt_rope_tree(L, B, N, int(Hq or 1), Hkv, d, rot, float(theta), _DT[k_tree.dtype], _ptr(position),
+                           _ptr(n_nodes), _ptr(q), _ptr(k_tree), _stream())
     _check(rc, "ddt_rope_tree")
     return q, k_tree
+
+
+def rope_workspace_bytes(base_bytes, B, N, rot_dim):
+    """Workspace of the rotary attention calls: the plain call's bytes rounded up to 256,
+    then the per-row cos/sin table."""
+    return ((int(base_bytes) + 255) // 256) * 256 + 4 * B * N * int(rot_dim)
+
+
+def ddt_tree_attn_rope(q, k_tree, v_tree, k_cache, v_cache, prefix_len, n_nodes, anc, position, *, scale: float,
+                       rot_dim=None, theta=10000.0, out_dtype=None, out=None, status=None, workspace=None):
+    """ddt_tree_attn with q BEFORE rotary embedding (rotated inside the kernel at position [B][N])."""
+    lib = _gpu()
+    L, B, N, Hq, d = q.shape
+    Hkv = k_tree.shape[3]
+    Pcap = k_cache.shape[3]
+    dt = q.dtype
+    _need(q, (L, B, N, Hq, d), dt, "q")
+    _need(k_tree, (L, B, N, Hkv, d), dt, "k_tree")
+    _need(v_tree, (L, B, N, Hkv, d), dt, "v_tree")
+    _need(k_cache, (L, B, Hkv, Pcap, d), dt, "k_cache")
+    _need(v_cache, (L, B, Hkv, Pcap, d), dt, "v_cache")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    _need(anc, (B, N, (N + 31) // 32), None, "anc")
+    _need(position, (B, N), torch.int32, "position")
+    out_dtype = out_dtype or dt
+    o = out if out is not None else torch.empty((L, B, N, Hq, d), dtype=out_dtype, device=q.device)
+    _need(o, (L, B, N, Hq, d), out_dtype, "o")
+    st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=q.device)
+    rot = int(rot_dim or d)
+    need = rope_workspace_bytes(lib.ddt_tree_attn_workspace(L, B, N, Hq, Hkv, d, Pcap), B, N, rot)
+    ws = workspace if workspace is not None else _ws(need, q.device)
+    rc = lib.ddt_tree_attn_rope(L, B, N, Hq, Hkv, d, Pcap, _DT[dt], _DT[out_dtype], _ptr(q), _ptr(k_tree),
+                                _ptr(v_tree), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_len), _ptr(n_nodes), _ptr(anc),
+                                _ptr(position), rot, float(theta), float(scale), _ptr(o), _ptr(st), _ptr(ws),
+                                ws.numel(), _stream())
+    _check(rc, "ddt_tree_attn_rope")
+    return {"o": o, "status": st}
+
+
+def ddt_tree_attn_paged_rope(q, k_tree, v_tree, k_pages, v_pages, block_table, prefix_len, n_nodes, anc, position, *,
+                             scale: float, rot_dim=None, theta=10000.0, out_dtype=None, out=None, status=None,
+                             workspace=None):
+    """ddt_tree_attn_paged with q BEFORE rotary embedding (rotated inside the kernel)."""
+    lib = _gpu()
+    L, B, N, Hq, d = q.shape
+    Hkv = k_tree.shape[3]
+    num_pages, page = k_pages.shape[1], k_pages.shape[3]
+    max_pages = block_table.shape[1]
+    dt = q.dtype
+    _need(q, (L, B, N, Hq, d), dt, "q")
+    _need(k_tree, (L, B, N, Hkv, d), dt, "k_tree")
+    _need(v_tree, (L, B, N, Hkv, d), dt, "v_tree")
+    _need(k_pages, (L, num_pages, Hkv, page, d), dt, "k_pages")
+    _need(v_pages, (L, num_pages, Hkv, page, d), dt, "v_pages")
+    _need(block_table, (B, max_pages), torch.int32, "block_table")
+    _need(prefix_len, (B,), torch.int32, "prefix_len")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    _need(anc, (B, N, (N + 31) // 32), None, "anc")
+    _need(position, (B, N), torch.int32, "position")
+    out_dtype = out_dtype or dt
+    o = out if out is not None else torch.empty((L, B, N, Hq, d), dtype=out_dtype, device=q.device)
+    _need(o, (L, B, N, Hq, d), out_dtype, "o")
+    st = status if status is not None else torch.empty((B,), dtype=torch.int32, device=q.device)
+    rot = int(rot_dim or d)
+    need = rope_workspace_bytes(lib.ddt_tree_attn_paged_workspace(L, B, N, Hq, Hkv, d, page, max_pages), B, N, rot)
+    ws = workspace if workspace is not None else _ws(need, q.device)
+    rc = lib.ddt_tree_attn_paged_rope(L, B, N, Hq, Hkv, d, page, num_pages, max_pages, _DT[dt], _DT[out_dtype], _ptr(q),
+                                      _ptr(k_tree), _ptr(v_tree), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                      _ptr(prefix_len), _ptr(n_nodes), _ptr(anc), _ptr(position), rot, float(theta),
+                                      float(scale), _ptr(o), _ptr(st), _ptr(ws), ws.numel(), _stream())
+    _check(rc, "ddt_tree_attn_paged_rope")
+    return {"o": o, "status": st}
 
 
 # ----------------------------------------------------------------------------- GDN

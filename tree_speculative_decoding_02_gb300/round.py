@@ -56,8 +56,10 @@ class Round:
                                           workload=workload, dtype=dt, device=dev, poison=poison)
             self.attn_o = torch.empty((self.Lf, B, N, c["Hq"], c["d"]), dtype=attn_out_dtype or dt, device=dev)
             self.attn_status = torch.empty((B,), **i32)
-            self.attn_ws = torch.empty(max(16, ddt.load().ddt_tree_attn_workspace(
-                self.Lf, B, N, c["Hq"], c["Hkv"], c["d"], self.Pcap)), dtype=torch.uint8, device=dev)
+            ws = ddt.load().ddt_tree_attn_workspace(self.Lf, B, N, c["Hq"], c["Hkv"], c["d"], self.Pcap)
+            if c.get("rope"):
+                ws = ddt.rope_workspace_bytes(ws, B, N, int(c["rope"]))
+            self.attn_ws = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
             if self.page:
                 self._to_pages(workload)
         # GDN layers (state stored [dv][dk])
@@ -114,17 +116,7 @@ class Round:
                            out=self.tree, workspace=self.build_ws)
         if wait and self.Lf:
             wait("attn")
-        if self.Lf and self.page:
-            a = self.attn
-            ddt.ddt_tree_attn_paged(a.q, a.k_tree, a.v_tree, self.k_pages, self.v_pages, self.block_table,
-                                    self.prefix_len, self.tree["n_nodes"], self.tree["anc"],
-                                    scale=1.0 / math.sqrt(c["d"]), out_dtype=self.attn_o.dtype, out=self.attn_o,
-                                    status=self.attn_status, workspace=self.attn_ws)
-        elif self.Lf:
-            a = self.attn
-            ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, self.prefix_len, self.tree["n_nodes"],
-                              self.tree["anc"], scale=1.0 / math.sqrt(c["d"]), out_dtype=self.attn_o.dtype,
-                              out=self.attn_o, status=self.attn_status, workspace=self.attn_ws)
+        self.attention()
         if self.Lg:
             if wait:
                 wait("gdn")
@@ -153,6 +145,33 @@ class Round:
                                  v_pages=self.v_pages, out=self.commit, **kw)
         else:
             ddt.ddt_commit(self.walk["acc_nodes"], self.walk["acc_len"], self.prefix_len, out=self.commit, **kw)
+
+    def attention(self):
+        """The round's attention call.  With cfg["rope"] (rotated channels) q and the tree
+        keys are taken before rotary embedding: the keys are rotated in place at their
+        positions (they are committed), and q inside the fused attention call."""
+        if not self.Lf:
+            return
+        c, a = self.cfg, self.attn
+        scale = 1.0 / math.sqrt(c["d"])
+        rot = int(c.get("rope", 0))
+        if rot:
+            ddt.ddt_rope_tree(None, a.k_tree, self.tree["position"], self.tree["n_nodes"], rot_dim=rot, Hq=c["Hq"])
+        common = dict(scale=scale, out_dtype=self.attn_o.dtype, out=self.attn_o, status=self.attn_status,
+                      workspace=self.attn_ws)
+        if self.page and rot:
+            ddt.ddt_tree_attn_paged_rope(a.q, a.k_tree, a.v_tree, self.k_pages, self.v_pages, self.block_table,
+                                         self.prefix_len, self.tree["n_nodes"], self.tree["anc"], self.tree["position"],
+                                         rot_dim=rot, **common)
+        elif self.page:
+            ddt.ddt_tree_attn_paged(a.q, a.k_tree, a.v_tree, self.k_pages, self.v_pages, self.block_table,
+                                    self.prefix_len, self.tree["n_nodes"], self.tree["anc"], **common)
+        elif rot:
+            ddt.ddt_tree_attn_rope(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, self.prefix_len, self.tree["n_nodes"],
+                                   self.tree["anc"], self.tree["position"], rot_dim=rot, **common)
+        else:
+            ddt.ddt_tree_attn(a.q, a.k_tree, a.v_tree, a.k_cache, a.v_cache, self.prefix_len, self.tree["n_nodes"],
+                              self.tree["anc"], **common)
 
     def restore_prefix(self):
         """Reset the committed prefix lengths (the commit advanced them)."""
