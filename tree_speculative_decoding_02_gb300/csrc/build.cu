@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(kRowThreads) k_build_row(const T* __restrict__
     }
     const bool row_bad = s_bad != 0;
 
-    // ---- pass 2: sum of exp(v - M) (fp32 per load of 8 and per thread, fp64 across
-    //      threads) and the entries that reach tau
+    // ---- pass 2: sum of exp(v - M) (fp32 per load of 8, per thread and across the warp,
+    //      fp64 across warps) and the entries that reach tau
     const float LOG2E = 1.4426950408889634f;
     const float mb = M * LOG2E;
     float acc = 0.f;
@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(kRowThreads) k_build_row(const T* __restrict__
             }
         }
     }
-    const double ws = warp_sum((double)acc);
-    if (lane == 0) s_sum[warp] = ws;
+    const float ws = warp_sum(acc);  // tree sum in fp32 across the warp, fp64 across warps
+    if (lane == 0) s_sum[warp] = (double)ws;
     __syncthreads();
     const int nc = s_nc;
     if (nc > kCandCap && !row_bad) {
@@ -388,35 +388,39 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int k, int budge
                 }
                 best = w;
             }
-            int nf = 0;
+            // the popped entry leaves the frontier (its slot takes the last entry); lane 0
+            // pushes its next-ranked sibling and lane 1 its best child at the same time
+            const Cand c = S.front[best];
+            const bool has_sib = c.rank + 1 < k, has_ch = c.depth < D;
+            const int me = n_sel, nf = n_front - 1;
+            __syncwarp();
             if (lane == 0) {
-                const Cand c = S.front[best];
-                S.front[best] = S.front[n_front - 1];
-                S.fs[best] = S.fs[n_front - 1];
-                nf = n_front - 1;
-                const int me = n_sel;
+                S.front[best] = S.front[nf];
+                S.fs[best] = S.fs[nf];
                 S.sel[me] = c;
-                const double L_par = (c.parent < 0) ? 0.0 : S.sel[c.parent].L;
-                if (c.rank + 1 < k) {  // next-ranked sibling: same parent, same depth
-                    Cand sib = c;
-                    sib.rank = c.rank + 1;
-                    sib.L = L_par + S.top_vd[(c.depth - 1) * k + sib.rank];
-                    sib.s = sib.L - S.cum[c.depth];
-                    S.front[nf] = sib;
-                    S.fs[nf++] = score_key(sib.s);
-                }
-                if (c.depth < D) {  // best child
-                    Cand ch;
-                    ch.depth = c.depth + 1;
-                    ch.rank = 0;
-                    ch.parent = me;
-                    ch.L = c.L + S.top_vd[c.depth * k];
-                    ch.s = ch.L - S.cum[c.depth + 1];
-                    S.front[nf] = ch;
-                    S.fs[nf++] = score_key(ch.s);
-                }
             }
-            n_front = __shfl_sync(kFull, nf, 0);
+            __syncwarp();
+            if (lane == 0 && has_sib) {  // same parent, same depth
+                const double L_par = (c.parent < 0) ? 0.0 : S.sel[c.parent].L;
+                Cand sib = c;
+                sib.rank = c.rank + 1;
+                sib.L = L_par + S.top_vd[(c.depth - 1) * k + sib.rank];
+                sib.s = sib.L - S.cum[c.depth];
+                S.front[nf] = sib;
+                S.fs[nf] = score_key(sib.s);
+            }
+            if (lane == 1 && has_ch) {
+                Cand ch;
+                ch.depth = c.depth + 1;
+                ch.rank = 0;
+                ch.parent = me;
+                ch.L = c.L + S.top_vd[c.depth * k];
+                ch.s = ch.L - S.cum[c.depth + 1];
+                ch.pad = 0;
+                S.front[nf + has_sib] = ch;
+                S.fs[nf + has_sib] = score_key(ch.s);
+            }
+            n_front = nf + has_sib + has_ch;
             ++n_sel;
             __syncwarp();
         }
@@ -530,8 +534,8 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
         k_build_row<__nv_bfloat16><<<counted(g1), kRowThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), D, V,
                                                                           k, vec, rows, tv, ti);
     else
-        k_build_row<float><<<counted(g1), kRowThreads, 0, st>>>(static_cast<const float*>(logits), D, V, k,
-                                                                  vec && (V % 8 == 0), rows, tv, ti);
+        k_build_row<float><<<counted(g1), kRowThreads, 0, st>>>(static_cast<const float*>(logits), D, V, k, vec, rows,
+                                                                  tv, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t sm = build_tree_smem(D, k, budget);
