@@ -47,7 +47,7 @@ def _load():
             lib = ctypes.CDLL(build())
             for name in ("ddto_build_tree", "ddto_attn_row", "ddto_tree_attn", "ddto_gdn_unit",
                          "ddto_tree_gdn", "ddto_walk", "ddto_commit", "ddto_gather_pages",
-                         "ddto_scatter_pages", "ddto_rope_tree", "ddto_walk_flat"):
+                         "ddto_scatter_pages", "ddto_rope_tree", "ddto_walk_flat", "ddto_walk_sample"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -243,6 +243,31 @@ def walk(token, parent, n_nodes, D: int, target_logits=None, target_argmax=None,
             _p(out["target_argmax"]), _p(out["acc_nodes"]), _p(out["acc_len"]), _p(out["bonus"]),
             _p(out["emitted"]), _p(out["n_emitted"]))
     _check(rc, "walk")
+    return out
+
+
+def walk_sample(token, parent, n_nodes, D: int, target_logits, uniforms, temperature: float, C: int):
+    """Tree-walk rejection sampling.  target_logits [B][N][V]; uniforms [B][D+1][C+1];
+    C = the most children a node may have.  Adds status [B] and margin [B] (the smallest
+    distance between a uniform's target and its threshold over the request's decisions)."""
+    lib = _load()
+    token, parent = _i32(token), _i32(parent)
+    B, N = token.shape
+    A = D + 1
+    tl = _f64(target_logits)
+    V = tl.shape[2]
+    U = _f64(uniforms)
+    if U.shape != (B, A, C + 1):
+        raise ValueError(f"uniforms must be [B][D+1][C+1] = {(B, A, C + 1)}, got {U.shape}")
+    out = {"acc_nodes": np.zeros((B, A), np.int32), "acc_len": np.zeros(B, np.int32),
+           "bonus": np.zeros(B, np.int32), "emitted": np.zeros((B, A), np.int32),
+           "n_emitted": np.zeros(B, np.int32), "margin": np.zeros(B, np.float64),
+           "status": np.zeros(B, np.int32)}
+    rc = lib.ddto_walk_sample(B, N, V, D, C, ctypes.c_double(float(temperature)), _p(tl), _p(U), _p(token),
+                              _p(parent), _p(_i32(n_nodes)), _p(out["acc_nodes"]), _p(out["acc_len"]),
+                              _p(out["bonus"]), _p(out["emitted"]), _p(out["n_emitted"]), _p(out["margin"]),
+                              _p(out["status"]))
+    _check(rc, "walk_sample")
     return out
 
 

@@ -565,6 +565,131 @@ int ddto_walk_flat(int B, int N, int V, int D, const double* target_logits,
                      acc_nodes, acc_len, bonus, emitted, n_emitted, 1);
 }
 
+/* Tree-walk rejection sampling: see ddt_oracle.h for the READING.  p_u is formed row by
+ * row in fp64 (max-shifted exponentials, their plain sum); every comparison of a
+ * probability with a uniform is in fp64. */
+static double min_d(double a, double b) { return a < b ? a : b; }
+
+int ddto_walk_sample(int B, int N, int V, int D, int C, double T, const double* target_logits,
+                     const double* uniforms, const int32_t* token, const int32_t* parent,
+                     const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
+                     int32_t* emitted, int32_t* n_emitted, double* margin, int32_t* status) {
+    if (B < 1 || N < 1 || V < 1 || D < 0 || C < 1 || !(T > 0.0)) return DDTO_ERR_ARG;
+    const int A = D + 1;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    char* rejected = (char*)malloc((size_t)V);
+    int* kids = (int*)malloc(sizeof(int) * (size_t)N);
+    for (int b = 0; b < B; ++b) {
+        const int nn = n_nodes[b];
+        const int32_t* tok = token + (long)b * N;
+        const int32_t* par = parent + (long)b * N;
+        int32_t* an = acc_nodes + (long)b * A;
+        int32_t* em = emitted + (long)b * A;
+        for (int j = 0; j < A; ++j) an[j] = em[j] = -1;
+        acc_len[b] = 0;
+        bonus[b] = -1;
+        n_emitted[b] = 0;
+        margin[b] = INFINITY;
+        /* the tree: parents before children, tokens in range, at most C children a node,
+         * no token twice among one node's children */
+        int st = (nn >= 1 && nn <= N) ? DDTO_OK : DDTO_ERR_TREE;
+        if (st == DDTO_OK && par[0] != -1) st = DDTO_ERR_TREE;
+        for (int i = 1; st == DDTO_OK && i < nn; ++i)
+            if (par[i] < 0 || par[i] >= i || tok[i] < 0 || tok[i] >= V) st = DDTO_ERR_TREE;
+        for (int u = 0; st == DDTO_OK && u < nn; ++u) {
+            int m = 0;
+            for (int i = 1; i < nn; ++i)
+                if (par[i] == u) {
+                    for (int j = 0; j < m; ++j)
+                        if (tok[kids[j]] == tok[i]) st = DDTO_ERR_TREE;
+                    kids[m++] = i;
+                }
+            if (m > C) st = DDTO_ERR_TREE;
+        }
+        for (int i = 0; st == DDTO_OK && i < nn; ++i)
+            for (int v = 0; v < V; ++v)
+                if (!isfinite(target_logits[((long)b * N + i) * V + v])) {
+                    st = DDTO_ERR_NONFINITE;
+                    break;
+                }
+        status[b] = st;
+        if (st != DDTO_OK) {
+            margin[b] = 0.0;
+            continue;
+        }
+        int cur = 0, a = 0;
+        an[0] = 0;
+        for (;;) {
+            /* p_u = softmax(logits[u] / T) */
+            const double* row = target_logits + ((long)b * N + cur) * V;
+            double mx = row[0];
+            for (int v = 1; v < V; ++v)
+                if (row[v] > mx) mx = row[v];
+            double Z = 0.0;
+            for (int v = 0; v < V; ++v) {
+                p[v] = exp((row[v] - mx) / T);
+                Z += p[v];
+            }
+            for (int v = 0; v < V; ++v) p[v] /= Z;
+            memset(rejected, 0, (size_t)V);
+            const double* U = uniforms + ((long)b * A + a) * (C + 1);
+            double R = 0.0;
+            int next = -1;
+            if (a + 1 < A) {
+                int i = 0;
+                for (int c = 1; c < nn; ++c) {
+                    if (par[c] != cur) continue;
+                    const double thr = p[tok[c]] / (1.0 - R);
+                    margin[b] = min_d(margin[b], fabs(U[i] - thr));
+                    if (U[i] < thr) {
+                        next = c;
+                        break;
+                    }
+                    R += p[tok[c]];
+                    rejected[tok[c]] = 1;
+                    ++i;
+                }
+            }
+            if (next < 0) {
+                /* bonus from the residual: rejected children removed, renormalised */
+                const double target = U[C] * (1.0 - R);
+                double run = 0.0;
+                int t = -1;
+                for (int v = 0; v < V; ++v) {
+                    if (rejected[v]) continue;
+                    const double before = run;
+                    run += p[v];
+                    if (run > target) {
+                        t = v;
+                        margin[b] = min_d(margin[b], min_d(target - before, run - target));
+                        break;
+                    }
+                }
+                if (t < 0) {
+                    for (int v = V - 1; v >= 0; --v)
+                        if (!rejected[v] && p[v] > 0.0) {
+                            t = v;
+                            break;
+                        }
+                    margin[b] = 0.0;
+                }
+                bonus[b] = t;
+                break;
+            }
+            cur = next;
+            an[++a] = cur;
+        }
+        acc_len[b] = a;
+        for (int j = 1; j <= a; ++j) em[j - 1] = tok[an[j]];
+        em[a] = bonus[b];
+        n_emitted[b] = a + 1;
+    }
+    free(p);
+    free(rejected);
+    free(kids);
+    return DDTO_OK;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Commit                                                                     */
 /* ------------------------------------------------------------------------- */

@@ -15,6 +15,13 @@
  *            Tree Construction and Verification".
  *   [CHALL]  "The Architecture of Speculation: Bridging DFlash and DDTree for
  *            Production Inference", section "The DDTree Integration Challenge".
+ *   [VALID]  "The Moment of Truth: Validating DDTree Speculative Decoding on
+ *            Qwen3.6-27B", section "The Path to This Message" (the serving stack's
+ *            sampler is a linear-chain rejection sampler; a tree walk needs its own).
+ *   [SPEC]   The pages name tree-walk rejection sampling but give no algorithm.  The
+ *            acceptance rule used is speculative sampling's (Leviathan, Kalman and
+ *            Matias, ICML 2023; Chen et al., 2023), applied over a node's children
+ *            with point-mass drafts as in SpecInfer (Miao et al., ASPLOS 2024).
  *   [GDN]    The pages name Gated DeltaNet layers but print no formula.  The gated
  *            delta rule used here is the one of Yang, Kautz and Hatamizadeh, "Gated
  *            Delta Networks: Improving Mamba2 with Delta Rule" (ICLR 2025), in the
@@ -40,6 +47,7 @@ extern "C" {
 #define DDTO_ERR_ARG 1
 #define DDTO_ERR_TREE 7
 #define DDTO_ERR_CAPACITY 3
+#define DDTO_ERR_NONFINITE 6
 
 /*
  * Best-first tree build ([ARCH]; [CHALL] item 2).
@@ -130,6 +138,30 @@ int ddto_walk_flat(int B, int N, int V, int D, const double* target_logits,
                    const int32_t* target_argmax_in, const int32_t* token, const int32_t* parent,
                    const int32_t* n_nodes, int32_t* target_argmax_out, int32_t* acc_nodes,
                    int32_t* acc_len, int32_t* bonus, int32_t* emitted, int32_t* n_emitted);
+
+/*
+ * Tree-walk rejection sampling ([VALID]; [SPEC]; [NOTES] "What broke along the way" for
+ * accepted vs emitted tokens).  READING: at the visited node u (step s = depth of u),
+ * p_u = softmax(target_logits[u] / T).  u's children are tried in row order; with R the
+ * p_u-mass of the children already rejected, child i (token x_i, i counted from 0) is
+ * accepted iff U[s][i] < p_u(x_i) / (1 - R), else R += p_u(x_i).  An accepted child is
+ * the next node.  When every child is rejected (or u has none, or the walk has already
+ * taken max-depth steps) the bonus token is the smallest id t, rejected children
+ * skipped, whose running sum of p_u in id order exceeds U[s][C] * (1 - R); if rounding
+ * leaves no such t, the largest id with positive residual mass.
+ *   target_logits [B][N][V]; uniforms [B][D+1][C+1] in [0, 1); temperature T > 0.
+ *   Outputs as ddto_walk, plus status [B] (DDTO_OK; DDTO_ERR_TREE for a node with more
+ *   than C children, a repeated sibling token or a token outside [0, V);
+ *   DDTO_ERR_NONFINITE for a non-finite logit in a row of the tree; the walk outputs
+ *   are then the empty walk: acc_len 0, bonus -1, n_emitted 0) and margin [B]: the
+ *   smallest distance, in probability, between a uniform's target and the threshold it
+ *   was compared with over the request's decisions (for the bonus: to either end of the
+ *   chosen token's interval of the running sum; 0 for the rounding fallback).
+ */
+int ddto_walk_sample(int B, int N, int V, int D, int C, double T, const double* target_logits,
+                     const double* uniforms, const int32_t* token, const int32_t* parent,
+                     const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
+                     int32_t* emitted, int32_t* n_emitted, double* margin, int32_t* status);
 
 /*
  * Commit of the accepted path ([NOTES] "Why hybrid attention makes it hard",

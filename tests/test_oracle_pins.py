@@ -400,6 +400,167 @@ def test_walk_chain_is_longest_prefix():
     np.testing.assert_array_equal(out["emitted"][0][:4], [3, 1, 4, 2])
 
 
+# ==================================================== walk, rejection sampling
+def _softmax(x, T):
+    z = np.exp((x - x.max()) / T)
+    return z / z.sum()
+
+
+def _sample_case(lg, U, tok, par, D, C, T=1.0):
+    N = len(tok)
+    tl = np.asarray(lg, np.float64).reshape(1, N, -1)
+    return oracle.walk_sample(np.array([tok]), np.array([par]), [N], D, tl, np.asarray(U)[None], T, C)
+
+
+def test_walk_sample_worked_examples():
+    """Hand-worked decisions of the rule (speculative sampling with point-mass drafts over
+    a node's children): accept x with probability p(x) / (1 - R), R the rejected mass;
+    otherwise the bonus comes from p with the rejected tokens removed."""
+    p = np.array([0.5, 0.25, 0.125, 0.125])
+    lg = np.log(np.tile(p, (3, 1)))
+    tok, par = [7, 1, 2], [-1, 0, 0]   # root, children tokens 1 (p 1/4) then 2 (p 1/8)
+    # 0.2 < 1/4: the first child is accepted; its node has no children, so the bonus
+    # target is U = 0.6 and the running sum 0.5, 0.75 first passes it at id 1
+    o = _sample_case(lg, [[0.2, 0.0, 0.0], [0.0, 0.0, 0.6]], tok, par, 1, 2)
+    assert o["acc_len"][0] == 1 and o["acc_nodes"][0].tolist() == [0, 1]
+    assert o["emitted"][0].tolist() == [1, 1] and o["bonus"][0] == 1
+    assert o["margin"][0] == pytest.approx(0.05)            # min(|0.2-0.25|, 0.6-0.5, 0.75-0.6)
+    # 0.3 >= 1/4 rejects token 1 (R = 1/4); 0.1 < (1/8)/(3/4) = 1/6 accepts token 2
+    o = _sample_case(lg, [[0.3, 0.1, 0.0], [0.0, 0.0, 0.1]], tok, par, 1, 2)
+    assert o["acc_nodes"][0].tolist() == [0, 2] and o["emitted"][0].tolist() == [2, 0]
+    assert o["margin"][0] == pytest.approx(min(0.05, 1 / 6 - 0.1, 0.1))
+    # both rejected (R = 3/8): target 0.9 * 5/8 = 0.5625 over ids 0, 3 (0.5, 0.625) -> 3
+    o = _sample_case(lg, [[0.3, 0.9, 0.9], [0.0, 0.0, 0.0]], tok, par, 1, 2)
+    assert o["acc_len"][0] == 0 and o["bonus"][0] == 3 and o["emitted"][0].tolist() == [3, -1]
+    assert o["margin"][0] == pytest.approx(min(0.05, 0.9 - 1 / 6, 0.0625, 0.0625))
+    # target 0.4 * 5/8 = 0.25 < 0.5 -> id 0 (the bonus never lands on a rejected token)
+    o = _sample_case(lg, [[0.3, 0.9, 0.4], [0.0, 0.0, 0.0]], tok, par, 1, 2)
+    assert o["bonus"][0] == 0
+    # at max depth 0 no child is tried: the bonus comes from the whole p_root
+    o = _sample_case(lg, [[0.0, 0.0, 0.55]], tok, par, 0, 2)
+    assert o["acc_len"][0] == 0 and o["bonus"][0] == 1
+    # temperature: the child token 1 is compared at softmax([2, 1, 0] / 2)[1], the tempered
+    # probability, not at the untempered softmax([2, 1, 0])[1]
+    lg2 = np.array([[2.0, 1.0, 0.0]] * 2)
+    q = _softmax(lg2[0], 2.0)
+    for u, acc in ((q[1] - 1e-3, 1), (q[1] + 1e-3, 0)):
+        o = _sample_case(lg2, [[u, 0.0], [0.0, 0.0]], [5, 1], [-1, 0], 1, 1, T=2.0)
+        assert o["acc_len"][0] == acc
+
+
+def test_walk_sample_statuses():
+    lg = np.zeros((4, 5))
+    U = np.zeros((3, 3))
+    # three children with C = 2
+    o = _sample_case(lg, U, [0, 1, 2, 3], [-1, 0, 0, 0], 2, 2)
+    assert o["status"][0] == 7 and o["n_emitted"][0] == 0 and o["bonus"][0] == -1
+    # a repeated sibling token
+    o = _sample_case(lg, U, [0, 1, 1, 3], [-1, 0, 0, 1], 2, 2)
+    assert o["status"][0] == 7
+    # a token outside the vocabulary
+    o = _sample_case(lg, U, [0, 1, 5, 3], [-1, 0, 0, 1], 2, 2)
+    assert o["status"][0] == 7
+    # a parent after its child
+    o = _sample_case(lg, U, [0, 1, 2, 3], [-1, 0, 3, 1], 2, 2)
+    assert o["status"][0] == 7
+    # a NaN logit in a row of the tree
+    bad = lg.copy()
+    bad[3, 4] = np.nan
+    o = _sample_case(bad, U, [0, 1, 2, 3], [-1, 0, 0, 1], 2, 2)
+    assert o["status"][0] == 6 and o["acc_len"][0] == 0 and (o["emitted"][0] == -1).all()
+    o = _sample_case(lg, U, [0, 1, 2, 3], [-1, 0, 0, 1], 2, 2)
+    assert o["status"][0] == 0
+
+
+def _emission_law(tok, par, tl, T, D):
+    """Closed form of the target's own sampling: each emitted token ~ p_u at the node the
+    previous tokens lead to (the sequence stops at the first token that is not a child,
+    or after D + 1 tokens).  Returns {tuple(emitted): probability}."""
+    law = {}
+
+    def rec(u, prefix, prob, depth):
+        pu = _softmax(tl[u], T)
+        kids = {tok[c]: c for c in range(1, len(tok)) if par[c] == u}
+        for t, pt in enumerate(pu):
+            if t in kids and depth < D:
+                rec(kids[t], prefix + (t,), prob * pt, depth + 1)
+            else:
+                law[prefix + (t,)] = law.get(prefix + (t,), 0.0) + prob * pt
+    rec(0, (), 1.0, 0)
+    return law
+
+
+@pytest.mark.parametrize("T,shape", [(1.0, "tree"), (0.6, "tree"), (1.5, "chain"), (1.0, "depth_cut")])
+def test_walk_sample_is_lossless_monte_carlo(T, shape):
+    """Lossless: the emitted sequence is distributed exactly as sampling the target token
+    by token (each cell within 5 standard errors over 200k seeded walks).  A dropped
+    renormalisation by 1 - R, a bonus that keeps rejected tokens, or a wrong step index
+    into the uniforms moves some cell by far more."""
+    rng = _rng(77)
+    V = 6
+    if shape == "chain":
+        tok, par, D = [9, 2, 4, 1], [-1, 0, 1, 2], 3
+    else:
+        # root: children tokens 1, 3, 4; token 1's node: children 0, 2; token 0's node: child 5
+        tok, par, D = [9, 1, 3, 4, 0, 2, 5], [-1, 0, 0, 0, 1, 1, 4], 3
+        if shape == "depth_cut":
+            D = 2
+    N, C = len(tok), 3
+    tl = rng.normal(0, 0.5, size=(N, V))
+    # children tokens carry most of their parent's mass, so that rejections happen after
+    # earlier rejections (R well above 0) and the deeper levels are visited often
+    for u in range(N):
+        for c in range(1, N):
+            if par[c] == u:
+                tl[u, tok[c]] += 1.5
+    n = 200_000
+    U = rng.random((n, D + 1, C + 1))
+    o = oracle.walk_sample(np.tile(tok, (n, 1)), np.tile(par, (n, 1)), np.full(n, N), D,
+                           np.broadcast_to(tl, (n, N, V)), U, T, C)
+    assert (o["status"] == 0).all()
+    law = _emission_law(tok, par, tl, T, D)
+    counts = {}
+    for b in range(n):
+        key = tuple(o["emitted"][b][:o["n_emitted"][b]].tolist())
+        counts[key] = counts.get(key, 0) + 1
+    assert set(counts) <= set(law)
+    for key, prob in law.items():
+        f = counts.get(key, 0) / n
+        assert abs(f - prob) <= 5 * math.sqrt(prob * (1 - prob) / n) + 1e-6, (key, f, prob)
+    # accepted nodes are the emitted children: acc_len = n_emitted - 1 and the path's tokens
+    for b in range(0, n, 997):
+        a = o["acc_len"][b]
+        assert o["n_emitted"][b] == a + 1
+        assert [tok[r] for r in o["acc_nodes"][b][1:a + 1]] == o["emitted"][b][:a].tolist()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_walk_sample_cold_limit_is_greedy(seed):
+    """T -> 0: p_u becomes the point mass on the argmax (logit gaps of 0.1 at T = 1e-3 leave
+    at most V e^-100 elsewhere), so for uniforms below 0.99 the sampler takes exactly the
+    greedy walk: a child is accepted iff it is the argmax, and the bonus is the argmax."""
+    rng = _rng(900 + seed)
+    B, D, V, k = 3, 5, 40, 4
+    tree = oracle.build_tree(rng.normal(0, 2, size=(B, D, V)), [1, 2, 3], [0, 0, 0], k, 24)
+    N = tree["token"].shape[1]
+    tl = np.stack([[rng.permutation(V) * 0.1 for _ in range(N)] for _ in range(B)]).astype(np.float64)
+    for b in range(B):   # plant a path so the walk descends
+        cur = 0
+        for _ in range(int(rng.integers(1, D + 1))):
+            kids = [c for c in range(1, tree["n_nodes"][b]) if tree["parent"][b][c] == cur]
+            if not kids:
+                break
+            nxt = kids[int(rng.integers(len(kids)))]
+            tl[b, cur, tree["token"][b][nxt]] = tl[b, cur].max() + 0.1
+            cur = nxt
+    U = rng.uniform(0, 0.99, size=(B, D + 1, k + 1))
+    s = oracle.walk_sample(tree["token"], tree["parent"], tree["n_nodes"], D, tl, U, 1e-3, k)
+    g = oracle.walk(tree["token"], tree["parent"], tree["n_nodes"], D, target_logits=tl)
+    assert (s["status"] == 0).all() and (g["acc_len"] > 0).any()
+    for key in ("acc_nodes", "acc_len", "bonus", "emitted", "n_emitted"):
+        np.testing.assert_array_equal(s[key], g[key])
+
+
 # =========================================================================== commit
 def test_commit_kv_gdn_conv():
     rng = _rng(16)
