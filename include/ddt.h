@@ -9,6 +9,8 @@
  *   ddt_tree_attn    tree attention: prefix KV + own ancestors, never siblings
  *   ddt_tree_gdn     branch-local gated delta rule + short conv, scratch-only state
  *   ddt_walk_accept  greedy tree walk against the target's argmax
+ *                    (ddt_walk_accept_sample: the same walk at a temperature, by
+ *                    rejection sampling over each node's children)
  *   ddt_commit       copy only the accepted path's KV / recurrent state
  *
  * Sources (web pages; no code is printed on them):
@@ -332,6 +334,46 @@ ddt_status ddt_walk_accept_flat(int B, int N, int V, int max_accept, ddt_dtype d
                                 int32_t* bonus, int32_t* emitted, int32_t* n_emitted,
                                 int32_t* status, void* workspace, size_t ws_bytes,
                                 ddt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * ddt_walk_accept_sample -- tree-walk rejection sampling at a temperature.
+ * ["The Moment of Truth: Validating DDTree Speculative Decoding on Qwen3.6-27B",
+ * "The Path to This Message": the serving stack samples with a linear-chain rejection
+ * sampler; a tree needs a walk of its own.  The pages give no algorithm: the rule here
+ * is speculative sampling's (Leviathan et al. and Chen et al., 2023) over each visited
+ * node's children, whose draft is a point mass (SpecInfer, Miao et al., 2024).]
+ *
+ * At the visited node u (step s = depth of u, root first), p_u = softmax(logits[u] / T).
+ * u's children are tried in row order (rank order for ddt_build_tree's trees); with R
+ * the p_u-mass of the children already rejected, child i (counted from 0, token x_i) is
+ * accepted iff U[b][s][i] < p_u(x_i) / (1 - R); a rejected child adds p_u(x_i) to R.  An
+ * accepted child is the next node.  When every child is rejected (or u has none, or the
+ * walk has taken max_accept steps), the bonus token is the smallest id, rejected
+ * children skipped, whose running sum of p_u in id order exceeds U[b][s][C] * (1 - R).
+ * Every emitted token is then distributed as the target's own p at its position.
+ *   target_logits [B][N][V] (dtype); uniforms [B][A][C + 1] fp32 in [0, 1), C =
+ *     max_children (the caller's random numbers: the same uniforms give the same walk).
+ *   temperature T > 0 with 1/T finite in fp32 (else DDT_ERR_INVALID_ARG).
+ *   token, parent, n_nodes as written by ddt_build_tree.
+ * Outputs as ddt_walk_accept (acc_nodes, acc_len, bonus, emitted, n_emitted, status);
+ * status [B]: DDT_ERR_TREE for a malformed tree, a node with more than C children, a
+ * token repeated among one node's children or a token outside [0, V); DDT_ERR_NONFINITE
+ * for a NaN or +-inf logit in any row of the tree; the walk is then empty (acc_len 0,
+ * bonus -1, n_emitted 0).
+ * Precision: the per-row normaliser is formed from fp32 terms exp((l - m) * (1/T)) summed
+ * in fp64 across threads; each comparison of a probability with a uniform is in fp64.
+ * A decision whose margin is below about 1e-6 may therefore differ from an exact one.
+ * Limits: 1 <= C <= 32, max_accept <= 64, N <= 1024, B <= 65535.
+ * workspace: ddt_walk_accept_sample_workspace(B, N, V) bytes, 16-byte aligned.
+ * ------------------------------------------------------------------------------- */
+size_t ddt_walk_accept_sample_workspace(int B, int N, int V);
+ddt_status ddt_walk_accept_sample(int B, int N, int V, int max_accept, int max_children,
+                                  float temperature, ddt_dtype dtype, const void* target_logits,
+                                  const float* uniforms, const int32_t* token,
+                                  const int32_t* parent, const int32_t* n_nodes,
+                                  int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus,
+                                  int32_t* emitted, int32_t* n_emitted, int32_t* status,
+                                  void* workspace, size_t ws_bytes, ddt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * ddt_commit -- [NOTES] "Why hybrid attention makes it hard": once a path is accepted,

@@ -47,6 +47,16 @@ int main(void) {
                         p, p, p, NULL, p, p, 256, stream) == DDT_ERR_UNSUPPORTED);
     EXPECT(ddt_walk_accept(0, 5, 10, 4, DDT_BF16, p, p, p, p, p, p, p, p, p, p, p, p, 256, stream)
            == DDT_ERR_INVALID_ARG);
+    EXPECT(ddt_walk_accept_sample_workspace(0, 65, 151936) == 0);
+    EXPECT(ddt_walk_accept_sample_workspace(32, 65, 151936) == 332800);  /* 32*65*10 partials of 16 B */
+    EXPECT(ddt_walk_accept_sample(1, 5, 10, 4, 2, 0.0f, DDT_BF16, p, (const float*)p, p, p, p, p, p, p, p, p, p,
+                                  p, 1 << 20, stream) == DDT_ERR_INVALID_ARG);
+    EXPECT(ddt_walk_accept_sample(1, 5, 10, 4, 2, 1e-40f, DDT_BF16, p, (const float*)p, p, p, p, p, p, p, p, p,
+                                  p, p, 1 << 20, stream) == DDT_ERR_INVALID_ARG);
+    EXPECT(ddt_walk_accept_sample(1, 5, 10, 4, 33, 1.0f, DDT_BF16, p, (const float*)p, p, p, p, p, p, p, p, p,
+                                  p, p, 1 << 20, stream) == DDT_ERR_UNSUPPORTED);
+    EXPECT(ddt_walk_accept_sample(1, 5, 10, 4, 2, 1.0f, DDT_BF16, p, NULL, p, p, p, p, p, p, p, p, p, p,
+                                  1 << 20, stream) == DDT_ERR_INVALID_ARG);
     EXPECT(ddt_commit(1, 5, 0, 0, 1, 64, 10, DDT_BF16, p, p, p, p, 0, 1, 1, 32, 32, 4, DDT_BF16, p, p,
                       (float*)p, (float*)p, (float*)p, p, p, p, p, p, p, p, stream) == DDT_ERR_INVALID_ARG);
     /* more accepted rows than any tree can have: refused before the KV part runs */

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 
 #include "ddt.h"
 #include "kernels.h"
@@ -306,6 +307,31 @@ ddt_status ddt_walk_accept_flat(int B, int N, int V, int max_accept, ddt_dtype d
                                 size_t ws_bytes, ddt_stream_t stream) {
     return walk_accept(B, N, V, max_accept, dtype, target_logits, target_argmax, token, parent, n_nodes, acc_nodes,
                        acc_len, bonus, emitted, n_emitted, status, workspace, ws_bytes, 1, stream);
+}
+
+size_t ddt_walk_accept_sample_workspace(int B, int N, int V) {
+    if (B < 1 || N < 1 || V < 1) return 0;
+    return walk_sample_ws_bytes(B, N, V);
+}
+
+ddt_status ddt_walk_accept_sample(int B, int N, int V, int max_accept, int max_children, float temperature,
+                                  ddt_dtype dtype, const void* target_logits, const float* uniforms,
+                                  const int32_t* token, const int32_t* parent, const int32_t* n_nodes,
+                                  int32_t* acc_nodes, int32_t* acc_len, int32_t* bonus, int32_t* emitted,
+                                  int32_t* n_emitted, int32_t* status, void* workspace, size_t ws_bytes,
+                                  ddt_stream_t stream) {
+    if (B < 1 || N < 1 || V < 1 || max_accept < 0 || max_children < 1 || !dtype_ok(dtype)) return DDT_ERR_INVALID_ARG;
+    // T > 0 with a finite fp32 reciprocal (the kernels scale by 1/T)
+    if (!(temperature > 0.0f) || !(1.0f / temperature < INFINITY) || !(temperature < INFINITY))
+        return DDT_ERR_INVALID_ARG;
+    if (N > kMaxRows || B > 65535 || max_accept > kMaxAccept || max_children > kMaxTopK) return DDT_ERR_UNSUPPORTED;
+    if (!target_logits || !uniforms || !token || !parent || !n_nodes || !acc_nodes || !acc_len || !bonus ||
+        !emitted || !n_emitted || !status)
+        return DDT_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < walk_sample_ws_bytes(B, N, V) || !aligned16(workspace)) return DDT_ERR_INVALID_ARG;
+    return from_cuda(launch_walk_sample(B, N, V, max_accept + 1, max_children, temperature, dtype, target_logits,
+                                        uniforms, token, parent, n_nodes, acc_nodes, acc_len, bonus, emitted,
+                                        n_emitted, status, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------------------- commit

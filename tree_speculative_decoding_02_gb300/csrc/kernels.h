@@ -34,6 +34,12 @@ cudaError_t launch_build_tree(int B, int D, int V, int k, int budget, ddt_dtype 
                               int32_t* parent, int32_t* depth, int32_t* position, int32_t* n_nodes,
                               uint32_t* anc, double* score, int32_t* status, void* ws, cudaStream_t st);
 
+size_t walk_sample_ws_bytes(int B, int N, int V);
+cudaError_t launch_walk_sample(int B, int N, int V, int A, int C, float temperature, ddt_dtype dtype,
+                               const void* logits, const float* uniforms, const int32_t* token,
+                               const int32_t* parent, const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len,
+                               int32_t* bonus, int32_t* emitted, int32_t* n_emitted, int32_t* status, void* ws,
+                               cudaStream_t st);
 size_t walk_ws_bytes(int B, int N, int V);
 cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void* logits, int32_t* targ,
                         const int32_t* token, const int32_t* parent, const int32_t* n_nodes, int32_t* acc_nodes,

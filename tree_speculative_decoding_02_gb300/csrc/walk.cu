@@ -114,9 +114,12 @@ __global__ void __launch_bounds__(256) k_walk_descend(int N, int V, int A, int n
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nn = n_nodes[b];
     const long ob = (long)b * N;
-    if (tid == 0) s_err = (nn < 1 || nn > N) ? DDT_ERR_TREE : DDT_OK;
+    // decided on each thread's own copy of n_nodes: the checks below write s_err, and a
+    // thread that read it late would leave while the others go on to the barriers
+    const bool nn_ok = nn >= 1 && nn <= N;
+    if (tid == 0) s_err = nn_ok ? DDT_OK : DDT_ERR_TREE;
     __syncthreads();
-    if (s_err != DDT_OK) {
+    if (!nn_ok) {
         for (int j = tid; j < A; j += blockDim.x) {
             acc_nodes[(long)b * A + j] = -1;
             emitted[(long)b * A + j] = -1;

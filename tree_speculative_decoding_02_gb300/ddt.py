@@ -43,6 +43,8 @@ _SIGS = {
     "ddt_walk_accept_workspace": ([_c_int] * 3, _c_size),
     "ddt_walk_accept": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_walk_accept_flat": ([_c_int] * 5 + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
+    "ddt_walk_accept_sample_workspace": ([_c_int] * 3, _c_size),
+    "ddt_walk_accept_sample": ([_c_int] * 5 + [_c_float, _c_int] + [_c_p] * 11 + [_c_p, _c_size, _c_p], _c_int),
     "ddt_tree_attn_paged_workspace": ([_c_int] * 8, _c_size),
     "ddt_tree_attn_paged": ([_c_int] * 11 + [_c_p] * 9 + [_c_float, _c_p, _c_p, _c_p, _c_size, _c_p], _c_int),
     "ddt_commit_paged": ([_c_int] * 9 + [_c_p] + [_c_int] + [_c_p] * 4 + [_c_int] * 6 + [_c_int] + [_c_p] * 13,
@@ -425,6 +427,40 @@ def ddt_walk_accept(token, parent, n_nodes, max_accept: int, *, target_logits=No
             _ptr(res["bonus"]), _ptr(res["emitted"]), _ptr(res["n_emitted"]), _ptr(res["status"]),
             _ptr(ws), ws.numel(), _stream())
     _check(rc, "ddt_walk_accept_flat" if flat else "ddt_walk_accept")
+    return res
+
+
+def ddt_walk_accept_sample(token, parent, n_nodes, max_accept: int, *, target_logits, uniforms, temperature: float,
+                           out=None, workspace=None):
+    """Tree-walk rejection sampling at `temperature`.  uniforms [B][max_accept + 1][C + 1]
+    fp32 in [0, 1); C (the most children a node may have) is read from its last dimension."""
+    lib = _gpu()
+    B, N = token.shape
+    dev = token.device
+    _need(token, (B, N), torch.int32, "token")
+    _need(parent, (B, N), torch.int32, "parent")
+    _need(n_nodes, (B,), torch.int32, "n_nodes")
+    A = max_accept + 1
+    V = target_logits.shape[2]
+    _need(target_logits, (B, N, V), None, "target_logits")
+    C = uniforms.shape[-1] - 1
+    _need(uniforms, (B, A, C + 1), torch.float32, "uniforms")
+    o = out or {}
+    i32 = dict(dtype=torch.int32, device=dev)
+    res = {"acc_nodes": o.get("acc_nodes", torch.empty((B, A), **i32)),
+           "acc_len": o.get("acc_len", torch.empty((B,), **i32)),
+           "bonus": o.get("bonus", torch.empty((B,), **i32)),
+           "emitted": o.get("emitted", torch.empty((B, A), **i32)),
+           "n_emitted": o.get("n_emitted", torch.empty((B,), **i32)),
+           "status": o.get("status", torch.empty((B,), **i32))}
+    need = lib.ddt_walk_accept_sample_workspace(B, N, V)
+    ws = workspace if workspace is not None else _ws(need, dev)
+    rc = lib.ddt_walk_accept_sample(B, N, V, int(max_accept), int(C), float(temperature), _DT[target_logits.dtype],
+                                    _ptr(target_logits), _ptr(uniforms), _ptr(token), _ptr(parent), _ptr(n_nodes),
+                                    _ptr(res["acc_nodes"]), _ptr(res["acc_len"]), _ptr(res["bonus"]),
+                                    _ptr(res["emitted"]), _ptr(res["n_emitted"]), _ptr(res["status"]), _ptr(ws),
+                                    ws.numel(), _stream())
+    _check(rc, "ddt_walk_accept_sample")
     return res
 
 

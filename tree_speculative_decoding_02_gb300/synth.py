@@ -83,6 +83,21 @@ def plant_path(target, token, parent, n_nodes, path_len, *, boost=8.0):
     return paths
 
 
+def add_peaks(target, n_peaks, height, *, g):
+    """Raise `n_peaks` seeded tokens of every row by height, height - 1, ...: a peaked
+    target in which a few tokens hold much of each row's mass (in place, fp32)."""
+    B, N, V = target.shape
+    idx = torch.randint(0, V, (B, N, n_peaks), generator=g)
+    bump = float(height) - torch.arange(n_peaks, dtype=torch.float32)
+    target.scatter_add_(2, idx, bump.expand(B, N, n_peaks).contiguous())
+    return target
+
+
+def uniforms(B, A, C, *, g, device="cpu"):
+    """[B][A][C + 1] fp32 uniforms in [0, 1): the random numbers of a sampling walk."""
+    return torch.rand((B, A, C + 1), generator=g, dtype=torch.float32, device=device)
+
+
 def prefix_lengths(B, lo, hi, *, g):
     """Committed prefix lengths ~ U{lo..hi}."""
     return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int32)
