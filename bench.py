@@ -283,8 +283,7 @@ def make_step(r, flat, ev):
             kw.update(x=g.x, conv_w=g.conv_w, beta=g.beta, decay=g.decay, S=g.S, conv_state=g.conv_state,
                       Hk=c["Hk"])
             mark("gdn")
-        ddt.ddt_walk_accept(r.tree["token"], r.tree["parent"], r.tree["n_nodes"], r.A - 1,
-                            target_logits=r.target_logits, out=r.walk, workspace=r.walk_ws, flat=flat)
+        r.walk_step()     # greedy, flat, or rejection sampling at the round's temperature
         mark("walk")
         if r.Lf and r.page:
             ddt.ddt_commit_paged(r.walk["acc_nodes"], r.walk["acc_len"], r.prefix_len, r.block_table,
@@ -369,6 +368,10 @@ def run_ours(args, rank, world, local):
     if args.rope and cfg.get("Lf"):
         cfg["rope"] = cfg["d"]
     cfg["flat"] = args.flat
+    if args.batch:
+        cfg["B"] = args.batch
+    if args.temperature > 0:
+        cfg["temperature"] = args.temperature
     r = Round(cfg, device=dev, workload=args.workload)
     st = torch.cuda.current_stream()
 
@@ -439,15 +442,19 @@ def run_ours(args, rank, world, local):
     if args.planted:
         out["config"]["acceptance"] = (f"planted paths, geometric lengths of mean {args.planted}; "
                                        f"mean accepted drafted nodes {accepted:.2f}")
+    if args.temperature > 0:
+        out["config"]["walk"] = (f"tree-walk rejection sampling at temperature {args.temperature} "
+                                 "(ddt_walk_accept_sample, seeded uniforms)")
     if args.kv_page:
         out["config"]["kv"] = f"paged: {args.kv_page} rows a page, shuffled block table"
     if args.rope:
         out["config"]["rope"] = ("rotary embedding by depth: tree keys rotated in place, q rotated inside the "
                                  "fused attention call (inputs taken before rotation)")
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg and not (args.kv_page or args.rope):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and r.Lf and r.Lg and not (
+            args.kv_page or args.rope or args.temperature or args.batch):
         out["cpu_baseline"] = cpu_baseline(r, seconds=args.cpu_seconds)
     if rank == 0 and world == 1 and args.per_config and args.workload == WORKLOAD and not (
-            args.kv_page or args.flat or args.planted or args.rope):
+            args.kv_page or args.flat or args.planted or args.rope or args.temperature or args.batch):
         del r
         torch.cuda.empty_cache()
         out["per_config"] = [config_line(w, dev, peaks, tc_peak, tc_kind, not args.no_cpu_baseline)
@@ -797,6 +804,10 @@ def main():
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
                     help="skip the per-workload lines of the smaller configurations")
     ap.add_argument("--flat", action="store_true", help="flat-commit safe mode: walk first children only")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="> 0: run the workload with this many requests instead of its own B")
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="> 0: verify by tree-walk rejection sampling at this temperature")
     ap.add_argument("--planted", type=float, default=0.0,
                     help="plant accepted paths with this mean length (0: random targets, little accepted)")
     ap.add_argument("--rope", action="store_true",

@@ -360,9 +360,11 @@ ddt_status ddt_walk_accept_flat(int B, int N, int V, int max_accept, ddt_dtype d
  * token repeated among one node's children or a token outside [0, V); DDT_ERR_NONFINITE
  * for a NaN or +-inf logit in any row of the tree; the walk is then empty (acc_len 0,
  * bonus -1, n_emitted 0).
- * Precision: the per-row normaliser is formed from fp32 terms exp((l - m) * (1/T)) summed
- * in fp64 across threads; each comparison of a probability with a uniform is in fp64.
- * A decision whose margin is below about 1e-6 may therefore differ from an exact one.
+ * Precision: each term exp((l - m) / T) is taken in fp32 as 2^((l - m) * s2), s2 =
+ * log2(e) / T rounded to fp32; the per-row normaliser sums them in fp32 within each
+ * 2048-entry unit and in fp64 across units; each comparison of a probability with a
+ * uniform is in fp64.  A decision whose margin is below about 2e-6 may therefore differ
+ * from an exact one.
  * Limits: 1 <= C <= 32, max_accept <= 64, N <= 1024, B <= 65535.
  * workspace: ddt_walk_accept_sample_workspace(B, N, V) bytes, 16-byte aligned.
  * ------------------------------------------------------------------------------- */

@@ -11,123 +11,144 @@
 //   is, the bonus is the smallest id whose running sum of p_u (rejected ids skipped)
 //   exceeds U[step][C] * (1 - R).
 //
-//   k_walk_lse     grid (chunks, N, B): one HBM pass over the target logits; each CTA
-//                  reduces a 16384-token chunk of one row to its max m_c and
-//                  sum_v exp((l_v - m_c) / T) (fp32 terms in groups of 8, fp64 across
-//                  threads).
-//   k_walk_sample  grid B: tree checks; warp 0 walks down, merging the visited row's
-//                  chunk partials and deciding each tried child in fp64; then the CTA
-//                  draws the bonus: a warp scan of the residual chunk masses picks the
-//                  chunk, a block scan over that chunk's 16384 terms picks the token.
+//   k_walk_lse     grid (units / 8, N, B): one HBM pass over the target logits; each warp
+//                  reduces a 2048-token unit of one row to its max m_u and
+//                  sum_v 2^((l_v - m_u) * s2), s2 = log2(e) / T (fp32: groups of 8 terms,
+//                  pairwise above them, a shuffle tree across the warp).  No block barrier
+//                  and no fp64, so loads of the next warp's unit overlap this one's math.
+//   k_walk_sample  grid B: tree checks; warp 0 walks down, merging the visited row's unit
+//                  partials in fp64 and deciding each tried child in fp64; then the CTA
+//                  draws the bonus: a warp scan of the residual unit masses picks the unit,
+//                  a block scan over that unit's 2048 terms picks the token.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace ddt {
 
-constexpr int kSampleChunk = 16384;                         // vocabulary entries a k_walk_lse CTA reduces
+constexpr int kSampleUnit = 2048;                         // vocabulary entries one warp reduces
 constexpr int kSampleThreads = 256;
-constexpr int kSamplePer = kSampleChunk / kSampleThreads;  // 64 entries a thread
+constexpr int kUnitsPerCta = kSampleThreads / 32;
+constexpr int kLanePer = kSampleUnit / 32;                // 64 entries a lane
+constexpr int kScanPer = kSampleUnit / kSampleThreads;    // 8 entries a thread in the bonus scan
 
+// One unit's partial: m = the largest raw logit, s = sum of 2^((l - m) * s2) over the
+// unit; s = -1 flags a NaN or +-inf logit in it; an empty unit has m = -inf, s = 0.
 struct LsePartial {
-    float m;        // largest raw logit of the chunk
-    int nonfinite;  // a NaN or +-inf logit in the chunk
-    double s;       // sum over the chunk of exp((l - m) * inv_t)
+    float m;
+    float s;
 };
 
+static inline int units_of(int V) { return (V + kSampleUnit - 1) / kSampleUnit; }
+
 size_t walk_sample_ws_bytes(int B, int N, int V) {
-    const long nch = (V + kSampleChunk - 1) / kSampleChunk;
-    return (((size_t)B * N * nch * sizeof(LsePartial)) + 255) & ~(size_t)255;
+    return (((size_t)B * N * units_of(V) * sizeof(LsePartial)) + 255) & ~(size_t)255;
 }
 
-// One tempered term: exp((l - m) / T) with the division taken as a product by the fp32
-// reciprocal inv_t.  -inf (an entry past the row's end) gives 0.
-__device__ __forceinline__ float tempered(float l, float m, float inv_t) { return expf((l - m) * inv_t); }
+// One tempered term: exp((l - m) / T) = 2^((l - m) * s2) with s2 = log2(e) / T rounded to
+// fp32.  -inf (an entry past the row's end, or the empty max) gives 0.
+__device__ __forceinline__ float tempered(float l, float m, float s2) { return exp2f((l - m) * s2); }
 
+// Eight consecutive entries kept in their storage format until used (bf16: one 16-byte
+// word, so a lane holds its 64 entries in 32 registers); entries at or past `len` read
+// as -inf.
 template <typename T>
-__global__ void __launch_bounds__(kSampleThreads) k_walk_lse(const T* __restrict__ logits, int N, int V, int nch,
-                                                             int vec, float inv_t,
-                                                             const int32_t* __restrict__ n_nodes,
-                                                             LsePartial* __restrict__ part) {
-    const int c = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
-    const int nn = n_nodes[b];
-    if (i >= nn || nn > N) return;  // rows past the tree are not needed
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const T* row = logits + ((long)b * N + i) * V + (long)c * kSampleChunk;
-    const int len = min(kSampleChunk, V - c * kSampleChunk);
-    float x[kSamplePer];
-    float mx = -INFINITY;
-    int bad = 0;
-#pragma unroll
-    for (int j = 0; j < kSamplePer / 8; ++j) {
-        const int e = tid * 8 + j * (kSampleThreads * 8);
-        float t8[8];
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 w;
+    __device__ __forceinline__ void load(const __nv_bfloat16* __restrict__ p, int e, int len, int vec) {
         if (vec && e + 8 <= len) {
-            load8_stream(row + e, t8);
+            w = ld_stream_u4(p + e);
+        } else {
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) h[q] = (e + q < len) ? (uint32_t)__bfloat16_as_ushort(p[e + q]) : 0xff80u;
+            w = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+        }
+    }
+    __device__ __forceinline__ float at(int q) const {
+        const uint32_t v = q < 2 ? w.x : (q < 4 ? w.y : (q < 6 ? w.z : w.w));
+        return __uint_as_float((q & 1) ? (v & 0xffff0000u) : (v << 16));
+    }
+};
+template <>
+struct Raw8<float> {
+    float v[8];
+    __device__ __forceinline__ void load(const float* __restrict__ p, int e, int len, int vec) {
+        if (vec && e + 8 <= len) {
+            load8_stream(p + e, v);
         } else {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) t8[u] = (e + u < len) ? to_f32(row[e + u]) : -INFINITY;
+            for (int q = 0; q < 8; ++q) v[q] = (e + q < len) ? p[e + q] : -INFINITY;
         }
+    }
+    __device__ __forceinline__ float at(int q) const { return v[q]; }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kSampleThreads) k_walk_lse(const T* __restrict__ logits, int N, int V, int nunits,
+                                                             int vec, float s2, const int32_t* __restrict__ n_nodes,
+                                                             LsePartial* __restrict__ part) {
+    const int i = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x & 31;
+    const int u = blockIdx.x * kUnitsPerCta + (threadIdx.x >> 5);
+    const int nn = n_nodes[b];
+    if (i >= nn || nn > N || u >= nunits) return;  // rows past the tree are not needed
+    const T* row = logits + ((long)b * N + i) * V + (long)u * kSampleUnit;
+    const int len = min(kSampleUnit, V - u * kSampleUnit);
+    Raw8<T> r[kLanePer / 8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            x[j * 8 + u] = t8[u];
-            if (e + u < len) {
-                if (!finite_f32(t8[u])) bad = 1;
-                mx = fmaxf(mx, t8[u]);
+    for (int j = 0; j < kLanePer / 8; ++j) r[j].load(row, lane * 8 + j * 256, len, vec);
+    float mt = -INFINITY;
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < kLanePer / 8; ++j)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float x = r[j].at(q);
+            if (lane * 8 + j * 256 + q < len) {
+                if (!finite_f32(x)) bad = 1;
+                mt = fmaxf(mt, x);
             }
         }
-    }
+    float g[kLanePer / 8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-    bad = __any_sync(kFull, bad);
-    __shared__ float s_mx[kSampleThreads / 32];
-    __shared__ int s_bad[kSampleThreads / 32];
-    __shared__ double s_sum[kSampleThreads / 32];
-    if (lane == 0) {
-        s_mx[warp] = mx;
-        s_bad[warp] = bad;
-    }
-    __syncthreads();
-    float m = s_mx[0];
-#pragma unroll
-    for (int w = 1; w < kSampleThreads / 32; ++w) m = fmaxf(m, s_mx[w]);
-    float g[kSamplePer / 8];
-#pragma unroll
-    for (int j = 0; j < kSamplePer / 8; ++j) {
+    for (int j = 0; j < kLanePer / 8; ++j) {
         float acc = 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc += tempered(x[j * 8 + u], m, inv_t);
+        for (int q = 0; q < 8; ++q) acc += tempered(r[j].at(q), mt, s2);
         g[j] = acc;
     }
-    double ds = (double)(((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7])));
+    float st = mt == -INFINITY ? 0.f : ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
+    float mw = mt;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ds += __shfl_down_sync(kFull, ds, o);
-    if (lane == 0) s_sum[warp] = ds;
-    __syncthreads();
-    if (tid == 0) {
-        double s = 0.0;
-        int anybad = 0;
-        for (int w = 0; w < kSampleThreads / 32; ++w) {
-            s += s_sum[w];
-            anybad |= s_bad[w];
-        }
+    for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(kFull, mw, o));
+    if (mt != -INFINITY) st *= tempered(mt, mw, s2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) st += __shfl_down_sync(kFull, st, o);
+    bad = __any_sync(kFull, bad);
+    if (lane == 0) {
         LsePartial pp;
-        pp.m = m;
-        pp.nonfinite = anybad;
-        pp.s = s;
-        part[((long)b * N + i) * nch + c] = pp;
+        pp.m = mw;
+        pp.s = bad ? -1.f : st;
+        part[((long)b * N + i) * nunits + u] = pp;
     }
 }
 
-// Warp-wide: the row's max and Z = sum_v exp((l_v - m) / T) from its chunk partials.  Every
-// lane returns lane 0's values, so decisions taken on them are uniform across the warp.
-__device__ __forceinline__ void row_stats(const LsePartial* __restrict__ P, int nch, float inv_t, int lane, float& m,
+// Warp-wide: the row's max and Z = sum_v exp((l_v - m) / T) from its unit partials, the
+// sum in fp64.  Every lane returns lane 0's values, so decisions taken on them are
+// uniform across the warp.
+__device__ __forceinline__ void row_stats(const LsePartial* __restrict__ P, int nunits, float s2, int lane, float& m,
                                           double& z) {
     float mm = -INFINITY;
-    for (int c = lane; c < nch; c += 32) mm = fmaxf(mm, P[c].m);
+    for (int c = lane; c < nunits; c += 32) mm = fmaxf(mm, P[c].m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, o));
     double zz = 0.0;
-    for (int c = lane; c < nch; c += 32) zz += P[c].s * (double)tempered(P[c].m, mm, inv_t);
+    for (int c = lane; c < nunits; c += 32) {
+        const LsePartial pp = P[c];
+        if (pp.s > 0.f) zz += (double)pp.s * (double)tempered(pp.m, mm, s2);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) zz += __shfl_down_sync(kFull, zz, o);
     m = mm;
@@ -136,7 +157,7 @@ __device__ __forceinline__ void row_stats(const LsePartial* __restrict__ P, int 
 
 template <typename T>
 __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
-    const T* __restrict__ logits, int N, int V, int A, int C, int nch, int vec, float inv_t,
+    const T* __restrict__ logits, int N, int V, int A, int C, int nunits, int vec, float s2,
     const LsePartial* __restrict__ part, const float* __restrict__ uniforms, const int32_t* __restrict__ token,
     const int32_t* __restrict__ parent, const int32_t* __restrict__ n_nodes, int32_t* __restrict__ acc_nodes,
     int32_t* __restrict__ acc_len, int32_t* __restrict__ bonus, int32_t* __restrict__ emitted,
@@ -145,7 +166,7 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
     __shared__ float s_lc[kMaxRows];  // logit of node i's token in its parent's row
     __shared__ double s_incl[kSampleThreads];
     __shared__ double s_wsum[kSampleThreads / 32];
-    __shared__ uint32_t s_rejbits[kSampleChunk / 32];
+    __shared__ uint32_t s_rejbits[kSampleUnit / 32];
     __shared__ int s_rejtok[kMaxTopK];
     __shared__ float s_rejterm[kMaxTopK];
     __shared__ int s_path[kMaxAccept + 1];
@@ -187,8 +208,8 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
                     break;
                 }
         }
-        for (int j = tid; j < nn * nch; j += kSampleThreads)
-            if (part[ob * nch + j].nonfinite) atomicMax(&s_err, DDT_ERR_NONFINITE);  // a tree error outranks it
+        for (int j = tid; j < nn * nunits; j += kSampleThreads)
+            if (part[ob * nunits + j].s < 0.f) atomicMax(&s_err, DDT_ERR_NONFINITE);  // a tree error outranks it
         __syncthreads();
         for (int i = tid; i < nn; i += kSampleThreads)
             if (s_cnt[i] > C) atomicMax(&s_err, DDT_ERR_TREE);
@@ -215,7 +236,7 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
         double zr = 0.0;
         if (lane == 0) s_path[0] = 0;
         for (;;) {
-            row_stats(part + (ob + cur) * nch, nch, inv_t, lane, m, zr);
+            row_stats(part + (ob + cur) * nunits, nunits, s2, lane, m, zr);
             const float* U = uniforms + ((long)b * A + a) * (C + 1);
             nrej = 0;
             int next = -1;
@@ -226,7 +247,7 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
                     while (mask != 0u && next < 0) {
                         const int cc = base + __ffs(mask) - 1;
                         mask &= mask - 1u;
-                        const float term = tempered(s_lc[cc], m, inv_t);
+                        const float term = tempered(s_lc[cc], m, s2);
                         // p(x) / (1 - R) with both taken relative to Z: term / (Z - rejected terms)
                         if ((double)U[nrej] < (double)term / zr) {
                             next = cc;
@@ -258,22 +279,23 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
     }
     __syncthreads();
 
-    // ---- the bonus chunk (warp 0): residual chunk masses in id order, inclusive scan
+    // ---- the bonus unit (warp 0): residual unit masses in id order, inclusive scan
     const int cur = s_cur, nrej = s_nrej;
     const float m = s_m;
     if (warp == 0) {
-        const LsePartial* P = part + (ob + cur) * nch;
+        const LsePartial* P = part + (ob + cur) * nunits;
         const double target = s_local;
         double carry = 0.0;
         int pick = -1, last = -1;
         double before = 0.0;
-        for (int base = 0; base < nch; base += 32) {
+        for (int base = 0; base < nunits; base += 32) {
             const int c = base + lane;
             double mc = 0.0;
-            if (c < nch) {
-                mc = P[c].s * (double)tempered(P[c].m, m, inv_t);
+            if (c < nunits) {
+                const LsePartial pp = P[c];
+                mc = (double)pp.s * (double)tempered(pp.m, m, s2);
                 for (int r = 0; r < nrej; ++r)
-                    if (s_rejtok[r] / kSampleChunk == c) mc -= (double)s_rejterm[r];
+                    if (s_rejtok[r] / kSampleUnit == c) mc -= (double)s_rejterm[r];
             }
             double incl = mc;
 #pragma unroll
@@ -282,8 +304,8 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
                 if (lane >= o) incl += y;
             }
             incl += carry;
-            const unsigned over = __ballot_sync(kFull, c < nch && incl > target);
-            const unsigned pos = __ballot_sync(kFull, c < nch && mc > 0.0);
+            const unsigned over = __ballot_sync(kFull, c < nunits && incl > target);
+            const unsigned pos = __ballot_sync(kFull, c < nunits && mc > 0.0);
             if (pick < 0 && over != 0u) {
                 const int l = __ffs(over) - 1;
                 pick = base + l;
@@ -293,7 +315,7 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
             carry = __shfl_sync(kFull, incl, 31);
         }
         if (lane == 0) {
-            // rounding left the target past the residual mass: the last chunk that has some,
+            // rounding left the target past the residual mass: the last unit that has some,
             // and in it the largest id with a positive term (an infinite local target)
             s_chunk = (pick >= 0) ? pick : last;
             s_local = (pick >= 0) ? target - before : INFINITY;
@@ -301,43 +323,38 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
             s_last = -1;
         }
     }
-    for (int j = tid; j < kSampleChunk / 32; j += kSampleThreads) s_rejbits[j] = 0u;
+    for (int j = tid; j < kSampleUnit / 32; j += kSampleThreads) s_rejbits[j] = 0u;
     __syncthreads();
-    const int chunk = s_chunk;
-    if (chunk >= 0) {
-        const int start = chunk * kSampleChunk;
+    const int unit = s_chunk;
+    if (unit >= 0) {
+        const int start = unit * kSampleUnit;
         if (tid < nrej) {
             const int t = s_rejtok[tid] - start;
-            if (t >= 0 && t < kSampleChunk) atomicOr(&s_rejbits[t >> 5], 1u << (t & 31));
+            if (t >= 0 && t < kSampleUnit) atomicOr(&s_rejbits[t >> 5], 1u << (t & 31));
         }
         __syncthreads();
-        // ---- the bonus token: block scan of this chunk's residual terms in id order
-        const int len = min(kSampleChunk, V - start);
+        // ---- the bonus token: block scan of this unit's residual terms in id order
+        const int len = min(kSampleUnit, V - start);
         const T* row = logits + (ob + cur) * V + start;
-        const int e0 = tid * kSamplePer;
-        float g[kSamplePer / 8];
-        int lastpos = -1;
+        const int e0 = tid * kScanPer;
+        float t8[kScanPer];
+        if (vec && e0 + kScanPer <= len) {
+            load8(row + e0, t8);
+        } else {
 #pragma unroll
-        for (int j = 0; j < kSamplePer / 8; ++j) {
-            const int e = e0 + j * 8;
-            float t8[8];
-            if (vec && e + 8 <= len) {
-                load8(row + e, t8);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) t8[u] = (e + u < len) ? to_f32(row[e + u]) : -INFINITY;
-            }
-            float acc = 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const bool rej = (s_rejbits[(e + u) >> 5] >> ((e + u) & 31)) & 1u;
-                const float tv = (e + u < len && !rej) ? tempered(t8[u], m, inv_t) : 0.f;
-                if (tv > 0.f) lastpos = e + u;
-                acc += tv;
-            }
-            g[j] = acc;
+            for (int q = 0; q < kScanPer; ++q) t8[q] = (e0 + q < len) ? to_f32(row[e0 + q]) : -INFINITY;
         }
-        double incl = (double)(((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7])));
+        const uint32_t rejw = (s_rejbits[e0 >> 5] >> (e0 & 31)) & 0xffu;  // 8 entries share a word
+        float tv[kScanPer];
+        int lastpos = -1;
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < kScanPer; ++q) {
+            tv[q] = (e0 + q < len && !((rejw >> q) & 1u)) ? tempered(t8[q], m, s2) : 0.f;
+            if (tv[q] > 0.f) lastpos = e0 + q;
+            acc += tv[q];
+        }
+        double incl = (double)acc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const double y = __shfl_up_sync(kFull, incl, o);
@@ -357,21 +374,12 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_sample(
             // the smallest thread whose inclusive sum passes the target walks its own ids
             double run = (tid == 0) ? 0.0 : s_incl[tid - 1];
             int pickid = (lastpos >= 0) ? lastpos : s_last;  // if rounding runs the scan dry
-            bool done = false;
-            for (int j = 0; j < kSamplePer / 8 && !done; ++j) {
-                if (run + (double)g[j] <= target) {
-                    run += (double)g[j];
-                    continue;
-                }
-                const int e = e0 + j * 8;
-                for (int u = 0; u < 8 && !done; ++u) {
-                    const bool rej = (s_rejbits[(e + u) >> 5] >> ((e + u) & 31)) & 1u;
-                    if (e + u >= len || rej) continue;
-                    run += (double)tempered(to_f32(row[e + u]), m, inv_t);
-                    if (run > target) {
-                        pickid = e + u;
-                        done = true;
-                    }
+            for (int q = 0; q < kScanPer; ++q) {
+                if (tv[q] <= 0.f) continue;
+                run += (double)tv[q];
+                if (run > target) {
+                    pickid = e0 + q;
+                    break;
                 }
             }
             s_bonus = (pickid >= 0) ? start + pickid : -1;
@@ -401,25 +409,25 @@ cudaError_t launch_walk_sample(int B, int N, int V, int A, int C, float temperat
                                const int32_t* parent, const int32_t* n_nodes, int32_t* acc_nodes, int32_t* acc_len,
                                int32_t* bonus, int32_t* emitted, int32_t* n_emitted, int32_t* status, void* ws,
                                cudaStream_t st) {
-    const int nch = (V + kSampleChunk - 1) / kSampleChunk;
-    const float inv_t = 1.0f / temperature;
+    const int nunits = units_of(V);
+    const float s2 = (float)(1.4426950408889634 / (double)temperature);  // log2(e) / T
     LsePartial* part = static_cast<LsePartial*>(ws);
     const int vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
-    dim3 g(nch, N, B);
+    dim3 g((nunits + kUnitsPerCta - 1) / kUnitsPerCta, N, B);
     if (dtype == DDT_BF16) {
         const __nv_bfloat16* l = static_cast<const __nv_bfloat16*>(logits);
-        k_walk_lse<__nv_bfloat16><<<counted(g), kSampleThreads, 0, st>>>(l, N, V, nch, vec, inv_t, n_nodes, part);
+        k_walk_lse<__nv_bfloat16><<<counted(g), kSampleThreads, 0, st>>>(l, N, V, nunits, vec, s2, n_nodes, part);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         k_walk_sample<__nv_bfloat16><<<counted(B), kSampleThreads, 0, st>>>(
-            l, N, V, A, C, nch, vec, inv_t, part, uniforms, token, parent, n_nodes, acc_nodes, acc_len, bonus,
+            l, N, V, A, C, nunits, vec, s2, part, uniforms, token, parent, n_nodes, acc_nodes, acc_len, bonus,
             emitted, n_emitted, status);
     } else {
         const float* l = static_cast<const float*>(logits);
-        k_walk_lse<float><<<counted(g), kSampleThreads, 0, st>>>(l, N, V, nch, vec, inv_t, n_nodes, part);
+        k_walk_lse<float><<<counted(g), kSampleThreads, 0, st>>>(l, N, V, nunits, vec, s2, n_nodes, part);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        k_walk_sample<float><<<counted(B), kSampleThreads, 0, st>>>(l, N, V, A, C, nch, vec, inv_t, part, uniforms,
+        k_walk_sample<float><<<counted(B), kSampleThreads, 0, st>>>(l, N, V, A, C, nunits, vec, s2, part, uniforms,
                                                                     token, parent, n_nodes, acc_nodes, acc_len,
                                                                     bonus, emitted, n_emitted, status);
     }

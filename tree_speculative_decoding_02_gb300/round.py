@@ -84,7 +84,13 @@ class Round:
                      "acc_len": torch.empty((B,), **i32), "bonus": torch.empty((B,), **i32),
                      "emitted": torch.empty((B, self.A), **i32), "n_emitted": torch.empty((B,), **i32),
                      "status": torch.empty((B,), **i32)}
-        self.walk_ws = torch.empty(max(16, lib.ddt_walk_accept_workspace(B, N, V)), dtype=torch.uint8, device=dev)
+        self.temperature = float(c.get("temperature", 0.0))   # > 0: the sampling walk
+        if self.temperature > 0:
+            self.uniforms = synth.uniforms(B, self.A, k, g=synth.gen(workload, 33, dev), device=dev)
+            ws = lib.ddt_walk_accept_sample_workspace(B, N, V)
+        else:
+            ws = lib.ddt_walk_accept_workspace(B, N, V)
+        self.walk_ws = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
         self.commit = {"src_row": torch.empty((B, self.A), **i32), "dst_pos": torch.empty((B, self.A), **i32),
                        "status": torch.empty((B,), **i32)}
 
@@ -126,9 +132,7 @@ class Round:
                              status=self.gdn_status)
         if wait:
             wait("walk")
-        ddt.ddt_walk_accept(self.tree["token"], self.tree["parent"], self.tree["n_nodes"], self.A - 1,
-                            target_logits=self.target_logits, out=self.walk, workspace=self.walk_ws,
-                            flat=bool(c.get("flat", False)))
+        self.walk_step()
         kw = {}
         if self.Lf and not self.page:
             kw.update(k_tree=self.attn.k_tree, v_tree=self.attn.v_tree, k_cache=self.attn.k_cache,
@@ -145,6 +149,18 @@ class Round:
                                  v_pages=self.v_pages, out=self.commit, **kw)
         else:
             ddt.ddt_commit(self.walk["acc_nodes"], self.walk["acc_len"], self.prefix_len, out=self.commit, **kw)
+
+    def walk_step(self):
+        """The round's walk: greedy (or its flat safe mode), or rejection sampling at
+        cfg["temperature"] with this round's uniforms."""
+        t = self.tree
+        if self.temperature > 0:
+            ddt.ddt_walk_accept_sample(t["token"], t["parent"], t["n_nodes"], self.A - 1,
+                                       target_logits=self.target_logits, uniforms=self.uniforms,
+                                       temperature=self.temperature, out=self.walk, workspace=self.walk_ws)
+        else:
+            ddt.ddt_walk_accept(t["token"], t["parent"], t["n_nodes"], self.A - 1, target_logits=self.target_logits,
+                                out=self.walk, workspace=self.walk_ws, flat=bool(self.cfg.get("flat", False)))
 
     def attention(self):
         """The round's attention call.  With cfg["rope"] (rotated channels) q and the tree
@@ -185,6 +201,8 @@ class Round:
         """The tensors a serving loop hands to each round (everything except the
         persistent caches, GDN state and conv state)."""
         ins = {"draft_logits": self.draft_logits, "root_token": self.root_token, "target_logits": self.target_logits}
+        if self.temperature > 0:
+            ins["uniforms"] = self.uniforms
         if self.Lf:
             ins.update(q=self.attn.q, k_tree=self.attn.k_tree, v_tree=self.attn.v_tree)
         if self.Lg:
@@ -198,7 +216,7 @@ class Round:
             g["attn"] = ["q", "k_tree", "v_tree"]
         if self.Lg:
             g["gdn"] = ["x", "beta", "decay"]
-        g["walk"] = ["target_logits"]
+        g["walk"] = ["target_logits"] + (["uniforms"] if self.temperature > 0 else [])
         return g
 
     def bind_inputs(self, ins: dict):
@@ -210,6 +228,8 @@ class Round:
             self.attn.q, self.attn.k_tree, self.attn.v_tree = ins["q"], ins["k_tree"], ins["v_tree"]
         if self.Lg:
             self.gdn.x, self.gdn.beta, self.gdn.decay = ins["x"], ins["beta"], ins["decay"]
+        if self.temperature > 0:
+            self.uniforms = ins["uniforms"]
 
     def round_outputs(self):
         return {"emitted": self.walk["emitted"], "n_emitted": self.walk["n_emitted"]}
