@@ -48,7 +48,7 @@ int main(void) {
     EXPECT(ddt_walk_accept(0, 5, 10, 4, DDT_BF16, p, p, p, p, p, p, p, p, p, p, p, p, 256, stream)
            == DDT_ERR_INVALID_ARG);
     EXPECT(ddt_walk_accept_sample_workspace(0, 65, 151936) == 0);
-    EXPECT(ddt_walk_accept_sample_workspace(32, 65, 151936) == 332800);  /* 32*65*10 partials of 16 B */
+    EXPECT(ddt_walk_accept_sample_workspace(32, 65, 151936) == 1248000);  /* 32*65*75 partials of 8 B */
     EXPECT(ddt_walk_accept_sample(1, 5, 10, 4, 2, 0.0f, DDT_BF16, p, (const float*)p, p, p, p, p, p, p, p, p, p,
                                   p, 1 << 20, stream) == DDT_ERR_INVALID_ARG);
     EXPECT(ddt_walk_accept_sample(1, 5, 10, 4, 2, 1e-40f, DDT_BF16, p, (const float*)p, p, p, p, p, p, p, p, p,
