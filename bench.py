@@ -334,6 +334,41 @@ def measure(r, steps, warmup, flat=False, clocks=None, world=1):
     return {"ms": t0.elapsed_time(t1), "per_call_ms": per_call, "launches": launches}
 
 
+def measure_graph(r, steps, warmup):
+    """The same round captured once into a CUDA graph and replayed: `steps` replays after
+    `warmup`, timed with CUDA events on the replaying stream.  Returns the ms per round and
+    the library launches the graph holds."""
+    from tree_speculative_decoding_02_gb300 import ddt
+
+    step = make_step(r, False, {})
+    cur = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            step(False)
+    cur.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = ddt.ddt_launch_count()
+    with torch.cuda.graph(g):
+        step(False)
+    captured = ddt.ddt_launch_count() - n0
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(cur)
+    for _ in range(steps):
+        g.replay()
+    t1.record(cur)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    del g
+    return ms, captured
+
+
 def roofline_of(call, work, ms, peaks, tc_peak, tc_kind, traffic=None):
     """The roofline object of one call: tensor-bound for the attention contraction, HBM-bound
     for the rest; `achieved` from the algorithmic work and the call's CUDA-event time."""
@@ -407,6 +442,7 @@ def run_ours(args, rank, world, local):
     value = nodes_total / (ms_max / 1e3)
     per_call = m["per_call_ms"]
 
+    graph_ms, graph_launches = measure_graph(r, args.steps, args.warmup)
     e2e = e2e_measure(r, args.steps, world, dev)
     e2e["value"] = all_sum(nodes_per_step * e2e.pop("rounds"), world, dev) / (all_max(e2e.pop("ms"), world, dev) / 1e3)
 
@@ -436,6 +472,9 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
         "gpu_launches": m["launches"],
         "clocks": clk,
+        "graph": {"ms_per_step": graph_ms, "value": nodes_per_step / (graph_ms / 1e3),
+                  "launches_per_step": graph_launches,
+                  "note": "the same round captured once into a CUDA graph and replayed (rank 0's replays)"},
     }
     if args.flat:
         out["config"]["walk"] = "flat-commit safe mode (first children only)"
@@ -570,6 +609,8 @@ def config_line(w, dev, peaks, tc_peak, tc_kind, with_cpu):
             "per_kernel_ms": per, "floor_ms": floors, "round_frac": sum(floors.values()) / step_ms,
             "roofline": roofline_of(dom, work, per[dom], peaks, tc_peak, tc_kind),
             "gpu_launches": m["launches"]}
+    gms, glaunch = measure_graph(r, 10, 3)
+    line["graph"] = {"ms_per_step": gms, "value": nodes / (gms / 1e3), "launches_per_step": glaunch}
     if with_cpu:
         line["cpu_baseline"] = config_cpu_baseline(r, w)
     del r
