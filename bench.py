@@ -201,10 +201,16 @@ def tensor_peak(peaks, clk):
 # own timed launch (dram__bytes_read.sum + dram__bytes_write.sum, one pass, full size),
 # keyed by the SHA-256 of the kernel's sources: once they change, the figure is stale
 # and the bench reports null until it is captured again.
+# DRAM traffic of one tree-attention launch, from a small capture: one launch of the
+# tree-attn-bf16 workload (1 request, prefix 4096, 16 layers, Hkv 4, d 256: 268 MB of
+# prefix K/V, more than L2), ncu dram__bytes_read.sum 286,167,552 B + dram__bytes_write.sum
+# 13,430,784 B, against 298,254,336 algorithmic bytes.  Keyed by the attention sources;
+# another workload's traffic is this per-algorithmic-byte figure times its own algorithmic
+# bytes (each (layer, request, KV head) streams its prefix K/V once, which is almost all of
+# the bytes, so traffic grows with sum_b P_b * Lf * Hkv * d).
 ATTN_TRAFFIC = {
-    # ncu, batched round, mean of the three timed launches of one capture:
-    # dram__bytes_read.sum 40,355,763,541 B + dram__bytes_write.sum 400,794,795 B
-    "bfdc4160d21e99d36f74f45bb592cfea7ca3e4b2aade0e9bd2f1fe0da592e0a8": {"workload": 5, "bytes": 40756558336.0},
+    "9f69801ee58a5d530efdd885aa6f477e949e50882f7fce1e099c55ccdd8448ff": {
+        "workload": 3, "bytes": 299598336.0, "algorithmic_bytes": 298254336.0},
 }
 ATTN_SOURCES = ("attn_tc.cu", "tc.cuh")
 
@@ -218,11 +224,13 @@ def attn_source_hash():
     return h.hexdigest()
 
 
-def attn_traffic(workload):
+def attn_traffic(algorithmic_bytes):
+    """DRAM bytes of one attention launch with these algorithmic bytes, scaled from the
+    recorded capture; None when the attention sources have changed since."""
     rec = ATTN_TRAFFIC.get(attn_source_hash())
-    if rec is None or rec["workload"] != workload:
+    if rec is None:
         return None
-    return rec["bytes"]
+    return rec["bytes"] * algorithmic_bytes / rec["algorithmic_bytes"]
 
 
 def workload_desc(c):
@@ -453,7 +461,7 @@ def run_ours(args, rank, world, local):
     step_ms = ms / args.steps
     rb = sum(by for by, _ in work.values())
     dom = max(per_call, key=per_call.get)
-    traffic = attn_traffic(args.workload) if dom == "attn" and not args.kv_page else None
+    traffic = attn_traffic(work["attn"][0]) if dom == "attn" and not args.kv_page else None
     roof = roofline_of(dom, work, per_call[dom], peaks, tc_peak, tc_kind, traffic)
     if roof["bound"] == "tensor":
         roof["frac_sustained"] = roof["achieved"] / peaks["sustained"]
@@ -607,7 +615,8 @@ def config_line(w, dev, peaks, tc_peak, tc_kind, with_cpu):
     line = {"workload": workload_desc(cfg), "dtype": "bf16" if cfg["dtype"] == torch.bfloat16 else "f32",
             "value": nodes / (step_ms / 1e3), "unit": UNIT, "ms_per_step": step_ms, "steps": 10, "warmup": 3,
             "per_kernel_ms": per, "floor_ms": floors, "round_frac": sum(floors.values()) / step_ms,
-            "roofline": roofline_of(dom, work, per[dom], peaks, tc_peak, tc_kind),
+            "roofline": roofline_of(dom, work, per[dom], peaks, tc_peak, tc_kind,
+                                    attn_traffic(work["attn"][0]) if dom == "attn" else None),
             "gpu_launches": m["launches"]}
     gms, glaunch = measure_graph(r, 10, 3)
     line["graph"] = {"ms_per_step": gms, "value": nodes / (gms / 1e3), "launches_per_step": glaunch}
