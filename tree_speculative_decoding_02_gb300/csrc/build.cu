@@ -29,12 +29,14 @@
 namespace ddt {
 
 // ---------------------------------------------------------------------------- row pass
-// One CTA per (depth, request) row of the drafter logits, two passes over the row:
-//   1. each thread's max and a non-finite check; a warp's k-th largest thread max is
+// One CTA per (depth, request) row of the drafter logits:
+//   1. one streaming pass: each thread's max, a running sum of exp(v - its max) (rescaled
+//      when the max grows) and a non-finite check.  A warp's k-th largest thread max is
 //      reached by k entries of the row, so the largest of those warp thresholds, tau, is
 //      at or below the value of the row's k-th best entry;
-//   2. (from L2) the sum of exp(v - max) and the entries whose value reaches tau (ties
-//      included), collected in shared memory -- usually a few dozen -- from which one
+//   2. only the threads whose max reaches tau can hold such entries (usually a few in
+//      the whole row): each warp re-reads those threads' entries together, and the ones
+//      that reach tau (ties included) are collected in shared memory, from which one
 //      warp takes the exact top-k by (value desc, id asc).
 // If more entries than the buffer holds reach tau (not seen on drafter-like rows), each
 // warp ranks its own entries with a warp top-k and the warp lists are merged instead.
@@ -58,7 +60,7 @@ constexpr int kCandCap = 1024;
 }  // namespace
 
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads) k_build_row(const T* __restrict__ logits, int D, int V, int k, int vec,
+__global__ void __launch_bounds__(kRowThreads, 4) k_build_row(const T* __restrict__ logits, int D, int V, int k, int vec,
                                                            BuildRow* __restrict__ rows, float* __restrict__ top_v,
                                                            int* __restrict__ top_id) {
     const int d = blockIdx.x, b = blockIdx.y;
@@ -78,26 +80,47 @@ __global__ void __launch_bounds__(kRowThreads) k_build_row(const T* __restrict__
         s_bad = 0;
     }
 
-    // ---- pass 1: each thread's max and a non-finite check.  The threshold keeps every
-    //      entry whose value reaches it (ties included), so it needs the values only.
-    float m = emp.v;
-    int bad = 0;
-    auto see = [&](float v) {
-        bad |= !finite_f32(v);
-        m = fmaxf(m, v);
+    // ---- pass 1.  A NaN or +inf entry makes the sum NaN (an exponential of NaN, or
+    //      inf - inf) and a -inf entry the smallest entry -inf: together they flag every
+    //      non-finite row.
+    const float LOG2E = 1.4426950408889634f;
+    float m = emp.v, acc = 0.f, lo = -emp.v;
+    auto see8 = [&](const float (&t8)[8], int n) {
+        float m8 = emp.v, l8 = -emp.v;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (u < n) {
+                m8 = fmaxf(m8, t8[u]);
+                l8 = fminf(l8, t8[u]);
+            }
+        lo = fminf(lo, l8);
+        if (m8 > m) {
+            acc *= exp2f((m - m8) * LOG2E);
+            m = m8;
+        }
+        const float mb = m * LOG2E;
+        float s8 = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (u < n) s8 += exp2f(fmaf(t8[u], LOG2E, -mb));
+        acc += s8;
     };
     if (vec) {  // V % 8 == 0 and 16-byte aligned rows: 8 entries a load
 #pragma unroll 4
         for (int e = tid * 8; e < V; e += kRowThreads * 8) {
             float t8[8];
             load8_stream(x + e, t8);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) see(t8[u]);
+            see8(t8, 8);
         }
     } else {
-#pragma unroll 4
-        for (int e = tid; e < V; e += kRowThreads) see(to_f32(x[e]));
+        for (int e = tid * 8; e < V; e += kRowThreads * 8) {
+            float t8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) t8[u] = (e + u < V) ? to_f32(x[e + u]) : emp.v;
+            see8(t8, min(8, V - e));
+        }
     }
+    int bad = !(fabsf(acc) < INFINITY) || lo == emp.v;  // a thread with no entries: acc 0, lo +inf
     // the warp's k-th largest thread max: k entries of the warp reach it
     float tv = m;
     int ti = lane;
@@ -117,46 +140,39 @@ __global__ void __launch_bounds__(kRowThreads) k_build_row(const T* __restrict__
         tau_v = fmaxf(tau_v, s_wv[w]);
     }
     const bool row_bad = s_bad != 0;
+    // the sum of exp(v - M): fp32 per thread and across the warp, fp64 across warps
+    const float ws = warp_sum(m == emp.v ? 0.f : acc * exp2f((m - M) * LOG2E));
+    if (lane == 0) s_sum[warp] = (double)ws;
 
-    // ---- pass 2: sum of exp(v - M) (fp32 per load of 8, per thread and across the warp,
-    //      fp64 across warps) and the entries that reach tau
-    const float LOG2E = 1.4426950408889634f;
-    const float mb = M * LOG2E;
-    float acc = 0.f;
-    auto take = [&](float v, int id) {
-        if (v >= tau_v) {
-            const int pos = atomicAdd(&s_nc, 1);
-            if (pos < kCandCap) {
-                s_cv[pos] = v;
-                s_ci[pos] = id;
-            }
-        }
-    };
+    // ---- pass 2: the entries that reach tau, from the threads whose max reaches it; the
+    //      warp re-reads one such thread's entries at a time, a load a lane
     if (!row_bad) {
-        if (vec) {
-#pragma unroll 4
-            for (int e = tid * 8; e < V; e += kRowThreads * 8) {
+        unsigned q = __ballot_sync(kFull, m >= tau_v);
+        while (q) {
+            const int t = warp * 32 + __ffs(q) - 1;  // the thread whose entries are re-read
+            q &= q - 1;
+            const int nch = t * 8 < V ? (V - t * 8 + kRowThreads * 8 - 1) / (kRowThreads * 8) : 0;
+            for (int j = lane; j < nch; j += 32) {
+                const int e = t * 8 + j * kRowThreads * 8;
                 float t8[8];
-                load8(x + e, t8);
-                float s8 = 0.f;
+                if (vec) {
+                    load8(x + e, t8);
+                } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    s8 += exp2f(fmaf(t8[u], LOG2E, -mb));
-                    take(t8[u], e + u);
+                    for (int u = 0; u < 8; ++u) t8[u] = (e + u < V) ? to_f32(x[e + u]) : emp.v;
                 }
-                acc += s8;
-            }
-        } else {
-#pragma unroll 4
-            for (int e = tid; e < V; e += kRowThreads) {
-                const float v = to_f32(x[e]);
-                acc += exp2f(fmaf(v, LOG2E, -mb));
-                take(v, e);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (t8[u] >= tau_v) {
+                        const int pos = atomicAdd(&s_nc, 1);
+                        if (pos < kCandCap) {
+                            s_cv[pos] = t8[u];
+                            s_ci[pos] = e + u;
+                        }
+                    }
             }
         }
     }
-    const float ws = warp_sum(acc);  // tree sum in fp32 across the warp, fp64 across warps
-    if (lane == 0) s_sum[warp] = (double)ws;
     __syncthreads();
     const int nc = s_nc;
     if (nc > kCandCap && !row_bad) {
@@ -201,13 +217,19 @@ __global__ void __launch_bounds__(kRowThreads) k_build_row(const T* __restrict__
 }
 
 // ---------------------------------------------------------------------- selection
+constexpr int kRegSlots = 3;  // frontier slots a lane holds in registers (budget <= 94)
+
 struct Cand {
-    double L;   // sum of path logits, depth 1 first
-    double s;   // L - cum LSE of its depth
+    double L;   // sum of path logits, depth 1 first (its score is L - cum LSE of its depth)
     int depth;  // 1..D
     int rank;   // within the depth's top-k
     int parent; // index into the selected list, -1 = root
     int pad;
+    // the two entries a pop of this one pushes, scored ahead of time: its next-ranked
+    // sibling and its best child (path sum L and score s; unused where none exists)
+    double sib_L, sib_s, ch_L, ch_s;
+    // the token path as a key with the path's lexicographic order (see lex_key_bits)
+    unsigned long long lk;
 };
 
 struct TreeSmem {
@@ -216,13 +238,19 @@ struct TreeSmem {
     double* top_vd; // [D][k] the same logits as doubles (converted once, not per push)
     int* top_id;    // [D][k]
     double* cum;    // [D+1] cumulative LSE, cum[0] = 0
-    // selection
-    Cand* sel;      // [budget]
-    Cand* front;    // [budget + 2] frontier entries
+    // selection: every candidate ever pushed stays in the pool, in push order; the
+    // frontier and the selected list hold pool indices, so a pop moves 12 bytes
+    Cand* pool;     // [2 budget + 1]
+    int* fidx;      // [budget + 2] frontier entries (pool indices)
     long long* fs;  // [budget + 2] their scores as order-preserving integer keys
+    unsigned long long* fl;  // [budget + 2] their token-path keys
+    int* idr;       // [D][k] 1 + the token's place among its depth's k token ids
+    int* sel;       // [budget] selected entries (pool indices)
     int* new_idx;   // [budget]
     int* out_par;   // [N]
 };
+
+__device__ __forceinline__ const Cand& selc(const TreeSmem& S, int i) { return S.pool[S.sel[i]]; }
 
 __device__ __forceinline__ int cand_token(const TreeSmem& S, int k, const Cand& c) {
     return S.top_id[(c.depth - 1) * k + c.rank];
@@ -238,22 +266,22 @@ __device__ bool lex_less(const TreeSmem& S, int k, const Cand& a, const Cand& b)
     int ta = cand_token(S, k, a), tb = cand_token(S, k, b);
     int pa = a.parent, pb = b.parent;  // rows of S.sel; -1 = the root
     while (da > db) {
-        const Cand& u = S.sel[pa];
+        const Cand& u = selc(S, pa);
         ta = cand_token(S, k, u);
         pa = u.parent;
         --da;
     }
     if (a.depth > b.depth && pa == pb && ta == tb) return false;  // b is a prefix of a
     while (db > da) {
-        const Cand& u = S.sel[pb];
+        const Cand& u = selc(S, pb);
         tb = cand_token(S, k, u);
         pb = u.parent;
         --db;
     }
     if (b.depth > a.depth && pa == pb && ta == tb) return true;   // a is a proper prefix of b
     while (pa != pb) {
-        const Cand& u = S.sel[pa];
-        const Cand& v = S.sel[pb];
+        const Cand& u = selc(S, pa);
+        const Cand& v = selc(S, pb);
         ta = cand_token(S, k, u);
         tb = cand_token(S, k, v);
         pa = u.parent;
@@ -272,10 +300,22 @@ __device__ __forceinline__ long long score_key(double s) {
     return b < 0 ? (b ^ 0x7fffffffffffffffLL) : b;
 }
 
+// Token paths as integer keys.  Every token at depth d is one of that depth's k top
+// tokens, so comparing two paths' tokens at a depth is comparing the tokens' places in
+// the depth's id order.  A path is packed as 1 + that place for each level, depth 1 in
+// the highest bits and zeros after its last level, so a prefix sorts before its
+// extensions: the integer order of two keys is the lexicographic order of the paths.
+// Bits a level, or 0 when D levels do not fit 64 bits (then ties climb the paths).
+__device__ __forceinline__ int lex_key_bits(int D, int k) {
+    int bits = 1;
+    while ((1 << bits) < k + 1) ++bits;
+    return bits * D <= 64 ? bits : 0;
+}
+
 // frontier entry i before entry j in the selection order (score, then token path)
 __device__ __forceinline__ bool front_before(const TreeSmem& S, int k, long long si, int i, long long sj, int j) {
     if (si != sj) return si > sj;
-    return i != j && lex_less(S, k, S.front[i], S.front[j]);
+    return i != j && lex_less(S, k, S.pool[S.fidx[i]], S.pool[S.fidx[j]]);
 }
 
 // rank-path key of selected node i: the ranks along its path from the root, `bits` bits
@@ -283,7 +323,7 @@ __device__ __forceinline__ bool front_before(const TreeSmem& S, int k, long long
 __device__ __forceinline__ unsigned long long rank_key(const TreeSmem& S, int i, int bits) {
     unsigned long long key = 0;
     int sh = 0;
-    for (int a = i; a >= 0; a = S.sel[a].parent, sh += bits) key |= (unsigned long long)S.sel[a].rank << sh;
+    for (int a = i; a >= 0; a = selc(S, a).parent, sh += bits) key |= (unsigned long long)selc(S, a).rank << sh;
     return key << (64 - sh);  // root-first levels at the top; depth is compared separately
 }
 
@@ -306,123 +346,367 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int k, int budge
     unsigned char* p = smem_raw;
     S.cum = reinterpret_cast<double*>(p);      p += sizeof(double) * (kMaxDepth + 1);
     S.fs = reinterpret_cast<long long*>(p);    p += sizeof(long long) * (budget + 2);
-    S.sel = reinterpret_cast<Cand*>(p);        p += sizeof(Cand) * (budget + 1);
-    S.front = reinterpret_cast<Cand*>(p);      p += sizeof(Cand) * (budget + 2);
+    S.fl = reinterpret_cast<unsigned long long*>(p); p += sizeof(unsigned long long) * (budget + 2);
+    S.pool = reinterpret_cast<Cand*>(p);       p += sizeof(Cand) * (2 * budget + 1);
     S.top_vd = reinterpret_cast<double*>(p);   p += sizeof(double) * D * k;
     S.top_v = reinterpret_cast<float*>(p);     p += sizeof(float) * D * k;
     S.top_id = reinterpret_cast<int*>(p);      p += sizeof(int) * D * k;
+    S.idr = reinterpret_cast<int*>(p);         p += sizeof(int) * D * k;
+    S.fidx = reinterpret_cast<int*>(p);        p += sizeof(int) * (budget + 2);
+    S.sel = reinterpret_cast<int*>(p);         p += sizeof(int) * (budget + 1);
     S.new_idx = reinterpret_cast<int*>(p);     p += sizeof(int) * (budget + 1);
     S.out_par = reinterpret_cast<int*>(p);     p += sizeof(int) * N;
     __shared__ int s_bad;
     __shared__ int s_nsel;
 
-    // 1. the depths' top-k lists and log-sum-exps (from the row pass)
+    // 1. the depths' top-k lists and log-sum-exps (from the row pass); the rows' records
+    //    are loaded by D threads at once and staged (S.cum[d + 1], and S.idr[d] until the
+    //    id places overwrite it)
     for (int e = tid; e < D * k; e += kThreads) {
         const float v = rtv[(long)b * D * k + e];
         S.top_v[e] = v;
         S.top_vd[e] = (double)v;
         S.top_id[e] = rti[(long)b * D * k + e];
     }
+    for (int d = tid; d < D; d += kThreads) {
+        const BuildRow rr = rows[(long)b * D + d];
+        S.cum[d + 1] = rr.lse;
+        S.idr[d] = rr.bad;
+    }
+    __syncthreads();
     if (tid == 0) {
         int bad = 0;
         double c = 0.0;
         S.cum[0] = 0.0;
         for (int d = 0; d < D; ++d) {
-            const BuildRow rr = rows[(long)b * D + d];
-            bad |= rr.bad;
-            c += rr.lse;
+            bad |= S.idr[d];       // the rows' flags and log-sum-exps, staged below
+            c += S.cum[d + 1];     // cumulative in depth order, as the scores are defined
             S.cum[d + 1] = c;
         }
         s_bad = bad;
     }
     __syncthreads();
     const bool bad = s_bad != 0;
+    for (int e = tid; e < D * k; e += kThreads) {
+        const int* ids = S.top_id + (e / k) * k;
+        const int t = S.top_id[e];
+        int pl = 1;
+        for (int r = 0; r < k; ++r) pl += ids[r] < t;
+        S.idr[e] = pl;
+    }
+    __syncthreads();
+    const int lbits = lex_key_bits(D, k);
 
     // 2. best-first selection: one warp keeps the frontier in shared memory (entries and
     //    their scores).  A pop is a warp argmax over the scores -- the token-path order is
-    //    consulted only on an exact score tie -- after which lane 0 moves the best entry
-    //    to the selected list and pushes its next-ranked sibling and its best child.
+    //    consulted only on an exact score tie -- after which the best entry moves to the
+    //    selected list and its next-ranked sibling and best child enter the frontier.
+    //    Their scores were formed when the popped entry itself was pushed, so a pop waits
+    //    on no fp64 add: lanes 0 and 1 score the successors of the two new entries right
+    //    after pushing them, and write those scores only after the next argmax, which
+    //    hides the adds' latency.  Every score is the same fp64 expression as ever:
+    //    L = L(parent) + logit, s = L - cum LSE of the depth.
     if (warp == 0) {
-        int n_sel = 0, n_front = 0;
-        if (budget > 0 && !bad) {
-            if (lane == 0) {
+        // successors of an entry at (depth d, rank r) whose parent path sums to Lp and
+        // whose own path sums to L: sibling (d, r + 1) and child (d + 1, 0); indices are
+        // clamped where the successor does not exist (its score is then never used)
+        auto successors = [&](int d, int r, double Lp, double L, double& sL, double& sS, double& cL, double& cS) {
+            const int rs = min(r + 1, k - 1), dc = min(d + 1, D);
+            sL = Lp + S.top_vd[(d - 1) * k + rs];
+            sS = sL - S.cum[d];
+            cL = L + S.top_vd[(dc - 1) * k];
+            cS = cL - S.cum[dc];
+        };
+        int n_sel = 0;
+        if (lbits && budget + 2 <= 32 * kRegSlots) {
+            // The frontier in registers: slot j is register j / 32 of lane j % 32, holding the
+            // entry's score key, token-path key and pool index.  A pop is then a lane-local
+            // compare of at most kRegSlots slots, a warp argmax, and register moves; only
+            // the pool records (written once, read at their pop) live in shared memory.
+            long long rk[kRegSlots];
+            unsigned long long rl[kRegSlots];
+            int rp[kRegSlots];
+#pragma unroll
+            for (int r = 0; r < kRegSlots; ++r) {
+                rk[r] = LLONG_MIN;
+                rl[r] = ~0ull;
+                rp[r] = -1;
+            }
+            int n_front = 0, n_pool = 0;
+            if (budget > 0 && !bad) {
                 Cand c0;
                 c0.depth = 1;
                 c0.rank = 0;
                 c0.parent = -1;
+                c0.pad = 0;
                 c0.L = S.top_vd[0];
-                c0.s = c0.L - S.cum[1];
-                S.front[0] = c0;
-                S.fs[0] = score_key(c0.s);
-            }
-            n_front = 1;
-        }
-        __syncwarp();
-        while (n_sel < budget && n_front > 0) {
-            int best = -1;
-            long long bs = 0;
-            for (int i = lane; i < n_front; i += 32) {
-                const long long si = S.fs[i];
-                if (best < 0 || front_before(S, k, si, i, bs, best)) {
-                    best = i;
-                    bs = si;
+                successors(1, 0, 0.0, c0.L, c0.sib_L, c0.sib_s, c0.ch_L, c0.ch_s);
+                c0.lk = (unsigned long long)S.idr[0] << (64 - lbits);
+                if (lane == 0) {
+                    S.pool[0] = c0;
+                    rk[0] = score_key(c0.L - S.cum[1]);
+                    rl[0] = c0.lk;
+                    rp[0] = 0;
                 }
+                n_front = 1;
+                n_pool = 1;
             }
-            // warp argmax on the integer keys alone; the token-path order decides only
-            // between lanes that hold the same top key (exact score ties, which bf16
-            // logits make common: every pair of nodes below two tied siblings ties too)
-            long long mk = best >= 0 ? bs : LLONG_MIN;
+            __syncwarp();
+            int pend = -1;
+            double pL = 0.0, pS = 0.0, qL = 0.0, qS = 0.0;
+            while (n_sel < budget && n_front > 0) {
+                // this lane's best slot by (score desc, token path asc)
+                int bj = -1;
+                long long bk = LLONG_MIN;
+                unsigned long long bl = ~0ull;
+                int bp = -1;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const long long om = __shfl_xor_sync(kFull, mk, o);
-                mk = om > mk ? om : mk;
-            }
-            const unsigned tied = __ballot_sync(kFull, best >= 0 && bs == mk);
-            if (__popc(tied) == 1) {
-                best = __shfl_sync(kFull, best, __ffs(tied) - 1);
-            } else {
-                int w = -1;
-                for (unsigned t = tied; t; t &= t - 1) {
-                    const int idx = __shfl_sync(kFull, best, __ffs(t) - 1);
-                    if (w < 0 || lex_less(S, k, S.front[idx], S.front[w])) w = idx;
+                for (int r = 0; r < kRegSlots; ++r) {
+                    const bool live = r * 32 + lane < n_front;
+                    if (live && (bj < 0 || rk[r] > bk || (rk[r] == bk && rl[r] < bl))) {
+                        bj = r;
+                        bk = rk[r];
+                        bl = rl[r];
+                        bp = rp[r];
+                    }
                 }
-                best = w;
+                long long mk = bk;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const long long om = __shfl_xor_sync(kFull, mk, o);
+                    mk = om > mk ? om : mk;
+                }
+                const bool top = bj >= 0 && bk == mk;
+                const unsigned tied = __ballot_sync(kFull, top);
+                int wl = __ffs(tied) - 1;
+                if (__popc(tied) > 1) {  // exact score tie: the smaller token path
+                    unsigned long long ml = top ? bl : ~0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const unsigned long long om = __shfl_xor_sync(kFull, ml, o);
+                        ml = om < ml ? om : ml;
+                    }
+                    wl = __ffs(__ballot_sync(kFull, top && bl == ml)) - 1;
+                }
+                const int wr = __shfl_sync(kFull, bj, wl);
+                const int pc = __shfl_sync(kFull, bp, wl);
+                // the last pop's new entries get their successor scores (the adds are done)
+                if (pend >= 0) {
+                    Cand& u = S.pool[pend];
+                    u.sib_L = pL;
+                    u.sib_s = pS;
+                    u.ch_L = qL;
+                    u.ch_s = qS;
+                }
+                __syncwarp();
+                const Cand& c = S.pool[pc];
+                const int c_depth = c.depth, c_rank = c.rank, c_parent = c.parent;
+                const unsigned long long c_lk = c.lk;
+                const double c_L = c.L, c_sL = c.sib_L, c_sS = c.sib_s, c_cL = c.ch_L, c_cS = c.ch_s;
+                const bool has_sib = c_rank + 1 < k, has_ch = c_depth < D;
+                const int me = n_sel, nf = n_front - 1;
+                // the last slot moves into the popped one
+                {
+                    const int ln = nf & 31, rn = nf >> 5;
+                    long long mv_k = rk[0];
+                    unsigned long long mv_l = rl[0];
+                    int mv_p = rp[0];
+#pragma unroll
+                    for (int r = 1; r < kRegSlots; ++r)
+                        if (r == rn) {
+                            mv_k = rk[r];
+                            mv_l = rl[r];
+                            mv_p = rp[r];
+                        }
+                    mv_k = __shfl_sync(kFull, mv_k, ln);
+                    mv_l = __shfl_sync(kFull, mv_l, ln);
+                    mv_p = __shfl_sync(kFull, mv_p, ln);
+                    if (lane == wl) {
+#pragma unroll
+                        for (int r = 0; r < kRegSlots; ++r)
+                            if (r == wr) {
+                                rk[r] = mv_k;
+                                rl[r] = mv_l;
+                                rp[r] = mv_p;
+                            }
+                    }
+                }
+                // the new entries (every lane forms the same keys; the slot's owner keeps them)
+                const int sh_s = 64 - lbits * c_depth, sh_c = 64 - lbits * (c_depth + 1);
+                const unsigned long long fmask = (((unsigned long long)1 << lbits) - 1) << sh_s;
+                const unsigned long long lk_s =
+                    (c_lk & ~fmask) | ((unsigned long long)S.idr[(c_depth - 1) * k + min(c_rank + 1, k - 1)] << sh_s);
+                const unsigned long long lk_c =
+                    has_ch ? (c_lk | ((unsigned long long)S.idr[min(c_depth, D - 1) * k] << sh_c)) : 0ull;
+                const int slot_s = nf, slot_c = nf + (int)has_sib;
+#pragma unroll
+                for (int r = 0; r < kRegSlots; ++r) {
+                    if (has_sib && slot_s == r * 32 + lane) {
+                        rk[r] = score_key(c_sS);
+                        rl[r] = lk_s;
+                        rp[r] = n_pool;
+                    }
+                    if (has_ch && slot_c == r * 32 + lane) {
+                        rk[r] = score_key(c_cS);
+                        rl[r] = lk_c;
+                        rp[r] = n_pool + (int)has_sib;
+                    }
+                }
+                // their pool records: lane 0 the sibling, lane 1 the child, each with its own
+                // successors' scores started now and stored after the next argmax
+                pend = -1;
+                if (lane < 2 && (lane == 0 ? has_sib : has_ch)) {
+                    Cand e;
+                    e.depth = lane == 0 ? c_depth : c_depth + 1;
+                    e.rank = lane == 0 ? c_rank + 1 : 0;
+                    e.parent = lane == 0 ? c_parent : me;
+                    e.pad = 0;
+                    e.L = lane == 0 ? c_sL : c_cL;
+                    e.lk = lane == 0 ? lk_s : lk_c;
+                    e.sib_L = e.sib_s = e.ch_L = e.ch_s = 0.0;
+                    pend = n_pool + (lane == 0 ? 0 : (int)has_sib);
+                    const double Lp = lane == 0 ? (c_parent < 0 ? 0.0 : selc(S, c_parent).L) : c_L;
+                    successors(e.depth, e.rank, Lp, e.L, pL, pS, qL, qS);
+                    S.pool[pend] = e;
+                }
+                if (lane == 0) S.sel[me] = pc;
+                n_front = nf + has_sib + has_ch;
+                n_pool += has_sib + has_ch;
+                ++n_sel;
+                __syncwarp();
             }
-            // the popped entry leaves the frontier (its slot takes the last entry); lane 0
-            // pushes its next-ranked sibling and lane 1 its best child at the same time
-            const Cand c = S.front[best];
-            const bool has_sib = c.rank + 1 < k, has_ch = c.depth < D;
-            const int me = n_sel, nf = n_front - 1;
+        } else {
+            int n_front = 0, n_pool = 0;
+            if (budget > 0 && !bad) {
+                if (lane == 0) {
+                    Cand c0;
+                    c0.depth = 1;
+                    c0.rank = 0;
+                    c0.parent = -1;
+                    c0.pad = 0;
+                    c0.L = S.top_vd[0];
+                    successors(1, 0, 0.0, c0.L, c0.sib_L, c0.sib_s, c0.ch_L, c0.ch_s);
+                    c0.lk = lbits ? (unsigned long long)S.idr[0] << (64 - lbits) : 0ull;
+                    S.pool[0] = c0;
+                    S.fidx[0] = 0;
+                    S.fs[0] = score_key(c0.L - S.cum[1]);
+                    S.fl[0] = c0.lk;
+                }
+                n_front = 1;
+                n_pool = 1;
+            }
             __syncwarp();
-            if (lane == 0) {
-                S.front[best] = S.front[nf];
-                S.fs[best] = S.fs[nf];
-                S.sel[me] = c;
+            // lanes 0 and 1: the pool entry pushed last pop whose successor scores are still in
+            // registers (-1: none)
+            int pend = -1;
+            double pL = 0.0, pS = 0.0, qL = 0.0, qS = 0.0;
+            while (n_sel < budget && n_front > 0) {
+                int best = -1;
+                long long bs = 0;
+                unsigned long long bl = 0;
+                for (int i = lane; i < n_front; i += 32) {
+                    const long long si = S.fs[i];
+                    const unsigned long long li = S.fl[i];
+                    const bool before = lbits ? (si > bs || (si == bs && li < bl)) : front_before(S, k, si, i, bs, best);
+                    if (best < 0 || before) {
+                        best = i;
+                        bs = si;
+                        bl = li;
+                    }
+                }
+                // warp argmax on the score keys; the token-path order decides only between
+                // lanes that hold the same top score (exact ties, which bf16 logits make
+                // common: every pair of nodes below two tied siblings ties too)
+                long long mk = best >= 0 ? bs : LLONG_MIN;
+    #pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const long long om = __shfl_xor_sync(kFull, mk, o);
+                    mk = om > mk ? om : mk;
+                }
+                const bool top = best >= 0 && bs == mk;
+                const unsigned tied = __ballot_sync(kFull, top);
+                if (__popc(tied) == 1) {
+                    best = __shfl_sync(kFull, best, __ffs(tied) - 1);
+                } else if (lbits) {
+                    unsigned long long ml = top ? bl : ~0ull;
+    #pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const unsigned long long om = __shfl_xor_sync(kFull, ml, o);
+                        ml = om < ml ? om : ml;
+                    }
+                    best = __shfl_sync(kFull, best, __ffs(__ballot_sync(kFull, top && bl == ml)) - 1);
+                } else {
+                    int w = -1;
+                    for (unsigned t = tied; t; t &= t - 1) {
+                        const int idx = __shfl_sync(kFull, best, __ffs(t) - 1);
+                        if (w < 0 || lex_less(S, k, S.pool[S.fidx[idx]], S.pool[S.fidx[w]])) w = idx;
+                    }
+                    best = w;
+                }
+                // the last pop's new entries get their successor scores (the adds are done by now)
+                if (pend >= 0) {
+                    Cand& u = S.pool[pend];
+                    u.sib_L = pL;
+                    u.sib_s = pS;
+                    u.ch_L = qL;
+                    u.ch_s = qS;
+                }
+                __syncwarp();
+                // the popped entry leaves the frontier (its slot takes the last entry) and joins
+                // the selected list; lane 0 pushes its next-ranked sibling, lane 1 its best child
+                const int pc = S.fidx[best];
+                const Cand& c = S.pool[pc];
+                const int c_depth = c.depth, c_rank = c.rank, c_parent = c.parent;
+                const unsigned long long c_lk = c.lk;
+                const bool has_sib = c_rank + 1 < k, has_ch = c_depth < D;
+                const int me = n_sel, nf = n_front - 1;
+                const bool push = lane < 2 && (lane == 0 ? has_sib : has_ch);
+                double eL = 0.0, eS = 0.0, Lp = 0.0;
+                if (push) {
+                    eL = lane == 0 ? c.sib_L : c.ch_L;
+                    eS = lane == 0 ? c.sib_s : c.ch_s;
+                    Lp = lane == 0 ? (c_parent < 0 ? 0.0 : selc(S, c_parent).L) : c.L;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    S.fidx[best] = S.fidx[nf];
+                    S.fs[best] = S.fs[nf];
+                    S.fl[best] = S.fl[nf];
+                    S.sel[me] = pc;
+                }
+                __syncwarp();
+                pend = -1;
+                if (push) {
+                    Cand e;
+                    e.depth = lane == 0 ? c_depth : c_depth + 1;
+                    e.rank = lane == 0 ? c_rank + 1 : 0;
+                    e.parent = lane == 0 ? c_parent : me;
+                    e.pad = 0;
+                    e.L = eL;
+                    e.lk = 0ull;
+                    if (lbits) {
+                        // the sibling replaces the last level of the popped entry's path, the
+                        // child appends a level
+                        const int sh = 64 - lbits * e.depth;
+                        const unsigned long long field = (unsigned long long)S.idr[(e.depth - 1) * k + e.rank] << sh;
+                        e.lk = lane == 0 ? ((c_lk & ~((((unsigned long long)1 << lbits) - 1) << sh)) | field) : (c_lk | field);
+                    }
+                    pend = n_pool + (lane == 0 ? 0 : (int)has_sib);
+                    const int slot = nf + (lane == 0 ? 0 : (int)has_sib);
+                    // its own successors: the sibling's parent path is the popped entry's, the
+                    // child's parent is the popped entry itself
+                    successors(e.depth, e.rank, Lp, e.L, pL, pS, qL, qS);
+                    e.sib_L = e.sib_s = e.ch_L = e.ch_s = 0.0;
+                    S.pool[pend] = e;
+                    S.fidx[slot] = pend;
+                    S.fs[slot] = score_key(eS);
+                    S.fl[slot] = e.lk;
+                }
+                n_front = nf + has_sib + has_ch;
+                n_pool += has_sib + has_ch;
+                ++n_sel;
+                __syncwarp();
             }
-            __syncwarp();
-            if (lane == 0 && has_sib) {  // same parent, same depth
-                const double L_par = (c.parent < 0) ? 0.0 : S.sel[c.parent].L;
-                Cand sib = c;
-                sib.rank = c.rank + 1;
-                sib.L = L_par + S.top_vd[(c.depth - 1) * k + sib.rank];
-                sib.s = sib.L - S.cum[c.depth];
-                S.front[nf] = sib;
-                S.fs[nf] = score_key(sib.s);
-            }
-            if (lane == 1 && has_ch) {
-                Cand ch;
-                ch.depth = c.depth + 1;
-                ch.rank = 0;
-                ch.parent = me;
-                ch.L = c.L + S.top_vd[c.depth * k];
-                ch.s = ch.L - S.cum[c.depth + 1];
-                ch.pad = 0;
-                S.front[nf + has_sib] = ch;
-                S.fs[nf + has_sib] = score_key(ch.s);
-            }
-            n_front = nf + has_sib + has_ch;
-            ++n_sel;
-            __syncwarp();
         }
         if (lane == 0) s_nsel = n_sel;
     }
@@ -437,28 +721,39 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int k, int budge
         int bits = 1;
         while ((1 << bits) < k) ++bits;
         const bool packed = bits * D <= 64;
-        unsigned long long* key = reinterpret_cast<unsigned long long*>(S.front);  // free now
-        if (packed)
-            for (int i = tid; i < n_sel; i += kThreads) key[i] = rank_key(S, i, bits);
+        unsigned long long* key = reinterpret_cast<unsigned long long*>(S.fs);  // free now
+        int* dep = S.out_par;                                                  // free until step 4
+        for (int i = tid; i < n_sel; i += kThreads) {
+            if (packed) key[i] = rank_key(S, i, bits);
+            dep[i] = selc(S, i).depth;
+        }
         __syncthreads();
         for (int i = tid; i < n_sel; i += kThreads) {
-            const int di = S.sel[i].depth;
+            const int di = dep[i];
             const unsigned long long ki = packed ? key[i] : 0ull;
             int r = 1;
+            if (packed) {
+                // every thread reads the same j: broadcast loads, no branches
+#pragma unroll 8
+                for (int j = 0; j < n_sel; ++j) {
+                    const int dj = dep[j];
+                    r += (dj < di) | ((dj == di) & (key[j] < ki));
+                }
+                S.new_idx[i] = r;
+                continue;
+            }
             for (int j = 0; j < n_sel; ++j) {
-                const int dj = S.sel[j].depth;
+                const int dj = dep[j];
                 if (dj < di) {
                     ++r;
                 } else if (dj == di && j != i) {
-                    if (packed) {
-                        r += key[j] < ki;
-                    } else {
+                    {
                         int a = i, c = j;
-                        while (S.sel[a].parent != S.sel[c].parent) {
-                            a = S.sel[a].parent;
-                            c = S.sel[c].parent;
+                        while (selc(S, a).parent != selc(S, c).parent) {
+                            a = selc(S, a).parent;
+                            c = selc(S, c).parent;
                         }
-                        r += S.sel[c].rank < S.sel[a].rank;
+                        r += selc(S, c).rank < selc(S, a).rank;
                     }
                 }
             }
@@ -472,14 +767,14 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int k, int budge
     for (int r = tid; r < N; r += kThreads) S.out_par[r] = -1;
     __syncthreads();
     for (int i = tid; i < n_sel; i += kThreads) {
-        const Cand& c = S.sel[i];
+        const Cand& c = selc(S, i);
         const int r = S.new_idx[i];
         S.out_par[r] = c.parent < 0 ? 0 : S.new_idx[c.parent];
         token[ob + r] = cand_token(S, k, c);
         parent[ob + r] = S.out_par[r];
         depth[ob + r] = c.depth;
         position[ob + r] = prefix_len[b] + c.depth;
-        if (score) score[ob + r] = c.s;
+        if (score) score[ob + r] = c.L - S.cum[c.depth];  // the same fp64 expression it was ranked by
     }
     for (int r = n_sel + 1 + tid; r < N; r += kThreads) {
         token[ob + r] = -1;
@@ -512,8 +807,9 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int k, int budge
 
 size_t build_tree_smem(int D, int k, int budget) {
     const int N = budget + 1;
-    size_t b = sizeof(double) * (kMaxDepth + 1) + sizeof(long long) * (budget + 2) + sizeof(Cand) * (budget + 1) +
-               sizeof(Cand) * (budget + 2) + sizeof(double) * D * k + sizeof(float) * D * k + sizeof(int) * D * k +
+    size_t b = sizeof(double) * (kMaxDepth + 1) + 2 * sizeof(long long) * (budget + 2) +
+               sizeof(Cand) * (2 * budget + 1) + sizeof(double) * D * k + sizeof(float) * D * k +
+               2 * sizeof(int) * D * k + sizeof(int) * (budget + 2) + sizeof(int) * (budget + 1) +
                sizeof(int) * (budget + 1) + sizeof(int) * N;
     return (b + 15) & ~(size_t)15;
 }
