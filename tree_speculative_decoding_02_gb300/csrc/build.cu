@@ -470,23 +470,21 @@ __global__ void __launch_bounds__(kThreads) k_build_tree(int D, int k, int budge
                         bp = rp[r];
                     }
                 }
-                long long mk = bk;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const long long om = __shfl_xor_sync(kFull, mk, o);
-                    mk = om > mk ? om : mk;
-                }
-                const bool top = bj >= 0 && bk == mk;
+                // warp argmax of the 64-bit keys as two 32-bit warp reductions: the high
+                // halves (sign bit flipped: unsigned order), then the low halves among the
+                // lanes that hold the top high half
+                const unsigned long long uk = (unsigned long long)bk ^ 0x8000000000000000ull;
+                const unsigned khi = (unsigned)(uk >> 32), klo = (unsigned)uk;
+                const unsigned mhi = __reduce_max_sync(kFull, khi);
+                const unsigned mlo = __reduce_max_sync(kFull, khi == mhi ? klo : 0u);
+                const bool top = bj >= 0 && khi == mhi && klo == mlo;
                 const unsigned tied = __ballot_sync(kFull, top);
                 int wl = __ffs(tied) - 1;
-                if (__popc(tied) > 1) {  // exact score tie: the smaller token path
-                    unsigned long long ml = top ? bl : ~0ull;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const unsigned long long om = __shfl_xor_sync(kFull, ml, o);
-                        ml = om < ml ? om : ml;
-                    }
-                    wl = __ffs(__ballot_sync(kFull, top && bl == ml)) - 1;
+                if (__popc(tied) > 1) {  // exact score tie: the smaller token path, the same way
+                    const unsigned lhi = (unsigned)(bl >> 32), llo = (unsigned)bl;
+                    const unsigned nhi = __reduce_min_sync(kFull, top ? lhi : ~0u);
+                    const unsigned nlo = __reduce_min_sync(kFull, top && lhi == nhi ? llo : ~0u);
+                    wl = __ffs(__ballot_sync(kFull, top && lhi == nhi && llo == nlo)) - 1;
                 }
                 const int wr = __shfl_sync(kFull, bj, wl);
                 const int pc = __shfl_sync(kFull, bp, wl);
