@@ -197,10 +197,6 @@ def tensor_peak(peaks, clk):
     return peaks[kind], kind
 
 
-# DRAM bytes (read + write) of one k_attn_tc launch, from an ncu capture of the bench's
-# own timed launch (dram__bytes_read.sum + dram__bytes_write.sum, one pass, full size),
-# keyed by the SHA-256 of the kernel's sources: once they change, the figure is stale
-# and the bench reports null until it is captured again.
 # DRAM traffic of one tree-attention launch, from a small capture: one launch of the
 # tree-attn-bf16 workload (1 request, prefix 4096, 16 layers, Hkv 4, d 256: 268 MB of
 # prefix K/V, more than L2), ncu dram__bytes_read.sum 286,167,552 B + dram__bytes_write.sum
