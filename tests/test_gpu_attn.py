@@ -116,3 +116,21 @@ def test_attn_bf16_values_past_fp16_range():
     r = _gpu(tree, inp)
     _check(r["o"], _oracle(tree, inp, 256), tree)
     assert r["status"].cpu().tolist() == [0, 0]
+
+
+def test_attn_bf16_values_far_past_fp16_range():
+    """V values of 1e5 to 5e8 (prefix tiles of both requests, a tree key) among N(0, 1)
+    values in the same rows: bf16 V is applied as it is, whatever its range."""
+    tree, inp, N = _case(3, 2, 2, 24, 4, 256, [300, 700], 64, torch.bfloat16)
+    vc = inp.v_cache.float()
+    vc[0, 0, 1, 5] *= 3e7          # tile 0 of request 0, kv head 1: bf16 path
+    vc[1, 1, 3, 650] = -5e8        # a later tile of request 1: bf16 path
+    vc[1, 1, 0, 200] = 1e5         # scaled fp16 (s = 3)
+    inp.v_cache = vc.to(torch.bfloat16)
+    vt = inp.v_tree.float()
+    vt[0, 1, 10, 2] = 2e7          # the tree tile of request 1: bf16 path
+    inp.v_tree = vt.to(torch.bfloat16)
+    for d in (256,):
+        r = _gpu(tree, inp)
+        _check(r["o"], _oracle(tree, inp, d), tree)
+        assert r["status"].cpu().tolist() == [0, 0]
