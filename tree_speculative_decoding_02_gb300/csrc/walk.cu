@@ -7,7 +7,8 @@
 // target's bonus token is emitted but must not be fed back as an accepted draft.
 //
 //   k_walk_argmax   grid (chunks, N, B): one HBM pass over the target logits; each CTA
-//                   reduces a 16384-token chunk of one row to (max, lowest argmax id).
+//                   reduces a 16384-token chunk of one row to (max, lowest argmax id)
+//                   (k_walk_argmax_bf16 for bf16 rows: packed maxima, then the id).
 //   k_walk_descend  grid B: warp-per-row merge of the chunk partials, tree check, then
 //                   one warp walks down with a ballot over the rows per step.
 #include "common.cuh"
@@ -95,6 +96,93 @@ __global__ void __launch_bounds__(256) k_walk_argmax(const T* __restrict__ logit
         pp.v = bv;
         pp.id = bid;
         pp.nonfinite = bad;
+        pp.pad = 0;
+        part[((long)b * N + i) * nch + c] = pp;
+    }
+}
+
+// bf16 logits: the chunk's maximum on packed bf16 pairs (one max per two entries), the
+// non-finite check as the largest exponent field seen, then the lowest id holding that
+// maximum from the few threads whose own maximum it is.  Same output as k_walk_argmax.
+__global__ void __launch_bounds__(256) k_walk_argmax_bf16(const __nv_bfloat16* __restrict__ logits, int N, int V,
+                                                           int nch, int vec, const int32_t* __restrict__ n_nodes,
+                                                           ArgPartial* __restrict__ part) {
+    const int c = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
+    const int nn = n_nodes[b];
+    if (i >= nn || nn > N) return;  // rows past the tree are not needed
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const __nv_bfloat16* row = logits + ((long)b * N + i) * V + (long)c * kWalkChunk;
+    const int len = min(kWalkChunk, V - c * kWalkChunk);
+    // entries past the row's end read as the lowest finite bf16 (never non-finite, and
+    // never taken: the id search below stops at the row's end)
+    constexpr uint32_t kLow = 0xff7fff7fu;
+    uint4 w[kWalkChunk / 2048];
+#pragma unroll
+    for (int j = 0; j < kWalkChunk / 2048; ++j) {
+        const int e = tid * 8 + j * 2048;
+        if (vec && e + 8 <= len) {
+            w[j] = ld_stream_u4(row + e);
+        } else {
+            uint32_t h[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) h[u] = (e + u < len) ? (uint32_t)__bfloat16_as_ushort(row[e + u]) : 0xff7fu;
+            w[j] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+        }
+    }
+    __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&kLow);
+    uint32_t ex = 0;  // largest exponent field per half: 0x7f80 marks Inf or NaN
+#pragma unroll
+    for (int j = 0; j < kWalkChunk / 2048; ++j) {
+        const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            ex = __vmaxu2(ex, ww[q] & 0x7f807f80u);
+            m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&ww[q]));
+        }
+    }
+    int bad = (ex & 0xffffu) == 0x7f80u || (ex >> 16) == 0x7f80u;
+    float mt = fmaxf(__low2float(m2), __high2float(m2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
+    bad = __any_sync(kFull, bad);
+    __shared__ float s_v[8];
+    __shared__ int s_id[8], s_bad[8];
+    if (lane == 0) {
+        s_v[warp] = mt;
+        s_bad[warp] = bad;
+    }
+    __syncthreads();
+    float M = s_v[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) M = fmaxf(M, s_v[q]);
+    // the lowest id holding M: a thread's ids rise with j, then u
+    int bid = 0x7fffffff;
+    const float mine = fmaxf(__low2float(m2), __high2float(m2));
+    if (mine == M) {
+        for (int j = 0; j < kWalkChunk / 2048 && bid == 0x7fffffff; ++j) {
+            const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid * 8 + j * 2048 + u;
+                const uint32_t h = (ww[u >> 1] >> ((u & 1) * 16)) << 16;
+                if (e < len && __uint_as_float(h) == M && bid == 0x7fffffff) bid = c * kWalkChunk + e;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bid = min(bid, __shfl_xor_sync(kFull, bid, o));
+    if (lane == 0) s_id[warp] = bid;
+    __syncthreads();
+    if (tid == 0) {
+        int id = s_id[0], anybad = s_bad[0];
+        for (int q = 1; q < 8; ++q) {
+            id = min(id, s_id[q]);
+            anybad |= s_bad[q];
+        }
+        ArgPartial pp;
+        pp.v = M;
+        pp.id = id;
+        pp.nonfinite = anybad;
         pp.pad = 0;
         part[((long)b * N + i) * nch + c] = pp;
     }
@@ -228,8 +316,8 @@ cudaError_t launch_walk(int B, int N, int V, int A, ddt_dtype dtype, const void*
         dim3 g(nch, N, B);
         const int vec = (V % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
         if (dtype == DDT_BF16)
-            k_walk_argmax<__nv_bfloat16><<<counted(g), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), N, V, nch,
-                                                            vec, n_nodes, part);
+            k_walk_argmax_bf16<<<counted(g), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), N, V, nch, vec,
+                                                            n_nodes, part);
         else
             k_walk_argmax<float><<<counted(g), 256, 0, st>>>(static_cast<const float*>(logits), N, V, nch, vec, n_nodes, part);
         cudaError_t e = cudaGetLastError();
