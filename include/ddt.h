@@ -361,7 +361,8 @@ ddt_status ddt_walk_accept_flat(int B, int N, int V, int max_accept, ddt_dtype d
  * for a NaN or +-inf logit in any row of the tree; the walk is then empty (acc_len 0,
  * bonus -1, n_emitted 0).
  * Precision: each term exp((l - m) / T) is taken in fp32 as 2^((l - m) * s2), s2 =
- * log2(e) / T rounded to fp32; the per-row normaliser sums them in fp32 within each
+ * log2(e) / T rounded to fp32, by the hardware base-2 exponential (relative error about
+ * 2^-22); the per-row normaliser sums them in fp32 within each
  * 2048-entry unit and in fp64 across units; each comparison of a probability with a
  * uniform is in fp64.  A decision whose margin is below about 2e-6 may therefore differ
  * from an exact one.

@@ -45,8 +45,14 @@ size_t walk_sample_ws_bytes(int B, int N, int V) {
 }
 
 // One tempered term: exp((l - m) / T) = 2^((l - m) * s2) with s2 = log2(e) / T rounded to
-// fp32.  -inf (an entry past the row's end, or the empty max) gives 0.
-__device__ __forceinline__ float tempered(float l, float m, float s2) { return exp2f((l - m) * s2); }
+// fp32, by the hardware base-2 exponential (ex2.approx.ftz: relative error about 2^-22;
+// terms below 2^-126 of the row's largest flush to zero).  -inf (an entry past the row's
+// end, or the empty max) gives 0.  Every term of both kernels comes from this one function.
+__device__ __forceinline__ float tempered(float l, float m, float s2) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"((l - m) * s2));
+    return y;
+}
 
 // Eight consecutive entries kept in their storage format until used (bf16: one 16-byte
 // word, so a lane holds its 64 entries in 32 registers); entries at or past `len` read
