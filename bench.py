@@ -147,6 +147,23 @@ def attn_flops_bytes(r):
     return flops, bytes_
 
 
+def attn_issued_flops(r):
+    """FLOPs the pair attention kernel issues to the tensor cores in one launch (head sizes
+    128 and 256, no prefix split): every 256-row pair tile of a (layer, request, kv head)
+    multiplies every 128-key tile, as one Q K^T and two P V passes (the two bf16 parts of P);
+    padding rows and masked keys included."""
+    c = r.cfg
+    nn = r.tree["n_nodes"].cpu().numpy()
+    P = r.prefix0.cpu().numpy()
+    G = c["Hq"] // c["Hkv"]
+    tiles = 0
+    for b in range(len(nn)):
+        pairs = -(-(r.N * G) // 256)
+        keys = -(-int(P[b]) // 128) + -(-int(nn[b]) // 128)
+        tiles += pairs * keys
+    return float(tiles) * r.Lf * c["Hkv"] * 2.0 * 3 * 256 * 128 * c["d"]
+
+
 def call_work(r):
     """Algorithmic work of each call of one round: {call: (bytes, flops)}; bytes are read +
     written once, flops are the attention contraction's (4 d per query row and visible key)."""
@@ -462,6 +479,11 @@ def run_ours(args, rank, world, local):
     if roof["bound"] == "tensor":
         roof["frac_sustained"] = roof["achieved"] / peaks["sustained"]
         roof["frac_burst"] = roof["achieved"] / peaks["burst"]
+        if cfg["d"] in (128, 256) and cfg["dtype"] == torch.bfloat16:
+            iss = attn_issued_flops(r)
+            roof["issued"] = {"flops": iss, "tflops": iss / (per_call[dom] / 1e3) / 1e12,
+                              "note": "MMA work the kernel issues: 256-row pair tiles x 128-key tiles, "
+                                      "Q K^T plus two P V passes"}
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
