@@ -259,11 +259,40 @@ def workload_desc(c):
     return ", ".join(parts)
 
 
+L2_BYTES = 129e6          # the GB300's L2
+FLUSH_BYTES = 512 << 20   # written between timed rounds when a round's inputs fit in L2
+
+
+def round_input_bytes(cfg, prefix_total):
+    """Bytes of the inputs one round reads at least once: drafter and target logits, the
+    committed prefix K/V, and the committed GDN state."""
+    esz = 2 if cfg["dtype"] == torch.bfloat16 else 4
+    n = cfg["budget"] + 1
+    by = cfg["B"] * (cfg["D"] + n) * cfg["V"] * esz
+    if cfg.get("Lf"):
+        by += 2 * cfg["Lf"] * cfg["Hkv"] * cfg["d"] * esz * prefix_total
+    if cfg.get("Lg"):
+        by += cfg["Lg"] * cfg["B"] * cfg["Hv"] * cfg["dk"] * cfg["dv"] * 4
+    return float(by)
+
+
+def needs_flush(cfg, prefix_total):
+    """A round whose inputs are under twice the L2 would find them cached on the next
+    round: those are timed with an L2 flush between rounds, outside the timed spans."""
+    return round_input_bytes(cfg, prefix_total) < 2 * L2_BYTES
+
+
 def arm_config(cfg, prefix_total, nodes_per_round, world):
     """The `config` object both arms print."""
+    by = round_input_bytes(cfg, prefix_total)
+    if needs_flush(cfg, prefix_total):
+        l2 = (f"L2 flushed between timed rounds ({FLUSH_BYTES >> 20} MB written outside the timed spans); "
+              f"inputs {by / 1e6:.1f} MB a round")
+    else:
+        l2 = f"inputs larger than L2 ({by / 1e9:.2f} GB read a round)"
     return {"workload": workload_desc(cfg), "B": cfg["B"], "budget": cfg["budget"],
             "nodes_per_round": nodes_per_round, "prefix_total": prefix_total,
-            "l2": "inputs larger than L2 (tens of GB per round)", "parallelism": f"replicas x{world}"}
+            "l2": l2, "parallelism": f"replicas x{world}"}
 
 
 # --------------------------------------------------------------------- our arm
@@ -318,19 +347,24 @@ def make_step(r, flat, ev):
             names = list(marks)
             for a_, b_ in zip(names[:-1], names[1:]):
                 ev.setdefault(b_, []).append((marks[a_], marks[b_]))
+            spans.append((marks[names[0]], marks[names[-1]]))
 
+    spans = ev.setdefault("_rounds", [])
     return step
 
 
 def measure(r, steps, warmup, flat=False, clocks=None, world=1):
     """Times `steps` rounds after `warmup` untimed ones: CUDA events on the launching stream
-    around the whole timed region (barrier + synchronize on both sides) and around each
-    call.  Returns the total ms, mean ms per call, and the library's launch count."""
+    around the whole timed region (barrier + synchronize on both sides), around each round
+    and around each call.  When the round's inputs fit in L2, a flush buffer is written
+    between rounds and the total is the sum of the rounds' own spans.  Returns the total
+    ms, mean ms per call, and the library's launch count."""
     from tree_speculative_decoding_02_gb300 import ddt
 
     st = torch.cuda.current_stream()
     ev = {}
     step = make_step(r, flat, ev)
+    flush = flush_buffer(r)
     for _ in range(warmup):
         step(False)
     torch.cuda.synchronize()
@@ -347,18 +381,31 @@ def measure(r, steps, warmup, flat=False, clocks=None, world=1):
     t0.record(st)
     for _ in range(steps):
         step(True)
+        if flush is not None:
+            flush.zero_()
     t1.record(st)
     launches = ddt.ddt_launch_count() - launches0
     torch.cuda.synchronize()
     barrier(world)
+    rounds = ev.pop("_rounds")
     per_call = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
-    return {"ms": t0.elapsed_time(t1), "per_call_ms": per_call, "launches": launches}
+    # with flushes in between, the rounds' own spans; otherwise the whole region
+    ms = sum(a.elapsed_time(b) for a, b in rounds) if flush is not None else t0.elapsed_time(t1)
+    return {"ms": ms, "per_call_ms": per_call, "launches": launches}
+
+
+def flush_buffer(r):
+    """The buffer written between timed rounds when the round's inputs fit in L2, else None."""
+    if not needs_flush(r.cfg, int(r.prefix0.sum())):
+        return None
+    return torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=r.prefix0.device)
 
 
 def measure_graph(r, steps, warmup):
     """The same round captured once into a CUDA graph and replayed: `steps` replays after
-    `warmup`, timed with CUDA events on the replaying stream.  Returns the ms per round and
-    the library launches the graph holds."""
+    `warmup`, each bracketed by CUDA events on the replaying stream (with the L2 flushed
+    between replays when the round's inputs fit in it).  Returns the ms per round and the
+    library launches the graph holds."""
     from tree_speculative_decoding_02_gb300 import ddt
 
     step = make_step(r, False, {})
@@ -378,14 +425,19 @@ def measure_graph(r, steps, warmup):
     for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(cur)
-    for _ in range(steps):
+    flush = flush_buffer(r)
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in marks:
+        a.record(cur)
         g.replay()
-    t1.record(cur)
+        b.record(cur)
+        if flush is not None:
+            flush.zero_()
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
+    if flush is None:
+        ms = marks[0][0].elapsed_time(marks[-1][1]) / steps
+    else:
+        ms = sum(a.elapsed_time(b) for a, b in marks) / steps
     del g
     return ms, captured
 

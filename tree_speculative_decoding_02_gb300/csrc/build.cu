@@ -31,9 +31,9 @@ namespace ddt {
 // ---------------------------------------------------------------------------- row pass
 // One CTA per (depth, request) row of the drafter logits:
 //   1. one streaming pass: each thread's max, a running sum of exp(v - its max) (rescaled
-//      when the max grows) and a non-finite check.  A warp's k-th largest thread max is
-//      reached by k entries of the row, so the largest of those warp thresholds, tau, is
-//      at or below the value of the row's k-th best entry;
+//      when the max grows) and a non-finite check.  The k-th largest of the 512 thread
+//      maxima, tau, is reached by k entries of the row, so it is at or below the value of
+//      the row's k-th best entry;
 //   2. only the threads whose max reaches tau can hold such entries (usually a few in
 //      the whole row): each warp re-reads those threads' entries together, and the ones
 //      that reach tau (ties included) are collected in shared memory, from which one
@@ -58,6 +58,12 @@ constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kCandCap = 1024;
 }  // namespace
+
+// an integer key with the order of the float (-0 just below +0); not for NaN
+__device__ __forceinline__ int ord_key(float f) {
+    const int i = __float_as_int(f);
+    return i >= 0 ? i : i ^ 0x7fffffff;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads, 4) k_build_row(const T* __restrict__ logits, int D, int V, int k, int vec,
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) k_build_row(const T* __restric
         }
     }
     int bad = !(fabsf(acc) < INFINITY) || lo == emp.v;  // a thread with no entries: acc 0, lo +inf
-    // the warp's k-th largest thread max: k entries of the warp reach it
+    // the warp's thread maxima, largest first
     float tv = m;
     int ti = lane;
     warp_sort_best_first(tv, ti);
@@ -131,13 +137,26 @@ __global__ void __launch_bounds__(kRowThreads, 4) k_build_row(const T* __restric
         s_m[warp] = wm;
         if (bad) s_bad = 1;
     }
-    if (lane == k - 1) s_wv[warp] = tv;
+    s_wv[warp * 32 + lane] = tv;
     __syncthreads();
-    float M = s_m[0], tau_v = s_wv[0];
+    float M = s_m[0];
 #pragma unroll 1
-    for (int w = 1; w < kRowWarps; ++w) {
-        M = fmaxf(M, s_m[w]);
-        tau_v = fmaxf(tau_v, s_wv[w]);
+    for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_m[w]);
+    // tau = the k-th largest thread max of the block: k thread maxima, i.e. k entries of
+    // the row, reach it, so it is at or below the row's k-th best value.  Every warp merges
+    // the warps' sorted lists (lane w walks warp w's list) and pops k times.
+    float tau_v = emp.v;
+    {
+        int pos = 0;
+        float head = lane < kRowWarps ? s_wv[lane * 32] : emp.v;
+#pragma unroll 1
+        for (int i = 0; i < k; ++i) {
+            const int key = lane < kRowWarps ? ord_key(head) : INT_MIN;
+            const unsigned who = __ballot_sync(kFull, key == __reduce_max_sync(kFull, key));
+            const int src = __ffs(who) - 1;
+            tau_v = __shfl_sync(kFull, head, src);
+            if (lane == src) head = ++pos < 32 ? s_wv[lane * 32 + pos] : emp.v;
+        }
     }
     const bool row_bad = s_bad != 0;
     // the sum of exp(v - M): fp32 per thread and across the warp, fp64 across warps

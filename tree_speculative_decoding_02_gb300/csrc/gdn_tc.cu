@@ -8,6 +8,8 @@
 //   u_t = b_t (v_t - g_t S0 k_t) - sum_{s in anc(t)} b_t G_ts (k_s . k_t) u_s
 //   o_t = g_t S0 q_t + sum_{s in anc(t)+t} G_ts (k_s . q_t) u_s
 // One CTA owns a (layer, request, key head) and the Hv/Hk value heads that read it:
+//   thread 0    TMA: the key head's q and k channel rows (node rows, then conv-state
+//               rows) at the start, and each value head's v channel rows one head ahead.
 //   all warps   conv + SiLU + L2 norm of q and k for every node, written once as a tf32
 //               K-major tile [k rows | q rows] (128-byte swizzle); the (k_s . k_t) and
 //               (k_s . q_t) dot products along every ancestor chain.
@@ -15,8 +17,9 @@
 //               contiguous) into shared memory.
 //   warp 1      tcgen05.mma kind::tf32: D = S0 [k | q]^T, i.e. S0 k_t and S0 q_t for every
 //               node, into one of two TMEM buffers (lane = value channel).
-//   warps 4-7   per value channel (= TMEM lane): v_t by the conv along the path,
-//               u_t by forward substitution down the tree, o_t; written to global.
+//   all warps   per value channel (= TMEM lane; the warps of a lane quarter take
+//               interleaved 8-node chunks): v_t by the conv along the path, the chain
+//               coefficients by back substitution, o_t; written to global.
 // S0 is read once from HBM; no node state ever exists.  Waits are bounded.
 #include <cuda.h>
 #include <math.h>
@@ -33,12 +36,15 @@ namespace {
 
 constexpr int kDK = 128, kDV = 128;  // head sizes of this path
 constexpr int kMD = 16;              // deepest tree this path takes (drafter depth <= 16)
-constexpr int kThr = 384;   // 12 warps; lane 0 of warp 0 loads S0, lane 0 of warp 1 issues the MMAs
-constexpr int kEpi = kThr;  // epilogue threads: every warp
+// threads a CTA: 16 warps for conv width 4 (registers allow it), 12 for the generic width;
+// lane 0 of warp 0 loads S0, lane 0 of warp 1 issues the MMAs, every warp runs the
+// epilogue (the warps of a TMEM lane quarter take interleaved node chunks)
+__host__ __device__ constexpr int gdn_threads(int kt) { return kt == 4 ? 512 : 384; }
 constexpr int kMaxK = 8;    // widest short conv
 
 struct GdnTcParams {
     int L, B, N, Hk, Hv, R, K, C, QOFF, NPAD;
+    int wvec;  // conv_w is 16-byte aligned: width-4 taps are read as vectors
     const void* x;
     const void* conv_w;
     const void* conv_state;
@@ -73,7 +79,7 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     if (L.u + ub < L.s0 + kq_bytes) ub = L.s0 + kq_bytes - L.u;
     // during the conv stage the k channels' input rows are staged past the low parts
     L.sk = (L.s0 + kq_bytes > L.u ? L.s0 + kq_bytes - L.u : 0);
-    L.sk = L.u + ((L.sk + 15) & ~(size_t)15);
+    L.sk = L.u + ((L.sk + 127) & ~(size_t)127);  // a TMA destination: 128-byte aligned
     const size_t skb = (size_t)(N + K - 1) * kDK * esz;
     if (L.u + ub < L.sk + skb) ub = L.sk + skb - L.u;
     off += (ub + 15) & ~(size_t)15;
@@ -92,8 +98,8 @@ __host__ __device__ GdnSmem gdn_tc_layout(int N, int NPAD, int K, int esz) {
     off += (size_t)N * kMD * 4;
     L.small = off;
     off += (size_t)N * 4 * 9;                // dep, par, qself, gcum[2], beta[2], decay[2]
-    off = (off + 15) & ~(size_t)15;
-    L.sv = off;                              // one value head's v channels: node rows, then conv-state rows
+    off = (off + 127) & ~(size_t)127;
+    L.sv = off;                              // one value head's v channels: node rows, then conv-state rows (TMA)
     off += (size_t)(N + K - 1) * kDV * esz;
     off = (off + 7) & ~(size_t)7;
     L.bars = off;
@@ -156,7 +162,10 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // KT: compile-time conv width (K == KT), or kMaxK for any K <= kMaxK given at run time
 template <typename Tin, typename Tout, int KT>
-__global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const __grid_constant__ CUtensorMap tm_s) {
+__global__ void __launch_bounds__(gdn_threads(KT), 1) k_gdn_tc(const GdnTcParams p, const __grid_constant__ CUtensorMap tm_s,
+                                                    const __grid_constant__ CUtensorMap tm_x,
+                                                    const __grid_constant__ CUtensorMap tm_cs) {
+    constexpr int kThr = gdn_threads(KT), kEpi = kThr, kQuads = kThr / 128;
     extern __shared__ unsigned char smem_raw[];
     // align to 1024 B by pointer arithmetic on the shared array (keeps the address space)
     unsigned char* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -172,6 +181,8 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     float* scb = reinterpret_cast<float*>(base + lay.cb);
     int* trow = reinterpret_cast<int*>(base + lay.tr);                // [N][K] the same rows in sv
     Tin* sv = reinterpret_cast<Tin*>(base + lay.sv);                  // [N + K - 1][kDV]
+    // the per-node chain arrays (alist, skk, sqk, sca, scb) are level-major, [level][N]:
+    // threads that each take a node touch consecutive words
     int* alist = reinterpret_cast<int*>(base + lay.alist);
     int* sdep = reinterpret_cast<int*>(base + lay.small);
     int* spar = sdep + N;
@@ -189,6 +200,8 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     int* err = abort_flag + 1;
+    uint64_t* qk_full = bars + 10;  // q and k rows staged
+    uint64_t* v_full = bars + 11;   // a value head's v rows staged (one phase a head)
 
     const int g = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -199,49 +212,97 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     const Tin* csb = static_cast<const Tin*>(p.conv_state) + lb * (K - 1) * C;
     const Tin* wl = static_cast<const Tin*>(p.conv_w) + (long)l * C * K;
 
-    // warm L2 with every x row the CTA will read (q and k channels of its key head and v
-    // channels of its value heads, for each node and each conv-state row), so the conv
-    // loads below wait on L2 rather than DRAM
+    Tin* sk = reinterpret_cast<Tin*>(base + lay.sk);  // [N + K - 1][kDK], like sv
+    // rows of one 128-channel group (x channels cb) into a staging buffer by TMA: the N
+    // node rows of this (layer, request), then its K - 1 conv-state rows at row N
+    const uint32_t stage_bytes = (uint32_t)((N + K - 1) * 128 * (int)sizeof(Tin));
+    auto stage_rows = [&](Tin* dst, uint64_t* bar, int cb) {
+        tc::tma_load_2d(dst, &tm_x, bar, cb, (int)(lb * N));
+        if (K > 1) tc::tma_load_2d(dst + (long)N * 128, &tm_cs, bar, cb, (int)(lb * (K - 1)));
+    };
+    if (tid == 0) {
+        *err = (nn < 1 || nn > N) ? DDT_ERR_TREE : DDT_OK;
+        *abort_flag = 0;
+        tc::mbar_init(full, 1);
+        tc::mbar_init(s_free, 1);
+        tc::mbar_init(d_full, 1);
+        tc::mbar_init(d_full + 1, 1);
+        tc::mbar_init(d_free, kEpi);
+        tc::mbar_init(d_free + 1, kEpi);
+        tc::mbar_init(drain, 1);
+        tc::mbar_init(g_done, 1);
+        tc::mbar_init(qk_full, 1);
+        tc::mbar_init(v_full, 1);
+        tc::fence_mbar_init();
+        // ---- the group's q and k channel rows (node rows and conv-state rows) into shared
+        //      memory, issued first so that they land while the tree is parsed
+        tc::prefetch_tmap(&tm_x);
+        if (K > 1) tc::prefetch_tmap(&tm_cs);
+        tc::mbar_expect_tx(qk_full, 2 * stage_bytes);
+        stage_rows(sv, qk_full, g * kDK);
+        stage_rows(sk, qk_full, (p.Hk + g) * kDK);
+    }
+    // the conv weights of the group's q and k channels (four channels a lane), and the
+    // first value head's gates and v-channel conv weights, all loaded early and kept in
+    // the input type until they are used (so that no conversion waits on the loads here);
+    // taps past K repeat the last one and are never used
+    const int c4 = 4 * lane;
+    Tin w_in[2][4][KT];
+    {
+        const int cbq = g * kDK, cbk = (p.Hk + g) * kDK;
+        if (KT == 4 && p.wvec) {
+            // width 4: a lane's four channels are 16 consecutive weights (16-byte vectors)
+            constexpr int kV = 16 * (int)sizeof(Tin) / 16;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                uint4 buf[kV];
+                const uint4* src = reinterpret_cast<const uint4*>(wl + (long)((part ? cbk : cbq) + c4) * 4);
+#pragma unroll
+                for (int i = 0; i < kV; ++i) buf[i] = src[i];
+                const Tin* vals = reinterpret_cast<const Tin*>(buf);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+                    for (int q = 0; q < KT; ++q) w_in[part][ch][q] = vals[ch * 4 + (q & 3)];
+            }
+        } else {
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+                    for (int q = 0; q < KT; ++q)
+                        w_in[part][ch][q] = wl[(long)((part ? cbk : cbq) + c4 + ch) * K + min(q, K - 1)];
+        }
+    }
+    float dec_nx = 0.f, beta_nx = 0.f;
+    if (tid < nn && nn <= N) {
+        dec_nx = p.decay[(lb * N + tid) * p.Hv + g * p.R];
+        beta_nx = p.beta[(lb * N + tid) * p.Hv + g * p.R];
+    }
+    Tin wv_nx[KT];
+    {
+        const int cv = 2 * p.Hk * kDK + g * p.R * kDV + (tid & (kDV - 1));
+#pragma unroll
+        for (int q = 0; q < KT; ++q) wv_nx[q] = wl[(long)cv * K + min(q, K - 1)];
+    }
+    // warm L2 with the v channels of the later value heads and with their gates
     {
         const int nr = min(max(nn, 0), N);
-        const int lq = (kDK * (int)sizeof(Tin) + 127) / 128, lv = (p.R * kDV * (int)sizeof(Tin) + 127) / 128;
-        const int per = 2 * lq + lv, step = 128 / (int)sizeof(Tin);
+        const int lv = (kDV * (int)sizeof(Tin) + 127) / 128, step = 128 / (int)sizeof(Tin);
+        const int per = (p.R - 1) * lv;
         for (int e = tid; e < (nr + K - 1) * per; e += kThr) {
             const int r = e / per, sgm = e % per;
             const Tin* row = r < nr ? xb + (long)r * C : csb + (long)(r - nr) * C;
-            long off;
-            if (sgm < lq) off = (long)g * kDK + sgm * step;
-            else if (sgm < 2 * lq) off = (long)(p.Hk + g) * kDK + (sgm - lq) * step;
-            else off = 2L * p.Hk * kDK + (long)g * p.R * kDV + (sgm - 2 * lq) * step;
-            prefetch_l2(row + off);
+            prefetch_l2(row + 2L * p.Hk * kDK + (long)(g * p.R + 1) * kDV + (long)sgm * step);
         }
-        for (int n = tid; n < nr; n += kThr) {  // the gates of the CTA's value heads
+        for (int n = tid; n < nr; n += kThr) {
             prefetch_l2(p.beta + (lb * N + n) * p.Hv + (long)g * p.R);
             prefetch_l2(p.decay + (lb * N + n) * p.Hv + (long)g * p.R);
         }
     }
-    if (tid == 0) {
-        *err = (nn < 1 || nn > N) ? DDT_ERR_TREE : DDT_OK;
-        *abort_flag = 0;
-    }
     __syncthreads();
     const int nv = (*err == DDT_OK) ? nn : 0;
-    // ---- the group's q and k channel rows of every node and conv-state row into shared
-    //      memory (16-byte cp.async, all in flight together), issued first so that they
-    //      land while the tree is parsed
-    constexpr int kVecQK = kDK * (int)sizeof(Tin) / 16;
-    Tin* sk = reinterpret_cast<Tin*>(base + lay.sk);  // [N + K - 1][kDK], like sv
-    {
-        const int cbq = g * kDK, cbk = (p.Hk + g) * kDK;
-        for (int i = tid; i < 2 * (nv > 0 ? nv + K - 1 : 0) * kVecQK; i += kThr) {
-            const int part = i & 1, r = (i >> 1) / kVecQK, c = (i >> 1) % kVecQK;
-            const Tin* src = (r < nv ? xb + (long)r * C : csb + (long)(r - nv) * C) + (part ? cbk : cbq) +
-                             c * (16 / (int)sizeof(Tin));
-            const int rs = r < nv ? r : N + (r - nv);
-            cp_async16(reinterpret_cast<unsigned char*>((part ? sk : sv) + (long)rs * kDK) + c * 16, src);
-        }
-        cp_async_commit();
-    }
     // ---- tree check, ancestor lists, conv input rows (the node's path, newest last,
     //      continued by the committed conv state past the root)
     for (int n = tid; n < nv; n += kThr) {
@@ -258,12 +319,12 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                     atomicExch(err, DDT_ERR_UNSUPPORTED);
                     break;
                 }
-                alist[n * kMD + d++] = a;
+                alist[d++ * N + n] = a;  // level-major: [level][node]
             }
             sdep[n] = d;
             for (int q = 0; q < K; ++q) {
                 const int back = K - 1 - q;
-                const int r = back == 0 ? n : (back <= d ? alist[n * kMD + back - 1] : N + (K - 1 - (back - d)));
+                const int r = back == 0 ? n : (back <= d ? alist[(back - 1) * N + n] : N + (K - 1 - (back - d)));
                 trow[n * K + q] = r;
             }
         }
@@ -271,7 +332,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     __syncthreads();
     Tout* obase = static_cast<Tout*>(p.o) + lb * N * p.Hv * kDV;
     if (*err != DDT_OK) {
-        cp_async_wait_all();  // no copy may still be landing when the CTA leaves
+        tc::mbar_wait(qk_full, 0, abort_flag);  // no copy may still be landing when the CTA leaves
         if (tid == 0 && g == 0 && l == 0) p.status[b] = *err;
         for (int hi = 0; hi < p.R; ++hi) {
             const int h = g * p.R + hi;
@@ -281,18 +342,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
         return;
     }
 
-    // ---- setup: barriers, TMEM, first S0 load
-    if (tid == 0) {
-        tc::mbar_init(full, 1);
-        tc::mbar_init(s_free, 1);
-        tc::mbar_init(d_full, 1);
-        tc::mbar_init(d_full + 1, 1);
-        tc::mbar_init(d_free, kEpi);
-        tc::mbar_init(d_free + 1, kEpi);
-        tc::mbar_init(drain, 1);
-        tc::mbar_init(g_done, 1);
-        tc::fence_mbar_init();
-    }
+    // ---- setup: TMEM, first S0 load
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, 512);
         tc::tmem_relinquish();
@@ -306,18 +356,14 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     //      channels of q and of k, so each norm is one warp reduction and each 16-byte store
     //      of the swizzled tile is conflict-free
     {
-        const int c4 = 4 * lane;
-        const int cbq = g * kDK, cbk = (p.Hk + g) * kDK;
         float w[2][4][KT];
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-                for (int q = 0; q < KT; ++q)
-                    w[part][ch][q] = (q < K) ? to_f32(wl[(long)((part ? cbk : cbq) + c4 + ch) * K + q]) : 0.f;
-        cp_async_wait_all();
-        __syncthreads();
+                for (int q = 0; q < KT; ++q) w[part][ch][q] = (q < K) ? to_f32(w_in[part][ch][q]) : 0.f;
+        tc::mbar_wait(qk_full, 0, abort_flag);
 #pragma unroll 3
         for (int n = warp; n < N; n += kThr / 32) {
             float y[2][4] = {};
@@ -368,18 +414,23 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 *reinterpret_cast<float4*>(sLO + sw_off(row, c4, p.NPAD)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        // padding rows of the tile
-        for (int e = tid; e < p.NPAD * (kDK / 4); e += kThr) {
-            const int row = e / (kDK / 4), col = (e % (kDK / 4)) * 4;
-            const bool used = row < N || (row >= p.QOFF && row < p.QOFF + N);
-            if (!used) {
-                *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4*>(sLO + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        // padding rows of the tile: [N, QOFF) and [QOFF + N, NPAD)
+        const int gap = p.QOFF - N;
+        for (int e = tid; e < (p.NPAD - 2 * N) * (kDK / 4); e += kThr) {
+            const int pr = e / (kDK / 4), col = (e % (kDK / 4)) * 4;
+            const int row = pr < gap ? N + pr : p.QOFF + N + (pr - gap);
+            *reinterpret_cast<float4*>(sKQ + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(sLO + sw_off(row, col, p.NPAD)) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     tc::fence_proxy_async();
     __syncthreads();
+    // the q rows are consumed: the first value head's v rows go into their buffer
+    const int cv0 = 2 * p.Hk * kDK + g * p.R * kDV;  // x channel of the first value head
+    if (tid == 0) {
+        tc::mbar_expect_tx(v_full, stage_bytes);
+        stage_rows(sv, v_full, cv0);
+    }
 
     // ---- dot products along ancestor chains: the Gram matrix G[t][c] = k_t . kq_c for tile
     //      rows t < 128 and every [k | q] column c holds all k_s . k_t and k_s . q_t.  It is
@@ -417,14 +468,15 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 tc::tma_load_2d(sS0 + blk * (kDV * 128), &tm_s, full, blk * 32, srow0);
         }
     }
-    if (warp >= 4 && warp < 8) {
-        const int t = tid - 128;
+    if (warp >= 4 && warp < 12) {
+        const int t = (tid & 127);  // tile row = TMEM lane
         const bool gok = __all_sync(kFull, tc::mbar_wait(g_done, 0, abort_flag));
         if (gok) {
             tc::tc_fence_after();
             const uint32_t rowaddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + gcol;
-            // the k columns [0, N) then the q columns [QOFF, QOFF + N), 32 at a time
-            for (int part = 0; part < 2; ++part) {
+            // warps 4-7 the k columns [0, N), warps 8-11 the q columns [QOFF, QOFF + N), 32 at a time
+            {
+                const int part = warp >= 8;
                 const int cb = part ? p.QOFF : 0, ob = part ? N : 0;
                 for (int c0 = 0; c0 < N; c0 += 32) {
                     uint32_t v0[16], v1[16];
@@ -449,15 +501,15 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
     }
     __syncthreads();
     for (int e = tid; e < nn * (kMD + 1); e += kThr) {
-        const int t = e / (kMD + 1), m = e % (kMD + 1);
+        const int m = e / nn, t = e % nn;
         const int dep = sdep[t];
         if (m > dep) continue;
         if (m == dep) {
             sqself[t] = gram[t * gs + N + t];  // k_t . q_t
         } else {
-            const int s = alist[t * kMD + m];
-            skk[t * kMD + m] = gram[t * gs + s];      // k_t . k_s
-            sqk[t * kMD + m] = gram[s * gs + N + t];  // k_s . q_t
+            const int s = alist[m * N + t];
+            skk[m * N + t] = gram[t * gs + s];      // k_t . k_s
+            sqk[m * N + t] = gram[s * gs + N + t];  // k_s . q_t
         }
     }
     tc::tc_fence_before();
@@ -491,34 +543,18 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
         // --------------------------------------------------------------- epilogue (12 warps)
         const int e = tid;
         const int j = e & (kDV - 1);  // value channel = TMEM lane
-        const int quad = e >> 7;      // which third of the node chunks
+        const int quad = e >> 7;      // which of the kQuads interleaved sets of node chunks
         const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         bool dead = false;
         // Per-head arrays come in two buffers (head hi uses buffer hi & 1), so that the
         // gates, chain coefficients and back substitution of head hi + 1 overlap the R and
         // output passes of head hi: two barriers a head.
-        //   top of head hi:  back substitution (hi); R pass (hi); gates (hi + 1)
-        //   barrier 1:       R rows, M rows (hi) and gates (hi + 1) visible; v rows free
-        //                    v rows (hi + 1) staged; chain coefficients (hi + 1); output
-        //                    pass (hi)
-        //   barrier 2:       coefficients (hi + 1) and v rows (hi + 1) visible; R rows free
-        float dec_nx = 0.f, beta_nx = 0.f;
-        if (e < nn) {
-            dec_nx = p.decay[(lb * N + e) * p.Hv + g * p.R];
-            beta_nx = p.beta[(lb * N + e) * p.Hv + g * p.R];
-        }
-        // stage a head's v channels of the node rows and conv-state rows (16-byte cp.async)
-        auto stage_v = [&](int h) {
-            constexpr int kVec = kDV * (int)sizeof(Tin) / 16;
-            const long cv0 = 2L * p.Hk * kDK + (long)h * kDV;
-            for (int i = e; i < (nn + K - 1) * kVec; i += kEpi) {
-                const int r = i / kVec, c = i % kVec;
-                const Tin* src = (r < nn ? xb + (long)r * C : csb + (long)(r - nn) * C) + cv0 + c * (16 / (int)sizeof(Tin));
-                const int rs = r < nn ? r : N + (r - nn);
-                cp_async16(reinterpret_cast<unsigned char*>(sv + (long)rs * kDV) + c * 16, src);
-            }
-            cp_async_commit();
-        };
+        //   top of head hi:  back substitution (hi); v rows (hi) landed; R pass (hi);
+        //                    gates (hi + 1)
+        //   barrier 1:       R rows, M rows (hi) and gates (hi + 1) visible; v rows free:
+        //                    one thread stages v rows (hi + 1) by TMA; chain coefficients
+        //                    (hi + 1); output pass (hi)
+        //   barrier 2:       coefficients (hi + 1) visible; R rows free
         // gates of head hi (already in registers) into buffer hi & 1; next head's into registers
         auto gates = [&](int hi) {
             if (e < nn) {
@@ -540,9 +576,9 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 const float bt = sbeta[(hi & 1) * N + e];
                 float* cb = scb + (hi & 1) * N * kMD;
                 for (int m = 0; m < dep; ++m) {
-                    const int s = alist[e * kMD + m];
-                    sca[e * kMD + m] = bt * gam * skk[e * kMD + m];
-                    cb[e * kMD + m] = gam * sqk[e * kMD + m];
+                    const int s = alist[m * N + e];
+                    sca[m * N + e] = bt * gam * skk[m * N + e];
+                    cb[m * N + e] = gam * sqk[m * N + e];
                     gam *= dec[s];
                 }
                 sg[(hi & 1) * N + e] = gam;
@@ -560,35 +596,32 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
 #pragma unroll
                 for (int k = 1; k <= kMD; ++k) {
                     if (k > dep) break;
-                    float acc = cb[e * kMD + k - 1];
-                    acc = fmaf(-mrow[0], sca[e * kMD + k - 1], acc);
+                    float acc = cb[(k - 1) * N + e];
+                    acc = fmaf(-mrow[0], sca[(k - 1) * N + e], acc);
 #pragma unroll
                     for (int i = 1; i < k; ++i) {
-                        const int pi = alist[e * kMD + i - 1];
-                        acc = fmaf(-mrow[i], sca[pi * kMD + (k - i - 1)], acc);
+                        const int pi = alist[(i - 1) * N + e];
+                        acc = fmaf(-mrow[i], sca[(k - i - 1) * N + pi], acc);
                     }
                     mrow[k] = acc;
                 }
 #pragma unroll
                 for (int k = 1; k <= kMD; ++k) {
                     if (k > dep) break;
-                    cb[e * kMD + k - 1] = mrow[k];  // own row only: B(t, .) is not read by others
+                    cb[(k - 1) * N + e] = mrow[k];  // own row only: B(t, .) is not read by others
                 }
             }
         };
-        stage_v(g * p.R);
         gates(0);
         named_bar(1, kEpi);
         coefs(0);
-        cp_async_wait_all();
         named_bar(1, kEpi);
         for (int hi = 0; hi < p.R; ++hi) {
             const int h = g * p.R + hi, db = hi & 1, cur = hi & 1;
-            // conv weights of this head's v channel (used by the R pass)
-            const int cv = 2 * p.Hk * kDK + h * kDV + j;
+            // conv weights of this head's v channel (used by the R pass), loaded a head ahead
             float wv[KT];
 #pragma unroll
-            for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wl[(long)cv * K + q]) : 0.f;
+            for (int q = 0; q < KT; ++q) wv[q] = (q < K) ? to_f32(wv_nx[q]) : 0.f;
             if (warp == 0 && lane == 0 && hi + 1 < p.R && tc::mbar_wait(s_free, hi & 1, abort_flag)) {
                 tc::mbar_expect_tx(full, kDV * kDK * 4);  // S0 of the next head over the read one
                 for (int blk = 0; blk < kDK / 32; ++blk)
@@ -600,6 +633,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             backsub(hi);
             // after a timeout the warp keeps meeting the named barriers but does no work
             if (!dead) dead = !__all_sync(kFull, tc::mbar_wait(d_full + db, (hi >> 1) & 1, abort_flag));
+            if (!dead) dead = !__all_sync(kFull, tc::mbar_wait(v_full, hi & 1, abort_flag));
             const float* sbc = sbeta + cur * N;
             const float* sgc = sg + cur * N;
             const float* scbc = scb + cur * N * kMD;
@@ -610,7 +644,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 // Each thread takes whole 8-node chunks (the three warps of a lane quarter
                 // take every third chunk), so every loaded column is used and 8 nodes are in
                 // flight.
-                for (int c = quad; c * 8 < nn; c += 3) {
+                for (int c = quad; c * 8 < nn; c += kQuads) {
                     const int t0 = c * 8;
                     uint32_t ks[8];
                     tmem_ld8(dcol + t0, ks);
@@ -646,13 +680,19 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
             if (warp == 1 && lane == 0 && hi + 1 < p.R && !dead) issue_mma(hi + 1);
             __syncwarp();
             if (hi + 1 < p.R) {
-                stage_v(h + 1);
+                if (tid == 0) {  // the R pass is done with the v rows
+                    tc::mbar_expect_tx(v_full, stage_bytes);
+                    stage_rows(sv, v_full, cv0 + (hi + 1) * kDV);
+                }
+                const int cv = cv0 + (hi + 1) * kDV + j;
+#pragma unroll
+                for (int q = 0; q < KT; ++q) wv_nx[q] = wl[(long)cv * K + min(q, K - 1)];
                 coefs(hi + 1);
             }
             if (!dead) {
                 // pass C: outputs as independent sums over each node's own path; the 8 nodes
                 // of a chunk advance one ancestor level at a time, so their loads overlap
-                for (int c = quad; c * 8 < N; c += 3) {
+                for (int c = quad; c * 8 < N; c += kQuads) {
                     const int t0 = c * 8;
                     uint32_t qs[8];
                     if (t0 < nn) {
@@ -677,7 +717,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
 #pragma unroll
                         for (int uu = 0; uu < 8; ++uu) {
                             const int t = t0 + uu;
-                            if (a < dp[uu]) ot[uu] = fmaf(scbc[t * kMD + a], ubuf[alist[t * kMD + a] * kDV + j], ot[uu]);
+                            if (a < dp[uu]) ot[uu] = fmaf(scbc[a * N + t], ubuf[alist[a * N + t] * kDV + j], ot[uu]);
                         }
                     }
 #pragma unroll
@@ -689,8 +729,7 @@ __global__ void __launch_bounds__(kThr, 1) k_gdn_tc(const GdnTcParams p, const _
                 tc::tc_fence_before();
                 tc::mbar_arrive(d_free + db);
             }
-            cp_async_wait_all();
-            named_bar(1, kEpi);  // coefficients and v rows of the next head visible; R rows free
+            named_bar(1, kEpi);  // coefficients of the next head visible; R rows free
         }
     }
     if (warp == 1 && lane == 0) {  // every MMA has completed before TMEM is freed
@@ -737,24 +776,24 @@ int npad_of(int N) { return (qoff_of(N) + N + 15) / 16 * 16; }
 }  // namespace
 
 bool gdn_tc_supported(int N, int Hk, int Hv, int dk, int dv, int K, ddt_dtype in) {
-    if (dk != kDK || dv != kDV || K < 1 || K > kMaxK || Hv % Hk != 0 || N > kEpi) return false;
+    if (dk != kDK || dv != kDV || K < 1 || K > kMaxK || Hv % Hk != 0 || N > gdn_threads(kMaxK)) return false;
     if (npad_of(N) > 256) return false;
     return gdn_tc_layout(N, npad_of(N), K, in == DDT_BF16 ? 2 : 4).total <= 227 * 1024;
 }
 
 template <typename Tin, typename Tout, int KT>
-static cudaError_t gdn_tc_go_k(const GdnTcParams& prm, const CUtensorMap& map, cudaStream_t st) {
+static cudaError_t gdn_tc_go_k(const GdnTcParams& prm, const CUtensorMap* maps, cudaStream_t st) {
     const size_t smem = gdn_tc_layout(prm.N, prm.NPAD, prm.K, (int)sizeof(Tin)).total;
     cudaError_t e = cudaFuncSetAttribute(k_gdn_tc<Tin, Tout, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_gdn_tc<Tin, Tout, KT><<<counted(dim3(prm.Hk, prm.B, prm.L)), kThr, smem, st>>>(prm, map);
+    k_gdn_tc<Tin, Tout, KT><<<counted(dim3(prm.Hk, prm.B, prm.L)), gdn_threads(KT), smem, st>>>(prm, maps[0], maps[1], maps[2]);
     return cudaGetLastError();
 }
 
 // the common conv width 4 gets its own instance; any other width up to kMaxK the generic one
 template <typename Tin, typename Tout>
-static cudaError_t gdn_tc_go(const GdnTcParams& prm, const CUtensorMap& map, cudaStream_t st) {
-    return prm.K == 4 ? gdn_tc_go_k<Tin, Tout, 4>(prm, map, st) : gdn_tc_go_k<Tin, Tout, kMaxK>(prm, map, st);
+static cudaError_t gdn_tc_go(const GdnTcParams& prm, const CUtensorMap* maps, cudaStream_t st) {
+    return prm.K == 4 ? gdn_tc_go_k<Tin, Tout, 4>(prm, maps, st) : gdn_tc_go_k<Tin, Tout, kMaxK>(prm, maps, st);
 }
 
 cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype in, ddt_dtype out, const void* x,
@@ -776,6 +815,7 @@ cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype 
     prm.NPAD = npad_of(N);
     prm.x = x;
     prm.conv_w = conv_w;
+    prm.wvec = (reinterpret_cast<uintptr_t>(conv_w) & 15) == 0;
     prm.conv_state = conv_state;
     prm.beta = beta;
     prm.decay = decay;
@@ -785,23 +825,44 @@ cudaError_t launch_gdn_tc(int L, int B, int N, int Hk, int Hv, int K, ddt_dtype 
     prm.status = status;
     // committed states as a 2-D fp32 tensor: rows (layer, request, value head, value
     // channel), columns the key channel; boxes of 32 columns x 128 rows
-    CUtensorMap map;
+    CUtensorMap maps[3];
     const cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)L * B * Hv * kDV};
     const cuuint64_t strides[1] = {(cuuint64_t)kDK * 4};
     const cuuint32_t box[2] = {32, (cuuint32_t)kDV};
     const cuuint32_t es[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(S), dims, strides, box, es,
+    if (enc(&maps[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(S), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // x rows (layer, request, node) and conv-state rows (layer, request, tap) as 2-D tensors
+    // of C channels; boxes of 128 channels x all N node rows (or the K - 1 state rows),
+    // unswizzled, so a box lands as the [rows][128] staging layout
+    const size_t esz = in == DDT_BF16 ? 2 : 4;
+    const CUtensorMapDataType dt = in == DDT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const cuuint64_t cstride[1] = {(cuuint64_t)prm.C * esz};
+    const cuuint64_t xdims[2] = {(cuuint64_t)prm.C, (cuuint64_t)L * B * N};
+    const cuuint32_t xbox[2] = {128, (cuuint32_t)N};
+    if (enc(&maps[1], dt, 2, const_cast<void*>(x), xdims, cstride, xbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    maps[2] = maps[1];  // (no conv-state rows to stage when K == 1)
+    if (K > 1) {
+        const cuuint64_t cdims[2] = {(cuuint64_t)prm.C, (cuuint64_t)L * B * (K - 1)};
+        const cuuint32_t cbox[2] = {128, (cuuint32_t)(K - 1)};
+        if (enc(&maps[2], dt, 2, const_cast<void*>(conv_state), cdims, cstride, cbox, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     // status words start at DDT_OK; CTAs only ever write errors into them
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t) * B, st);
     if (e != cudaSuccess) return e;
     const bool ib = in == DDT_BF16, ob = out == DDT_BF16;
-    if (ib && ob) return gdn_tc_go<__nv_bfloat16, __nv_bfloat16>(prm, map, st);
-    if (ib) return gdn_tc_go<__nv_bfloat16, float>(prm, map, st);
-    if (ob) return gdn_tc_go<float, __nv_bfloat16>(prm, map, st);
-    return gdn_tc_go<float, float>(prm, map, st);
+    if (ib && ob) return gdn_tc_go<__nv_bfloat16, __nv_bfloat16>(prm, maps, st);
+    if (ib) return gdn_tc_go<__nv_bfloat16, float>(prm, maps, st);
+    if (ob) return gdn_tc_go<float, __nv_bfloat16>(prm, maps, st);
+    return gdn_tc_go<float, float>(prm, maps, st);
 }
 
 }  // namespace ddt
