@@ -14,8 +14,10 @@
 //   k_walk_lse     grid (units / 8, N, B): one HBM pass over the target logits; each warp
 //                  reduces a 2048-token unit of one row to its max m_u and
 //                  sum_v 2^((l_v - m_u) * s2), s2 = log2(e) / T (fp32: groups of 8 terms,
-//                  pairwise above them, a shuffle tree across the warp).  No block barrier
-//                  and no fp64, so loads of the next warp's unit overlap this one's math.
+//                  pairwise above them, a shuffle tree across the warp).  A full bf16 unit
+//                  takes its max and its finiteness check two entries at a time on the
+//                  packed pairs.  No block barrier and no fp64, so loads of the next warp's
+//                  unit overlap this one's math.
 //   k_walk_sample  grid B: tree checks; warp 0 walks down, merging the visited row's unit
 //                  partials in fp64 and deciding each tried child in fp64; then the CTA
 //                  draws the bonus: a warp scan of the residual unit masses picks the unit,
@@ -107,16 +109,37 @@ __global__ void __launch_bounds__(kSampleThreads) k_walk_lse(const T* __restrict
     for (int j = 0; j < kLanePer / 8; ++j) r[j].load(row, lane * 8 + j * 256, len, vec);
     float mt = -INFINITY;
     int bad = 0;
+    if constexpr (sizeof(T) == 2) {
+        if (len == kSampleUnit) {
+            // a full bf16 unit: packed maxima two entries at a time, and the largest exponent
+            // field of each half (0x7f80 marks Inf or NaN)
+            __nv_bfloat162 m2 = __float2bfloat162_rn(-INFINITY);
+            uint32_t ex = 0;
 #pragma unroll
-    for (int j = 0; j < kLanePer / 8; ++j)
+            for (int j = 0; j < kLanePer / 8; ++j) {
+                const uint32_t ww[4] = {r[j].w.x, r[j].w.y, r[j].w.z, r[j].w.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float x = r[j].at(q);
-            if (lane * 8 + j * 256 + q < len) {
-                if (!finite_f32(x)) bad = 1;
-                mt = fmaxf(mt, x);
+                for (int q = 0; q < 4; ++q) {
+                    ex = __vmaxu2(ex, ww[q] & 0x7f807f80u);
+                    m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&ww[q]));
+                }
             }
+            bad = (ex & 0xffffu) == 0x7f80u || (ex >> 16) == 0x7f80u;
+            mt = fmaxf(__low2float(m2), __high2float(m2));
         }
+    }
+    if (sizeof(T) != 2 || len != kSampleUnit) {
+#pragma unroll
+        for (int j = 0; j < kLanePer / 8; ++j)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float x = r[j].at(q);
+                if (lane * 8 + j * 256 + q < len) {
+                    if (!finite_f32(x)) bad = 1;
+                    mt = fmaxf(mt, x);
+                }
+            }
+    }
     float g[kLanePer / 8];
 #pragma unroll
     for (int j = 0; j < kLanePer / 8; ++j) {
