@@ -151,12 +151,6 @@ __device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
     v[3] = a.w;
 }
 
-// 16-byte global -> shared copy that completes asynchronously (both addresses 16-byte aligned)
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 }  // namespace
 
