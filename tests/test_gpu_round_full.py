@@ -2,7 +2,9 @@
 prefixes ~ U[1024, 32768], 16 attention + 48 GDN layers, bf16) in the configuration the
 bench times, with planted acceptances, checked on samples the oracle can compute one by
 one: every request's tree and walk, sampled attention rows and GDN units, and the commit
-of sampled KV rows, GDN states and conv states."""
+of sampled KV rows, GDN states and conv states.  Run twice: with fp32 attention and GDN
+outputs (parity mode, within 2e-3), and with the bf16 outputs the bench times (within
+2e-3 plus one bf16 rounding, 2^-8 of the vector's largest entry)."""
 import math
 
 import numpy as np
@@ -18,9 +20,11 @@ from tree_speculative_decoding_02_gb300.round import Round
 pytestmark = pytest.mark.gpu
 
 
-def test_full_batched_round_sampled():
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["fp32_out", "bf16_out"])
+def test_full_batched_round_sampled(out_dtype):
     cfg = dict(synth.WORKLOADS[5])
-    r = Round(cfg, device="cuda", workload=5, attn_out_dtype=torch.float32, gdn_out_dtype=torch.float32)
+    r = Round(cfg, device="cuda", workload=5, attn_out_dtype=out_dtype, gdn_out_dtype=out_dtype)
+    tol = TOL if out_dtype == torch.float32 else TOL + 2.0 ** -8
     B, N, D = cfg["B"], r.N, cfg["D"]
     rng = np.random.default_rng(55)
 
@@ -67,7 +71,7 @@ def test_full_batched_round_sampled():
         want = oracle.attn_row(C.f64(a.q[l, b, row, hq]), C.f64(a.k_cache[l, b, g, :P]), C.f64(a.v_cache[l, b, g, :P]),
                                C.f64(a.k_tree[l, b, :n, g]), C.f64(a.v_tree[l, b, :n, g]), anc[b, row], n, scale)
         err = normwise(C.f64(r.attn_o[l, b, row, hq]), want, axes=-1)
-        assert err <= TOL, (l, b, row, hq, err)
+        assert err <= tol, (l, b, row, hq, err)
 
     # GDN: sampled (layer, request, value head), every node
     gi = r.gdn
@@ -76,7 +80,7 @@ def test_full_batched_round_sampled():
         u = oracle.gdn_unit(C.f64(gi.x[l, b]), C.f64(gi.conv_w[l]), cs0[(l, b, h)], C.f64(gi.beta[l, b]),
                             C.f64(gi.decay[l, b]), S0[(l, b, h)][h], par[b], n, cfg["Hk"], cfg["Hv"], h)
         err = normwise(C.f64(r.gdn_o[l, b, :n, h]), u["o"][:n], axes=-1)
-        assert err.max() <= TOL, (l, b, h, err.max())
+        assert err.max() <= tol, (l, b, h, err.max())
 
     # commit: KV rows land at prefix_len + j; the state and conv state follow the path
     src = r.commit["src_row"].cpu().numpy()
