@@ -254,8 +254,8 @@ ddt_status ddt_tree_gdn(int n_layers, int B, int N, int Hk, int Hv, int dk, int 
         return DDT_ERR_INVALID_ARG;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    // head size 128: dense part on the tensor cores (its 16-byte row copies want x and the
-    // conv state 16-byte aligned); other sizes on the CUDA cores
+    // head size 128: dense part on the tensor cores (its TMA row loads want x and the conv
+    // state 16-byte aligned); other sizes on the CUDA cores
     if (gdn_tc_supported(N, Hk, Hv, dk, dv, conv_k, in_dtype) && aligned16(x) && (conv_k == 1 || aligned16(conv_state)))
         e = launch_gdn_tc(n_layers, B, N, Hk, Hv, conv_k, in_dtype, out_dtype, x, conv_w, conv_state, beta, decay, S,
                           parent, n_nodes, o, status, st);
