@@ -101,6 +101,37 @@ def test_walk_nonfinite_flagged():
     assert g["status"].tolist() == [6, 0]
 
 
+def test_walk_bf16_nonfinite_in_packed_rows():
+    """bf16 rows take the packed argmax (two entries a step, and the exponent field's max for
+    the finiteness check): +inf, -inf and NaN in either half of a packed pair, in a full
+    16384-entry chunk and in the ragged last chunk, flag the request; a non-finite entry
+    in a row past the tree and the largest finite bf16 do not, and the clean requests walk
+    as the oracle does."""
+    B, D, V = 8, 3, 16384 + 6181
+    tree, _ = C.tree_from_logits(46, B, D, 300, 3, 8, std=2.0, boost=2.0)
+    tree = {k: np.array(v) for k, v in tree.items()}
+    N = tree["token"].shape[1]
+    tree["n_nodes"][4] = N - 2                                  # the last rows (leaves) dropped
+    tl = synth.target_logits(B, N, V, g=synth.gen(46, 30), dtype=torch.float32)
+    tl[0, 0, 1234] = float("inf")                                # low half of a pair, full chunk
+    tl[1, 1, 4321] = float("-inf")                               # high half of a pair
+    tl[2, 0, V - 5] = float("nan")                               # ragged last chunk
+    tl[3, 2, 16383] = float("nan")                               # last entry of the first chunk
+    tl[4, N - 1, 100] = float("inf")                             # a row past the tree: ignored
+    tl[6, 0, 0] = float("-inf")                                  # the very first entry
+    tl[7, 1, 777] = 3.3895313892515355e38                        # the largest finite bf16
+    tl = tl.to(torch.bfloat16)
+    assert float(tl[7, 1, 777]) == 3.3895313892515355e38
+    g = _walk_gpu(tree, D, tl=tl)
+    assert g["status"].tolist() == [6, 6, 6, 6, 0, 0, 6, 0]
+    clean = [4, 5, 7]
+    sub = {k: v[clean] for k, v in tree.items()}
+    o = oracle.walk(sub["token"], sub["parent"], sub["n_nodes"], D, target_logits=C.f64(tl[clean]))
+    for k in _WALK_KEYS:
+        np.testing.assert_array_equal(g[k][clean], o[k], err_msg=k)
+    assert g["target_argmax"][7][1] == 777
+
+
 def _commit_case(La, Lg, B, budget, D, wl, Pcap_extra=8, dtype=torch.bfloat16, dims=(32, 32, 1, 2)):
     dk, dv, Hk, Hv = dims
     tree, _ = C.tree_from_logits(wl, B, D, 200, 3, budget, std=2.0, boost=0.0)

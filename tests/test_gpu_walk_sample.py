@@ -214,6 +214,35 @@ def test_sample_statuses():
     assert o3["status"][0] == 0 and o3["status"][5] == 0
 
 
+def test_sample_bf16_nonfinite_in_packed_units():
+    """Full 2048-entry bf16 units take their max and finiteness check on packed pairs:
+    +inf, -inf and NaN in either half of a pair, in a full unit and in the ragged last
+    unit, flag the request as the oracle does; a non-finite entry in a row past the tree
+    and the largest finite bf16 do not."""
+    B, D, V = 8, 3, 3 * 2048 + 613
+    tree, _ = C.tree_from_logits(47, B, D, 300, 3, 8, std=2.0, boost=2.0)
+    tree = {k: np.array(v) for k, v in tree.items()}
+    N = tree["token"].shape[1]
+    tree["n_nodes"][4] = N - 2                                  # the last rows (leaves) dropped
+    tl = synth.target_logits(B, N, V, g=synth.gen(47, 30), dtype=torch.float32)
+    tl[0, 0, 2 * 2048 + 10] = float("inf")                       # low half of a pair, full unit
+    tl[1, 1, 2048 + 7] = float("-inf")                           # high half of a pair
+    tl[2, 0, V - 3] = float("nan")                               # ragged last unit
+    tl[3, 0, 1] = float("nan")                                   # first unit, high half
+    tl[4, N - 1, 100] = float("inf")                             # a row past the tree: ignored
+    tl[6, 2, 0] = float("-inf")                                  # the very first entry of a row
+    tl[7, 1, 99] = 3.3895313892515355e38                         # the largest finite bf16
+    tl = tl.to(torch.bfloat16)
+    U = synth.uniforms(B, D + 1, 4, g=synth.gen(47, 32))
+    g = _gpu(tree, D, tl, U, 1.0)
+    o = oracle.walk_sample(tree["token"], tree["parent"], tree["n_nodes"], D, C.f64(tl), U.double().numpy(), 1.0, 4)
+    np.testing.assert_array_equal(g["status"], o["status"])
+    assert g["status"].tolist() == [6, 6, 6, 6, 0, 0, 6, 0]
+    for b in range(B):
+        if o["status"][b] != 0:
+            assert g["n_emitted"][b] == 0 and g["bonus"][b] == -1 and (g["emitted"][b] == -1).all()
+
+
 def test_sample_deterministic_and_graph_safe():
     """Same inputs, same outputs, call after call (no atomics decide anything)."""
     B, D, V, k = 16, 15, 151936, 8
